@@ -1,0 +1,327 @@
+// moe_oracle.cpp -- the CPU oracle for the MoE layer hot path.
+//
+// TEST INFRASTRUCTURE ONLY.  This file is the plain, slow, obviously correct
+// statement of what the GPU library computes.  Only the test suite, the smoke
+// check and the benchmark's CPU-baseline leg may load it.  It shares no source,
+// header, table or helper with the CUDA library, and it includes nothing from
+// it: status codes, activation ids and the BF16 rounding are restated here.
+//
+// Sources (web pages this restates; each function names the passage it follows):
+//  [ORT]   ONNX Runtime PR #33963 "Extend MoEPacked for Bolt ReLU-square routing
+//          and BF16 IQ2 precision": the "Measured CUDA kernel latency" section
+//          (softmax routing over logits or preselected FP32 ids/weights, the
+//          +16/-16 worked case with weights 1/9) and the Description bullets
+//          (ReLU-square experts, SwiGLU default, malformed-route isolation,
+//          BF16 store boundaries with FP32 routing and reduction).
+//  [AFD]   afdEP-comm count-first validation record (JSON): keys .change and
+//          .setup (counts and their prefix sums before the payload moves;
+//          capacity 2048), .correctness_shipped.runner (invalid routes
+//          dummy / duplicate / negative / wide must fail).
+//  [MI300] DeepSeek fleet megakernel REPORT.md, per-op-type table
+//          (MOE_GATE_TOPK, EXPERT_W13_SILU, EXPERT_W2, MOE_COMBINE_RESIDUAL).
+//
+// Precision: every floating-point sum is taken in double (FP64) in the natural
+// index order; BF16 values are produced by one round-to-nearest-even from the
+// double result at the three store boundaries (h, y_perm, out).
+//
+// Parity pins: every function below is pinned by tests that do not re-use it
+// (brute force, closed forms from [ORT], integer-exact analytic cases,
+// invariants).  No function here is "parity unpinned".
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <vector>
+#include <algorithm>
+
+namespace {
+
+// Status codes of the library contract, restated (numeric values are part of
+// the public contract).
+constexpr int ST_OK = 0;
+constexpr int ST_INVALID_ARG = 1;
+constexpr int ST_INVALID_ROUTE = 2;
+constexpr int ST_CAPACITY = 3;
+constexpr int ST_NONFINITE = 4;
+
+constexpr int ACT_SWIGLU = 0;
+constexpr int ACT_RELU2 = 1;
+
+// ---- BF16 <-> double ------------------------------------------------------
+// BF16 = the top 16 bits of an IEEE binary32.  Decoding is exact.
+double bf16_to_double(uint16_t b) {
+    uint32_t u = static_cast<uint32_t>(b) << 16;
+    float f;
+    std::memcpy(&f, &u, 4);
+    return static_cast<double>(f);
+}
+
+// One rounding, to nearest with ties to even, from a double to BF16
+// (8 significant bits, exponent range of binary32, subnormals kept).
+// Written from the number format: scale |d| so that one BF16 ulp becomes 1,
+// round to the nearest integer with ties to even, scale back.
+uint16_t double_to_bf16(double d) {
+    if (std::isnan(d)) return 0x7fc0;
+    const bool neg = std::signbit(d);
+    double a = std::fabs(d);
+    double r;
+    if (a == 0.0) {
+        r = 0.0;
+    } else if (std::isinf(a)) {
+        r = INFINITY;
+    } else {
+        int e;
+        std::frexp(a, &e);             // a = m * 2^e, m in [0.5, 1)
+        // The ulp of a normal BF16 with this exponent is 2^(e-8); BF16
+        // subnormals have the fixed ulp 2^-133.
+        int ulp_exp = e - 8;
+        if (ulp_exp < -133) ulp_exp = -133;
+        double q = std::ldexp(a, -ulp_exp);   // exact (power-of-two scale)
+        double qi = std::floor(q);
+        double frac = q - qi;                 // exact
+        if (frac > 0.5 || (frac == 0.5 && std::fmod(qi, 2.0) != 0.0)) qi += 1.0;
+        r = std::ldexp(qi, ulp_exp);
+        // Largest finite BF16 is (2 - 2^-7) * 2^127.
+        const double max_bf16 = std::ldexp(255.0, 120);
+        if (r > max_bf16) r = INFINITY;
+    }
+    float f = static_cast<float>(neg ? -r : r);   // exact: r has <= 8 bits
+    uint32_t u;
+    std::memcpy(&u, &f, 4);
+    return static_cast<uint16_t>(u >> 16);
+}
+
+double silu(double g) { return g / (1.0 + std::exp(-g)); }
+
+}  // namespace
+
+extern "C" {
+
+uint16_t oracle_bf16_from_double(double d) { return double_to_bf16(d); }
+double oracle_double_from_bf16(uint16_t b) { return bf16_to_double(b); }
+
+// ---- route --------------------------------------------------------------
+// [ORT] "Measured CUDA kernel latency": softmax routing over router logits.
+// Order the experts by (logit descending, index ascending) -- ties go to the
+// lower expert index -- and keep the first k.  The k weights are the softmax
+// of the k selected logits (the full softmax renormalised over the selected
+// experts), so they sum to 1; in the +16/-16 case every weight is 1/9.
+// Non-finite logits are rejected (status 4) before anything is written.
+int oracle_route(int T, int E, int k, const float* logits, int32_t* ids, float* w) {
+    if (T < 0 || E < 1 || k < 1 || k > E) return ST_INVALID_ARG;
+    for (long long i = 0; i < (long long)T * E; ++i)
+        if (!std::isfinite(logits[i])) return ST_NONFINITE;
+    std::vector<int> order(E);
+    for (int t = 0; t < T; ++t) {
+        const float* l = logits + (size_t)t * E;
+        for (int e = 0; e < E; ++e) order[e] = e;
+        std::sort(order.begin(), order.end(), [&](int a, int b) {
+            if (l[a] > l[b]) return true;
+            if (l[a] < l[b]) return false;
+            return a < b;   // equal logits (including -0 == +0): lower index first
+        });
+        const double m = l[order[0]];
+        double z = 0.0;
+        for (int j = 0; j < k; ++j) z += std::exp((double)l[order[j]] - m);
+        for (int j = 0; j < k; ++j) {
+            ids[(size_t)t * k + j] = order[j];
+            w[(size_t)t * k + j] = (float)(std::exp((double)l[order[j]] - m) / z);
+        }
+    }
+    return ST_OK;
+}
+
+// ---- dispatch -----------------------------------------------------------
+// [AFD] .change / .setup: count-first dispatch.  Counts per expert first,
+// their exclusive prefix sums next, and only then the payload rows move, each
+// straight into its expert-contiguous slot.  A pair p = t*k + j is valid when
+// 0 <= id < E and no earlier slot of the same token holds the same id
+// ([AFD] runner: negative / wide / duplicate routes are errors; [ORT]
+// Description: malformed routes are isolated).  Invalid pairs are neither
+// counted nor placed (dest = -1).  The capacity is a per-expert receive bound
+// ([AFD] .setup "capacity 2048"): if any count exceeds it, counts and offsets
+// are still produced but no payload is written.
+// Returns the largest status raised (capacity 3 > invalid route 2).
+int oracle_dispatch(int T, int E, int k, int H, int capacity,
+                    const int32_t* ids, const uint16_t* x,
+                    int32_t* counts, int32_t* offsets, int32_t* dest,
+                    int32_t* sorted_pair, uint16_t* x_perm) {
+    if (T < 0 || E < 1 || k < 1 || H < 1) return ST_INVALID_ARG;
+    const long long R = (long long)T * k;
+    int status = ST_OK;
+    std::vector<char> valid(R, 0);
+    for (int t = 0; t < T; ++t)
+        for (int j = 0; j < k; ++j) {
+            const int32_t e = ids[(size_t)t * k + j];
+            bool ok = (e >= 0 && e < E);
+            for (int jj = 0; jj < j && ok; ++jj)
+                if (ids[(size_t)t * k + jj] == e) ok = false;
+            valid[(size_t)t * k + j] = ok;
+            if (!ok) status = std::max(status, ST_INVALID_ROUTE);
+        }
+    for (int e = 0; e < E; ++e) counts[e] = 0;
+    for (long long p = 0; p < R; ++p)
+        if (valid[p]) counts[ids[p]] += 1;
+    offsets[0] = 0;
+    for (int e = 0; e < E; ++e) offsets[e + 1] = offsets[e] + counts[e];
+    for (int e = 0; e < E; ++e)
+        if (counts[e] > capacity) status = std::max(status, ST_CAPACITY);
+    if (status == ST_CAPACITY) return status;
+    std::vector<int32_t> fill(E, 0);
+    for (long long p = 0; p < R; ++p) {
+        if (!valid[p]) { dest[p] = -1; continue; }
+        const int32_t e = ids[p];
+        const int32_t d = offsets[e] + fill[e];
+        fill[e] += 1;
+        dest[p] = d;
+        sorted_pair[d] = (int32_t)p;
+        const long long t = p / k;
+        std::memcpy(x_perm + (size_t)d * H, x + (size_t)t * H, sizeof(uint16_t) * H);
+    }
+    return status;
+}
+
+// ---- expert FFN ---------------------------------------------------------
+// [MI300] EXPERT_W13_SILU and [ORT] Description (ReLU-square experts, SwiGLU
+// default).  One row of the up projection with the activation:
+//   SwiGLU: W13 rows 0..I-1 are the gate, rows I..2I-1 the up projection;
+//           h[n] = bf16( silu(g_n) * u_n ),  silu(g) = g / (1 + exp(-g)).
+//   ReLU^2: W1 has I rows; h[n] = bf16( max(a_n, 0)^2 ).
+// Dot products are summed over h = 0..H-1 in double.
+void oracle_expert_up(int H, int I, int act, const uint16_t* x_row,
+                      const uint16_t* w13_e, uint16_t* h_row) {
+    auto dot = [&](const uint16_t* wrow) {
+        double s = 0.0;
+        for (int c = 0; c < H; ++c) s += bf16_to_double(x_row[c]) * bf16_to_double(wrow[c]);
+        return s;
+    };
+    for (int n = 0; n < I; ++n) {
+        if (act == ACT_SWIGLU) {
+            const double g = dot(w13_e + (size_t)n * H);
+            const double u = dot(w13_e + (size_t)(I + n) * H);
+            h_row[n] = double_to_bf16(silu(g) * u);
+        } else {
+            const double a = dot(w13_e + (size_t)n * H);
+            const double r = a > 0.0 ? a : 0.0;
+            h_row[n] = double_to_bf16(r * r);
+        }
+    }
+}
+
+// [MI300] EXPERT_W2: the down projection of one row, accumulated in double
+// into acc[0..H-1] (not rounded, so shared experts can be summed first).
+void oracle_expert_down_acc(int H, int I, const uint16_t* h_row,
+                            const uint16_t* w2_e, double* acc) {
+    for (int c = 0; c < H; ++c) {
+        const uint16_t* wrow = w2_e + (size_t)c * I;
+        double s = 0.0;
+        for (int n = 0; n < I; ++n) s += bf16_to_double(h_row[n]) * bf16_to_double(wrow[n]);
+        acc[c] += s;
+    }
+}
+
+// One routed row end to end: h (BF16) and y (BF16, one rounding).
+void oracle_expert_row(int H, int I, int act, const uint16_t* x_row,
+                       const uint16_t* w13_e, const uint16_t* w2_e,
+                       uint16_t* h_row, uint16_t* y_row) {
+    oracle_expert_up(H, I, act, x_row, w13_e, h_row);
+    std::vector<double> acc(H, 0.0);
+    oracle_expert_down_acc(H, I, h_row, w2_e, acc.data());
+    for (int c = 0; c < H; ++c) y_row[c] = double_to_bf16(acc[c]);
+}
+
+// Shared (always-on) experts for one token row: each shared expert s gives
+// h_s = act(x W13s[s]^T) (BF16), the S down projections are summed in double
+// in s order and rounded once.  h_shared_row holds S*Is values (s-major).
+void oracle_shared_row(int H, int Is, int S, int act, const uint16_t* x_row,
+                       const uint16_t* ws13, const uint16_t* ws2,
+                       uint16_t* h_shared_row, uint16_t* y_shared_row) {
+    const size_t up = (act == ACT_SWIGLU) ? 2 * (size_t)Is : (size_t)Is;
+    std::vector<double> acc(H, 0.0);
+    for (int s = 0; s < S; ++s) {
+        uint16_t* hs = h_shared_row + (size_t)s * Is;
+        oracle_expert_up(H, Is, act, x_row, ws13 + (size_t)s * up * H, hs);
+        oracle_expert_down_acc(H, Is, hs, ws2 + (size_t)s * H * Is, acc.data());
+    }
+    for (int c = 0; c < H; ++c) y_shared_row[c] = double_to_bf16(acc[c]);
+}
+
+// The whole grouped expert FFN over the expert-contiguous buckets:
+// rows [offsets[e], offsets[e+1]) of x_perm go through expert e.
+// W13 is [E][up][H] (up = 2I for SwiGLU, I for ReLU^2), W2 is [E][H][I].
+// Shared experts (S > 0) run over every row of x into y_shared [T][H].
+void oracle_expert_ffn(int T, int H, int E, int I, int act, int S, int Is,
+                       const uint16_t* x_perm, const int32_t* offsets,
+                       const uint16_t* w13, const uint16_t* w2,
+                       const uint16_t* x, const uint16_t* ws13, const uint16_t* ws2,
+                       uint16_t* h, uint16_t* y_perm,
+                       uint16_t* h_shared, uint16_t* y_shared) {
+    const size_t up = (act == ACT_SWIGLU) ? 2 * (size_t)I : (size_t)I;
+    for (int e = 0; e < E; ++e)
+        for (int r = offsets[e]; r < offsets[e + 1]; ++r)
+            oracle_expert_row(H, I, act, x_perm + (size_t)r * H,
+                              w13 + (size_t)e * up * H, w2 + (size_t)e * H * I,
+                              h + (size_t)r * I, y_perm + (size_t)r * H);
+    if (S > 0)
+        for (int t = 0; t < T; ++t)
+            oracle_shared_row(H, Is, S, act, x + (size_t)t * H, ws13, ws2,
+                              h_shared + (size_t)t * S * Is, y_shared + (size_t)t * H);
+}
+
+// ---- combine ------------------------------------------------------------
+// [MI300] MOE_COMBINE_RESIDUAL (the weighted combine; the residual add is not
+// part of this layer) and [ORT] "FP32 final routing/reduction": for token t,
+// out[t] = bf16( sum_{j<k} w[t,j] * y_perm[dest[t,j]] + y_shared[t] ), summed
+// in j order, then the shared term.  Pairs with dest < 0 (invalid routes)
+// contribute nothing.
+void oracle_combine_row(int k, int H, const uint16_t* y_perm, const int32_t* dest_t,
+                        const float* w_t, const uint16_t* y_shared_t, uint16_t* out_t) {
+    for (int c = 0; c < H; ++c) {
+        double s = 0.0;
+        for (int j = 0; j < k; ++j) {
+            if (dest_t[j] < 0) continue;
+            s += (double)w_t[j] * bf16_to_double(y_perm[(size_t)dest_t[j] * H + c]);
+        }
+        if (y_shared_t) s += bf16_to_double(y_shared_t[c]);
+        out_t[c] = double_to_bf16(s);
+    }
+}
+
+void oracle_combine(int T, int k, int H, const uint16_t* y_perm, const int32_t* dest,
+                    const float* w, const uint16_t* y_shared, uint16_t* out) {
+    for (int t = 0; t < T; ++t)
+        oracle_combine_row(k, H, y_perm, dest + (size_t)t * k, w + (size_t)t * k,
+                           y_shared ? y_shared + (size_t)t * H : nullptr,
+                           out + (size_t)t * H);
+}
+
+// ---- whole layer --------------------------------------------------------
+// route (or take preselected ids/weights) -> dispatch -> expert FFN -> combine.
+// ids/w/counts/offsets/dest/sorted_pair/x_perm/h/y_perm/h_shared/y_shared are
+// caller-provided scratch so the tests can inspect every stage.
+int oracle_layer(int T, int H, int E, int k, int I, int act, int S, int Is, int capacity,
+                 const float* logits, const int32_t* ids_in, const float* w_in,
+                 const uint16_t* x, const uint16_t* w13, const uint16_t* w2,
+                 const uint16_t* ws13, const uint16_t* ws2,
+                 int32_t* ids, float* w, int32_t* counts, int32_t* offsets,
+                 int32_t* dest, int32_t* sorted_pair, uint16_t* x_perm,
+                 uint16_t* h, uint16_t* y_perm, uint16_t* h_shared, uint16_t* y_shared,
+                 uint16_t* out) {
+    const size_t R = (size_t)T * k;
+    if (logits) {
+        int st = oracle_route(T, E, k, logits, ids, w);
+        if (st != ST_OK) return st;
+    } else {
+        std::memcpy(ids, ids_in, R * sizeof(int32_t));
+        std::memcpy(w, w_in, R * sizeof(float));
+    }
+    int st = oracle_dispatch(T, E, k, H, capacity, ids, x, counts, offsets, dest,
+                             sorted_pair, x_perm);
+    if (st == ST_CAPACITY) return st;
+    oracle_expert_ffn(T, H, E, I, act, S, Is, x_perm, offsets, w13, w2, x, ws13, ws2,
+                      h, y_perm, h_shared, y_shared);
+    oracle_combine(T, k, H, y_perm, dest, w, S > 0 ? y_shared : nullptr, out);
+    return st;
+}
+
+}  // extern "C"

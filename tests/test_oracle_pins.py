@@ -1,0 +1,396 @@
+"""Pins of the CPU oracle against facts that do not come from the oracle itself.
+
+Each test checks one oracle function against something fixed independently:
+the worked decode case printed on the ONNX Runtime MoEPacked page
+(golden/decode_closed_form.json), brute force on tiny inputs, closed forms,
+integer-exact analytic cases, invariants, and library routines (Python's
+sorted, numpy float64 matmul, torch's float->bf16 conversion).  The cases are
+chosen so that a dropped term, a wrong sign or index, a transposed operand or a
+wrong tie rule fails at least one of them.
+"""
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+from mixture_experts_routing_router_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def torch_bf16_bits_from_float(vals):
+    t = torch.tensor(vals, dtype=torch.float32).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def bits_to_f64(a):
+    return (np.asarray(a, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def rand_bf16(rng, shape, std=1.0):
+    f = (rng.standard_normal(shape) * std).astype(np.float32)
+    return torch_bf16_bits_from_float(f.reshape(-1)).reshape(shape)
+
+
+# --------------------------------------------------------------------------
+# BF16 rounding
+# --------------------------------------------------------------------------
+def test_bf16_rounding_matches_torch_on_float_values(oracle_mod):
+    rng = np.random.default_rng(1)
+    vals = np.concatenate([rng.standard_normal(4000) * s for s in (1e-40, 1e-20, 1e-3, 1.0, 1e5, 1e30)])
+    vals = vals.astype(np.float32)
+    vals = np.concatenate([vals, np.array([0.0, -0.0, 1.0, -1.0, 3.0e38, -3.0e38, 1e-45], np.float32)])
+    want = torch_bf16_bits_from_float(vals)
+    got = np.array([oracle_mod.bf16_from_double(float(v)) for v in vals], np.uint16)
+    assert np.array_equal(got, want)
+
+
+def test_bf16_rounding_single_rounding_from_double(oracle_mod):
+    # 1 + 2^-8 is a tie between 1 and 1 + 2^-7: ties go to even (1.0)
+    assert oracle_mod.bf16_from_double(1.0 + 2.0 ** -8) == 0x3F80
+    # 1 + 3*2^-8 is a tie between 1+2^-7 (odd) and 1+2^-6 (even)
+    assert oracle_mod.bf16_from_double(1.0 + 3 * 2.0 ** -8) == 0x3F82
+    # just above the tie: must round up.  Rounding to float first would lose
+    # the 2^-40 and then tie to even (1.0) -- the wrong answer.
+    assert oracle_mod.bf16_from_double(1.0 + 2.0 ** -8 + 2.0 ** -40) == 0x3F81
+    assert oracle_mod.bf16_from_double(-(1.0 + 2.0 ** -8 + 2.0 ** -40)) == 0xBF81
+    # overflow threshold: (2 - 2^-8) * 2^127 rounds to inf, just below stays finite
+    assert oracle_mod.bf16_from_double(math.ldexp(2 - 2.0 ** -8, 127)) == 0x7F80
+    assert oracle_mod.bf16_from_double(math.ldexp(2 - 2.0 ** -7, 127)) == 0x7F7F
+    # subnormal: smallest bf16 subnormal is 2^-133; half of it ties to 0
+    assert oracle_mod.bf16_from_double(2.0 ** -133) == 0x0001
+    assert oracle_mod.bf16_from_double(2.0 ** -134) == 0x0000
+    assert oracle_mod.bf16_from_double(1.5 * 2.0 ** -133) == 0x0002
+    assert oracle_mod.bf16_from_double(-0.0) == 0x8000
+
+
+# --------------------------------------------------------------------------
+# route
+# --------------------------------------------------------------------------
+def brute_topk(row, k):
+    return sorted(range(len(row)), key=lambda e: (-float(row[e]), e))[:k]
+
+
+@pytest.mark.parametrize("E,k", [(1, 1), (4, 2), (7, 3), (16, 2), (16, 16), (33, 5)])
+def test_route_bruteforce_with_ties(oracle_mod, E, k):
+    rng = np.random.default_rng(E * 100 + k)
+    T = 64
+    logits = rng.integers(-2, 3, size=(T, E)).astype(np.float32)   # many ties
+    st, ids, w = oracle_mod.route(logits, k)
+    assert st == 0
+    for t in range(T):
+        assert list(ids[t]) == brute_topk(logits[t], k)
+    assert np.all(np.abs(w.astype(np.float64).sum(1) - 1.0) <= 1e-6)
+    # weights follow the logit order
+    assert np.all(np.diff(w, axis=1) <= 0)
+
+
+def test_route_negative_zero_ties_positive_zero(oracle_mod):
+    logits = np.array([[-0.0, 0.0, -1.0, 0.0]], np.float32)
+    st, ids, w = oracle_mod.route(logits, 3)
+    assert st == 0 and list(ids[0]) == [0, 1, 3]
+    assert np.all(w == np.float32(1.0 / 3))
+
+
+def test_route_closed_form_two_experts(oracle_mod):
+    # logits 0 and -ln 3: softmax over the pair is exactly (3/4, 1/4) in the reals
+    logits = np.array([[-5.0, 0.0, -math.log(3.0), -7.0]], np.float32)
+    st, ids, w = oracle_mod.route(logits, 2)
+    assert st == 0 and list(ids[0]) == [1, 2]
+    assert abs(w[0, 0] - 0.75) < 1e-7 and abs(w[0, 1] - 0.25) < 1e-7
+    # the weights are renormalised over the selected experts: unselected logits
+    # do not change them
+    logits2 = logits.copy()
+    logits2[0, 0] = -0.5
+    logits2[0, 3] = -0.6
+    _, ids3, w3 = oracle_mod.route(logits2, 2)
+    assert list(ids3[0]) == [1, 0]
+
+
+def test_route_decode_closed_form_golden(oracle_mod):
+    g = json.load(open(os.path.join(GOLDEN, "decode_closed_form.json")))
+    E, k = g["experts"], g["top_k"]
+    want_w = np.float32(g["selected_weight_num"] / g["selected_weight_den"])
+    for rows in g["rows"]:
+        for kind in ("shared", "distinct"):
+            wl = synth.WORKLOADS[f"decode_{rows}_{kind}"]
+            lg = synth.make_logits(wl).numpy()
+            assert set(np.unique(lg)) == {g["selected_logit"], g["other_logit"]}
+            st, ids, w = oracle_mod.route(lg, k)
+            assert st == 0
+            for r, s in enumerate(synth.decode_route_sets(wl)):
+                assert list(ids[r]) == sorted(s)
+            assert np.all(w == want_w)
+            if rows == 16:
+                assert ids.size == g["routes_at_16_rows"]
+
+
+@pytest.mark.parametrize("bad", [float("nan"), float("inf"), float("-inf")])
+def test_route_rejects_nonfinite(oracle_mod, bad):
+    logits = np.zeros((3, 8), np.float32)
+    logits[2, 5] = bad
+    st, _, _ = oracle_mod.route(logits, 2)
+    assert st == oracle_mod.ST_NONFINITE
+
+
+# --------------------------------------------------------------------------
+# dispatch
+# --------------------------------------------------------------------------
+def naive_placement(ids, E):
+    """Expert-major enumeration: walk experts in order and, for each, the pairs
+    in ascending p.  A different algorithm from counting + scan + scatter."""
+    flat = ids.reshape(-1)
+    dest = np.full(flat.size, -1, np.int64)
+    slot = 0
+    for e in range(E):
+        for p in range(flat.size):
+            if flat[p] == e:
+                dest[p] = slot
+                slot += 1
+    return dest
+
+
+@pytest.mark.parametrize("T,E,k", [(1, 1, 1), (5, 4, 4), (64, 16, 2), (37, 33, 5), (128, 8, 3)])
+def test_dispatch_bruteforce_and_invariants(oracle_mod, T, E, k):
+    rng = np.random.default_rng(T + E + k)
+    ids = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    H = 24
+    x = rng.integers(0, 65535, size=(T, H)).astype(np.uint16)
+    st, counts, offsets, dest, sp, xp = oracle_mod.dispatch(ids, x, E, T)
+    assert st == 0
+    assert counts.sum() == T * k
+    assert np.array_equal(counts, np.bincount(ids.reshape(-1), minlength=E))
+    assert offsets[0] == 0 and offsets[E] == T * k
+    assert np.array_equal(np.diff(offsets), counts)
+    assert np.array_equal(dest, naive_placement(ids, E))
+    assert np.array_equal(np.sort(dest), np.arange(T * k))           # bijection
+    assert np.array_equal(sp[dest], np.arange(T * k))                  # inverse
+    for e in range(E):                                                 # stable buckets
+        toks = sp[offsets[e]:offsets[e + 1]] // k
+        assert np.all(np.diff(toks) > 0)
+    for j in range(k):                                                 # round trip
+        assert np.array_equal(xp[dest.reshape(T, k)[:, j]], x)
+
+
+def test_dispatch_decode_closed_form(oracle_mod):
+    for rows in (1, 8, 16):
+        for kind in ("shared", "distinct"):
+            wl = synth.WORKLOADS[f"decode_{rows}_{kind}"]
+            ids = np.array(synth.decode_route_sets(wl), np.int32)
+            x = np.zeros((rows, 8), np.uint16)
+            st, counts, offsets, dest, sp, xp = oracle_mod.dispatch(ids, x, wl.experts, wl.cap)
+            assert st == 0
+            want = np.zeros(wl.experts, np.int32)
+            if kind == "shared":
+                want[:9] = rows
+            else:
+                want[:9 * rows] = 1
+            assert np.array_equal(counts, want)
+
+
+def test_dispatch_capacity_exceeded_moves_no_payload(oracle_mod):
+    T, E, k = 10, 4, 2
+    ids = np.tile(np.array([[0, 1]], np.int32), (T, 1))
+    x = np.ones((T, 8), np.uint16)
+    st, counts, offsets, dest, sp, xp = oracle_mod.dispatch(ids, x, E, 9)
+    assert st == oracle_mod.ST_CAPACITY
+    assert list(counts) == [10, 10, 0, 0] and offsets[-1] == 20
+    assert np.all(dest == -7) and np.all(xp == 0)
+    # exactly at capacity is fine
+    st, *_ = oracle_mod.dispatch(ids, x, E, 10)
+    assert st == 0
+
+
+@pytest.mark.parametrize("kind", ["negative", "wide", "duplicate", "dummy"])
+def test_dispatch_invalid_routes(oracle_mod, kind):
+    T, E, k = 6, 8, 3
+    ids = np.array([[0, 1, 2], [3, 4, 5], [6, 7, 0], [1, 2, 3], [4, 5, 6], [7, 0, 1]], np.int32)
+    bad = ids.copy()
+    if kind == "negative":
+        bad[2, 1] = -3
+    elif kind == "wide":
+        bad[2, 1] = E
+    elif kind == "duplicate":
+        bad[2, 1] = bad[2, 0]
+    else:   # a dummy (-1) route
+        bad[2, 1] = -1
+    x = np.arange(T * 8, dtype=np.uint16).reshape(T, 8)
+    st, counts, offsets, dest, sp, xp = oracle_mod.dispatch(bad, x, E, T)
+    assert st == oracle_mod.ST_INVALID_ROUTE
+    assert counts.sum() == T * k - 1
+    assert dest[2 * k + 1] == -1
+    valid = np.ones(T * k, bool)
+    valid[2 * k + 1] = False
+    assert np.array_equal(np.sort(dest[valid]), np.arange(T * k - 1))
+
+
+# --------------------------------------------------------------------------
+# expert FFN
+# --------------------------------------------------------------------------
+def np_dense_mlp(xb, w13b, w2b, act):
+    """Independent dense MLP in numpy float64 (matmul order differs from the
+    oracle's sequential sums), with torch doing the BF16 rounding."""
+    x = bits_to_f64(xb)
+    w13 = bits_to_f64(w13b)
+    w2 = bits_to_f64(w2b)
+    I = w2.shape[1]
+    a = x @ w13.T
+    if act == 0:
+        g, u = a[:, :I], a[:, I:]
+        hv = g / (1.0 + np.exp(-g)) * u
+    else:
+        hv = np.maximum(a, 0.0) ** 2
+    h = torch.tensor(hv).to(torch.bfloat16)      # float64 -> bf16, one rounding
+    hb = h.view(torch.int16).numpy().view(np.uint16)
+    y = torch.tensor(bits_to_f64(hb) @ w2.T).to(torch.bfloat16)
+    return hb, y.view(torch.int16).numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("act", [0, 1])
+def test_ffn_single_expert_is_dense_mlp(oracle_mod, act):
+    rng = np.random.default_rng(7 + act)
+    T, H, I = 40, 96, 56
+    up = 2 * I if act == 0 else I
+    x = rand_bf16(rng, (T, H))
+    w13 = rand_bf16(rng, (1, up, H), 1 / math.sqrt(H))
+    w2 = rand_bf16(rng, (1, H, I), 1 / math.sqrt(I))
+    offsets = np.array([0, T], np.int32)
+    h, y, _, _ = oracle_mod.expert_ffn(x, offsets, w13, w2, act)
+    hn, yn = np_dense_mlp(x, w13[0], w2[0], act)
+    hd = np.abs(bits_to_f64(h) - bits_to_f64(hn))
+    # matmul order can flip a BF16 rounding of h by one ulp, rarely
+    assert np.mean(h != hn) < 0.01
+    assert np.all(hd <= np.abs(bits_to_f64(hn)) * 2 ** -7 + 1e-30)
+    yd = np.abs(bits_to_f64(y) - bits_to_f64(yn))
+    assert yd.max() <= 1e-2 * np.abs(bits_to_f64(yn)).max()
+    # gate and up are not interchangeable (catches a swapped half)
+    if act == 0:
+        w13s = np.concatenate([w13[:, I:], w13[:, :I]], axis=1)
+        h2, _, _, _ = oracle_mod.expert_ffn(x, offsets, w13s, w2, act)
+        assert np.mean(h2 != h) > 0.5
+
+
+def test_ffn_identical_experts_give_dense_mlp_for_any_routing(oracle_mod):
+    rng = np.random.default_rng(11)
+    T, H, I, E, k = 24, 64, 40, 6, 3
+    w13_1 = rand_bf16(rng, (1, 2 * I, H), 1 / 8)
+    w2_1 = rand_bf16(rng, (1, H, I), 1 / 6)
+    w13 = np.repeat(w13_1, E, axis=0)
+    w2 = np.repeat(w2_1, E, axis=0)
+    x = rand_bf16(rng, (T, H))
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    o = oracle_mod.layer(x, w13, w2, 0, k, T, logits=logits)
+    assert o["status"] == 0
+    h1, y1, _, _ = oracle_mod.expert_ffn(x, np.array([0, T], np.int32), w13_1, w2_1, 0)
+    assert np.array_equal(o["out"], y1)
+
+
+def relu2_analytic_case(rng, T, E, k, H, I):
+    """x, W in {-1, 0, 1}; each token's k experts tie at logit 1 (others 0),
+    so every weight is exactly 1/k.  Integers stay small enough that every
+    value is exact until the one BF16 rounding torch applies."""
+    x = rng.integers(-1, 2, size=(T, H))
+    w1 = rng.integers(-1, 2, size=(E, I, H))
+    w2 = rng.integers(-1, 2, size=(E, H, I))
+    sets = [sorted(rng.permutation(E)[:k].tolist()) for _ in range(T)]
+    logits = np.zeros((T, E), np.float32)
+    for t, s in enumerate(sets):
+        logits[t, s] = 1.0
+    return x, w1, w2, sets, logits
+
+
+def bf16_of_exact(vals):
+    """Round exact integers/dyadics to BF16 by torch (float64 -> bf16 is one
+    rounding for these values since they are exact in float64)."""
+    t = torch.tensor(np.asarray(vals, np.float64)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("k", [2, 4])
+def test_layer_relu2_analytic_exact(oracle_mod, k):
+    rng = np.random.default_rng(100 + k)
+    T, E, H, I = 16, 8, 40, 24
+    x, w1, w2, sets, logits = relu2_analytic_case(rng, T, E, k, H, I)
+    xb, w1b, w2b = (bf16_of_exact(a) for a in (x, w1, w2))
+    o = oracle_mod.layer(xb, w1b, w2b, 1, k, T, logits=logits)
+    assert o["status"] == 0
+    assert np.all(o["w"] == np.float32(1.0 / k))
+    want = np.zeros((T, H), np.uint16)
+    for t in range(T):
+        acc = [Fraction(0)] * H
+        for e in sets[t]:
+            a = w1[e] @ x[t]                                 # exact ints
+            hq = bits_to_f64(bf16_of_exact(np.maximum(a, 0) ** 2))
+            yv = bits_to_f64(bf16_of_exact(w2[e] @ hq))      # exact sum of ints
+            for c in range(H):
+                acc[c] += Fraction(yv[c]) / k
+        want[t] = bf16_of_exact([float(a) for a in acc])     # dyadic: exact in f64
+    assert np.array_equal(o["out"], want)
+
+
+def test_shared_experts_sum_before_rounding(oracle_mod):
+    rng = np.random.default_rng(5)
+    H, Is, S = 32, 16, 2
+    x = rand_bf16(rng, (1, H))
+    ws13 = rand_bf16(rng, (S, 2 * Is, H), 0.3)
+    ws2 = rand_bf16(rng, (S, H, Is), 0.3)
+    hs, ys = oracle_mod.shared_row(x[0], ws13, ws2, 0)
+    # independent: both shared experts as one expert with intermediate S*Is
+    # (gate rows of both, then up rows of both; down weights side by side)
+    w13cat = np.concatenate([ws13[0, :Is], ws13[1, :Is], ws13[0, Is:], ws13[1, Is:]])[None]
+    w2cat = np.concatenate([ws2[0], ws2[1]], axis=1)[None]
+    h1, y1, _, _ = oracle_mod.expert_ffn(x, np.array([0, 1], np.int32), w13cat, w2cat, 0)
+    assert np.array_equal(hs, h1[0])
+    assert np.array_equal(ys, y1[0])
+
+
+# --------------------------------------------------------------------------
+# combine
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("k", [1, 2, 4, 8])
+def test_combine_identity_experts_return_x(oracle_mod, k):
+    rng = np.random.default_rng(k)
+    T, E, H = 30, 12, 48
+    x = rand_bf16(rng, (T, H))
+    ids = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    st, counts, offsets, dest, sp, xp = oracle_mod.dispatch(ids, x, E, T)
+    w = np.full((T, k), 1.0 / k, np.float32)          # powers of two: exact
+    out = oracle_mod.combine(xp, dest, w)
+    assert np.array_equal(out, x)
+    # shared term is added: x + x = 2x exactly
+    out2 = oracle_mod.combine(xp, dest, w, y_shared=x)
+    assert np.array_equal(bits_to_f64(out2), 2 * bits_to_f64(x))
+
+
+def test_combine_weights_are_applied_per_slot(oracle_mod):
+    # y rows 1.0 and 2.0 with weights 0.75 / 0.25 -> 1.25 exactly; swapped -> 1.75
+    y = bf16_of_exact([[1.0] * 4, [2.0] * 4])
+    out = oracle_mod.combine(y, np.array([0, 1], np.int32), np.array([[0.75, 0.25]], np.float32))
+    assert np.all(bits_to_f64(out) == 1.25)
+    out = oracle_mod.combine(y, np.array([1, 0], np.int32), np.array([[0.75, 0.25]], np.float32))
+    assert np.all(bits_to_f64(out) == 1.75)
+    # an invalid pair (dest -1) contributes nothing
+    out = oracle_mod.combine(y, np.array([1, -1], np.int32), np.array([[0.75, 0.25]], np.float32))
+    assert np.all(bits_to_f64(out) == 1.5)
+
+
+# --------------------------------------------------------------------------
+# layer
+# --------------------------------------------------------------------------
+def test_layer_internal_routing_equals_preselected(oracle_mod):
+    wl = synth.WORKLOADS["tiny"].with_(tokens=16)
+    d = synth.make_inputs(wl, unit_scale=True)
+    x = synth.bf16_bits(d["x"])
+    w13 = synth.bf16_bits(d["w13"])
+    w2 = synth.bf16_bits(d["w2"])
+    lg = d["logits"].numpy()
+    a = oracle_mod.layer(x, w13, w2, 0, wl.top_k, wl.cap, logits=lg)
+    st, ids, w = oracle_mod.route(lg, wl.top_k)
+    b = oracle_mod.layer(x, w13, w2, 0, wl.top_k, wl.cap, ids_in=ids, w_in=w)
+    assert a["status"] == b["status"] == 0
+    assert np.array_equal(a["out"], b["out"])
+    assert np.abs(bits_to_f64(a["out"])).max() > 0.05          # unit-scale twin is not ~0
