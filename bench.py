@@ -1,0 +1,401 @@
+"""Benchmark of the MoE layer hot path on one GB300 (or N data-parallel replicas).
+
+One step = one moe_layer call over the large workload: 16384 tokens, hidden
+7168, 256 experts top-8, intermediate 2048, SwiGLU, Zipf(1.2)-biased router
+logits -- route, count-first dispatch, grouped expert FFN and combine.  Inputs
+(22.5 GB of weights, 235 MB of x) are larger than the 129 MB L2, so no flush
+is needed between steps.  Under torchrun every rank runs its own replica on its
+own 16384 tokens (weak scaling, no data-path collective); the elapsed time is
+the max over ranks.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
+prints one JSON line.  --impl reference times the CPU oracle (the program the
+GPU path is checked against) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from mixture_experts_routing_router_gb300 import synth  # noqa: E402
+
+WORKLOAD = "large"
+METRIC = "MoE layer tokens/s; dispatch+combine HBM GB/s; expert GEMM TFLOP/s vs peak"
+
+
+def describe(wl):
+    return (f"{wl.name}: {wl.tokens} tokens, hidden {wl.hidden}, {wl.experts} experts top-{wl.top_k}, "
+            f"intermediate {wl.inter}, {'SwiGLU' if wl.act == 0 else 'ReLU^2'}, "
+            f"router logits N(0,1) + Zipf({wl.zipf_s}) expert bias, W ~ N(0,0.02), x ~ N(0,1), seed 0")
+
+
+def algorithmic(wl, counts=None):
+    """Bytes / FLOPs the method itself must move or compute (no padding)."""
+    T, H, E, k, I = wl.tokens, wl.hidden, wl.experts, wl.top_k, wl.inter
+    R = T * k
+    up = wl.up
+    d = {
+        "dispatch_bytes": T * H * 2 + R * H * 2 + R * 8 + E * 8,
+        "combine_bytes": R * H * 2 + T * H * 2 + R * 8,
+        "up_flops": 2 * R * H * up + 2 * T * H * wl.shared * wl.shared_up,
+        "down_flops": 2 * R * I * H + 2 * T * wl.shared * wl.shared_inter * H,
+    }
+    if counts is not None:
+        nz = int((counts > 0).sum())
+        d["nonempty_experts"] = nz
+        d["up_bytes"] = nz * up * H * 2 + R * H * 2 + R * I * 2
+        d["down_bytes"] = nz * H * I * 2 + R * I * 2 + R * H * 2
+    return d
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm_gbs=d["hbm_gbs"], bf16_tflops=d["bf16_tflops"],
+                    bf16_tflops_sustained=d.get("bf16_tflops_sustained", d["bf16_tflops"]), source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+def kernel_source_sha():
+    h = hashlib.sha256()
+    for f in ("common.cuh", "gemm.cu"):
+        h.update(open(os.path.join(ROOT, "mixture_experts_routing_router_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic():
+    """DRAM bytes per launch of the up-projection GEMM from the committed ncu
+    summary, only while the kernel source is the one that was captured."""
+    p = os.path.join(ROOT, "profiles", "gemm_up_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    if d.get("kernel_source_sha") != kernel_source_sha():
+        return None
+    return d.get("dram_bytes_per_launch_full_size")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples during the timed region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.lines = []
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def max_over_ranks(value: float, world: int, device) -> float:
+    """The largest value over all ranks (timing only; no data-path collective)."""
+    if world <= 1:
+        return value
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (baseline leg and the reference arm)
+# ---------------------------------------------------------------------------
+def oracle_sample(wl, g_logits_host, x_host, tokens, weight_device, seed=0):
+    """Time the oracle on `tokens` tokens of the workload: routing of those
+    tokens, their k expert rows (up projection, activation, down projection)
+    and the combine.  Weights of the touched experts are regenerated from
+    their seeded streams.  Returns (seconds, tokens)."""
+    import oracle
+    from mixture_experts_routing_router_gb300.synth import bf16_bits, expert_weights
+    _, ids, w = oracle.route(g_logits_host[tokens], wl.top_k)
+    need = sorted(set(ids.reshape(-1).tolist()))
+    wts = {}
+    for e in need:
+        a, b = expert_weights(wl, e, seed, weight_device)
+        wts[e] = (bf16_bits(a), bf16_bits(b))
+    t0 = time.perf_counter()
+    _, ids, w = oracle.route(g_logits_host[tokens], wl.top_k)
+    for i, t in enumerate(tokens):
+        ys = []
+        for j in range(wl.top_k):
+            e = int(ids[i, j])
+            _, y = oracle.expert_row(x_host[t], wts[e][0], wts[e][1], wl.act)
+            ys.append(y)
+        oracle.combine_row(np.stack(ys), np.arange(wl.top_k, dtype=np.int32), w[i])
+    return time.perf_counter() - t0, len(tokens)
+
+
+def run_reference(args, wl, world, rank):
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    logits = synth.make_logits(wl, 0, dev).cpu().numpy()
+    x = synth.bf16_bits(synth.normal((wl.tokens, wl.hidden), 1.0, 0, "x", dev))
+    rng = np.random.default_rng(0)
+    per_step = 1
+    times, toks = [], 0
+    for step in range(args.warmup + args.steps):
+        tokens = sorted(rng.choice(wl.tokens, per_step, replace=False).tolist())
+        s, n = oracle_sample(wl, logits, x, tokens, dev)
+        if step >= args.warmup:
+            times.append(s)
+            toks += n
+    total = sum(times)
+    value = toks / total
+    sample = (f"{per_step} random token(s) per step of the {wl.tokens}-token batch: routing, the top-{wl.top_k} "
+              f"expert rows (FP64 sums) and the combine; single-threaded")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": describe(wl), "tokens_per_step": per_step},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+def run_native(args, wl, world, rank, local):
+    from mixture_experts_routing_router_gb300 import native as N
+    N.lib()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.Stream(device=dev)
+    g = synth.make_inputs(wl, seed=rank, device=dev)
+    shape = N.shape_of(wl)
+    ws = N.workspace(shape, dev)
+    T, H, E, k, I = wl.tokens, wl.hidden, wl.experts, wl.top_k, wl.inter
+    R = T * k
+    out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    kernels_per_layer = 6 + (2 if wl.shared else 0)
+
+    def layer():
+        N.moe_layer(shape, g["logits"], None, None, g["x"], g["w13"], g["w2"], g.get("ws13"), g.get("ws2"),
+                    out, ws, stream)
+
+    # ---- headline: K whole-layer steps ---------------------------------------
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            layer()
+    stream.synchronize()
+    st = N.moe_status_read(ws, stream)
+    if st != N.MOE_OK:
+        raise RuntimeError(f"device status {st} after warm-up")
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for _ in range(args.steps):
+                layer()
+            ev1.record(stream)
+        ev1.synchronize()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    elapsed = ev0.elapsed_time(ev1) / 1e3
+    elapsed = max_over_ranks(elapsed, world, dev)
+    tokens_per_s = world * T * args.steps / elapsed
+
+    # ---- per-stage times (same stream, events between the stage calls) --------
+    ids = torch.empty(T, k, dtype=torch.int32, device=dev)
+    w = torch.empty(T, k, dtype=torch.float32, device=dev)
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    dest = torch.empty(R, dtype=torch.int32, device=dev)
+    sp = torch.empty(R, dtype=torch.int32, device=dev)
+    x_perm = torch.empty(R, H, dtype=torch.bfloat16, device=dev)
+    h = torch.empty(R, I, dtype=torch.bfloat16, device=dev)
+    y_perm = torch.empty(R, H, dtype=torch.bfloat16, device=dev)
+    y_sh = torch.empty(T, H, dtype=torch.bfloat16, device=dev) if wl.shared else None
+    names = ["route", "dispatch", "expert_up", "expert_down", "combine"]
+    reps = max(3, min(args.steps, 20))
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(reps)]
+    with torch.cuda.stream(stream):
+        for r in range(reps + 2):
+            e = evs[r - 2] if r >= 2 else None
+            if e: e[0].record(stream)
+            N.moe_route(shape, g["logits"], ids, w, ws, stream)
+            if e: e[1].record(stream)
+            N.moe_dispatch(shape, g["x"], ids, counts, offsets, dest, sp, x_perm, ws, stream)
+            if e: e[2].record(stream)
+            N.moe_expert_up(shape, x_perm, offsets, g["w13"], g["x"], g.get("ws13"), h, ws, stream)
+            if e: e[3].record(stream)
+            N.moe_expert_down(shape, h, offsets, g["w2"], g.get("ws2"), y_perm, y_sh, ws, stream)
+            if e: e[4].record(stream)
+            N.moe_combine(shape, y_perm, dest, w, y_sh, out, ws, stream)
+            if e: e[5].record(stream)
+    stream.synchronize()
+    stage_ms = {n: statistics.median(evs[r][i].elapsed_time(evs[r][i + 1]) for r in range(reps))
+                for i, n in enumerate(names)}
+    st = N.moe_status_read(ws, stream)
+    if st != N.MOE_OK:
+        raise RuntimeError(f"device status {st} after stage timing")
+    cnt = counts.cpu().numpy()
+    alg = algorithmic(wl, cnt)
+
+    # ---- end to end through the C-ABI with host buffers -----------------------
+    x_host = g["x"].cpu().pin_memory()
+    lg_host = g["logits"].cpu().pin_memory()
+    out_host = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
+    x_d = torch.empty_like(g["x"])
+    lg_d = torch.empty_like(g["logits"])
+    e2e_steps = max(3, min(args.steps, 10))
+    with torch.cuda.stream(stream):
+        for r in range(e2e_steps + 1):
+            if r == 1:
+                stream.synchronize()
+                barrier(world)
+                t0 = time.perf_counter()
+            x_d.copy_(x_host, non_blocking=True)
+            lg_d.copy_(lg_host, non_blocking=True)
+            N.moe_layer(shape, lg_d, None, None, x_d, g["w13"], g["w2"], g.get("ws13"), g.get("ws2"), out, ws,
+                        stream)
+            out_host.copy_(out, non_blocking=True)
+        stream.synchronize()
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / e2e_steps, world, dev)
+    e2e = {"value": world * T / e2e_s, "unit": "tokens/s",
+           "h2d_bytes_per_step": x_host.numel() * 2 + lg_host.numel() * 4,
+           "d2h_bytes_per_step": out_host.numel() * 2}
+
+    peaks = load_peaks()
+    up_s = stage_ms["expert_up"] / 1e3
+    achieved = alg["up_flops"] / up_s / 1e12
+    peak = peaks["bf16_tflops_sustained"]
+    dc_s = (stage_ms["dispatch"] + stage_ms["combine"]) / 1e3
+    dc_gbs = (alg["dispatch_bytes"] + alg["combine_bytes"]) / dc_s / 1e9
+    gemm_tflops = (alg["up_flops"] + alg["down_flops"]) / ((stage_ms["expert_up"] + stage_ms["expert_down"]) / 1e3) / 1e12
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        rng = np.random.default_rng(0)
+        toks = sorted(rng.choice(T, args.cpu_tokens, replace=False).tolist())
+        secs, n = oracle_sample(wl, g["logits"].cpu().numpy(), synth.bf16_bits(g["x"]), toks, dev, seed=rank)
+        cpu = {"value": n / secs, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+               "sample": f"{n} random tokens of the {T}-token batch: routing, their top-{k} expert rows with FP64 "
+                         f"sums, and the combine ({secs:.1f} s single-threaded)"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * elapsed / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": describe(wl), "tokens_per_gpu": T, "global_tokens": world * T,
+                       "parallelism": f"dp{world} (independent replicas)",
+                       "l2": "inputs larger than L2 (22.5 GB weights, 235 MB x, 1.9 GB x_perm): no flush"},
+            "roofline": {"kernel": "grouped_gemm_kernel<SwiGLU> (expert up projection)", "bound": "tensor",
+                         "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                         "peak_source": f"{peaks['source']} bf16_tflops_sustained",
+                         "traffic": ncu_traffic()},
+            "dispatch_combine_gbs": dc_gbs, "dispatch_combine_hbm_frac": dc_gbs / peaks["hbm_gbs"],
+            "gemm_tflops": gemm_tflops, "gemm_frac": gemm_tflops / peak,
+            "stages_ms": stage_ms, "algorithmic": alg,
+            "e2e": e2e, "gpu_launches": kernels_per_layer * args.steps,
+            "clocks": clk.summary(), "cpu_baseline": cpu,
+            "kernel_source_sha": kernel_source_sha(),
+        }
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--workload", default=WORKLOAD, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--cpu-tokens", type=int, default=24)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be at least 3")
+    wl = synth.WORKLOADS[args.workload]
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        return run_reference(args, wl, world, rank)
+    return run_native(args, wl, world, rank, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

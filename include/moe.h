@@ -1,0 +1,199 @@
+/*
+ * moe.h -- C ABI of libmoe.so, the single-GPU MoE layer hot path for GB300 (sm_103a).
+ *
+ * The layer (ONNX Runtime PR #33963 "Extend MoEPacked for Bolt ReLU-square routing
+ * and BF16 IQ2 precision", Description and "Measured CUDA kernel latency"): router
+ * logits -> softmax top-k routing (or caller-preselected expert ids with FP32
+ * weights) -> count-first dispatch of token rows into expert-contiguous buckets
+ * (afdEP-comm count-first validation record, keys .change and .setup) -> the
+ * grouped expert FFN with SwiGLU (the default) or ReLU-square experts in BF16 with
+ * FP32 accumulation -> the weighted combine back to token order (DeepSeek fleet
+ * megakernel REPORT.md, MOE_GATE_TOPK / EXPERT_W13_SILU / EXPERT_W2 /
+ * MOE_COMBINE_RESIDUAL rows of the per-op table).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Pointers named "device" must be device memory of the current CUDA device;
+ *    the caller owns every buffer.  The library never allocates or frees memory.
+ *  - BF16 tensors are passed as uint16_t bit patterns.  All tensors are
+ *    row-major and contiguous: a row of x, x_perm, y_perm, y_shared and out has
+ *    `hidden` elements, a row of h has `inter` elements.
+ *  - Device pointers must be 16-byte aligned; the workspace 256-byte aligned.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every call
+ *    only enqueues work on it: no host synchronisation, no allocation, so a
+ *    sequence of calls can be captured in a CUDA graph.  The one exception is
+ *    moe_status_read, which synchronises the stream.
+ *  - Errors come in two tiers.  (1) Host-detectable errors (bad shape, null or
+ *    misaligned pointers, small workspace) are returned at once and nothing is
+ *    launched.  (2) Errors only the device can see -- an invalid route, a
+ *    bucket over capacity, non-finite logits, a bounded wait that ran out --
+ *    are folded into a status word in the workspace with an atomic max of the
+ *    code and read back by moe_status_read.  After a device-side error the
+ *    call's outputs are unspecified, but no kernel ever reads or writes outside
+ *    the buffers described here.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum moe_status {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,    /* host: bad shape, null/misaligned pointer, small workspace */
+    MOE_ERR_INVALID_ROUTE = 2,  /* device: an id < 0, an id >= experts, or a duplicate id inside a token */
+    MOE_ERR_CAPACITY = 3,       /* device: some expert received more than `capacity` pairs */
+    MOE_ERR_NONFINITE = 4,      /* device: a NaN or infinite router logit */
+    MOE_ERR_TIMEOUT = 5,        /* device: a bounded wait inside a kernel gave up */
+    MOE_ERR_CUDA = 6,           /* host: a CUDA runtime/driver call failed (launch, tensor map) */
+    MOE_ERR_UNSUPPORTED = 7,    /* host: a shape this build does not handle */
+    MOE_ERR_INTERNAL = 8
+} moe_status;
+
+typedef enum moe_act {
+    MOE_ACT_SWIGLU = 0,  /* h = silu(x W_gate^T) * (x W_up^T); W13 rows [0,I) gate, [I,2I) up */
+    MOE_ACT_RELU2 = 1    /* h = max(x W1^T, 0)^2; W13 has I rows */
+} moe_act;
+
+/* Shape of one layer call.
+ *   tokens T >= 1; hidden H, multiple of 8; experts E in [1, 1024];
+ *   top_k k in [1, min(E, 32)]; inter I, multiple of 8 (expert intermediate);
+ *   shared S >= 0 always-on shared experts of intermediate shared_inter
+ *   (multiple of 8 when S > 0); capacity >= 1: the most pairs one expert may
+ *   receive (a receive-buffer bound, as "capacity 2048" in the afdEP-comm
+ *   record's .setup; it is not a drop policy); act: a moe_act value.
+ * Derived: R = T*k routed pairs; up = 2I (SwiGLU) or I (ReLU^2). */
+typedef struct moe_shape {
+    int32_t tokens;
+    int32_t hidden;
+    int32_t experts;
+    int32_t top_k;
+    int32_t inter;
+    int32_t shared;
+    int32_t shared_inter;
+    int32_t capacity;
+    int32_t act;
+} moe_shape;
+
+/* Bytes of device workspace that every call below needs for this shape (the
+ * moe_layer figure, which covers the others).  Host only, synchronous. */
+MOE_API moe_status moe_workspace_size(const moe_shape* shape, size_t* bytes);
+
+/* Zero the workspace's status word and counters.  Call once after allocating
+ * a workspace (or allocate it zero-filled).  Enqueued on `stream`. */
+MOE_API moe_status moe_workspace_init(void* ws, size_t ws_bytes, void* stream);
+
+/* Routing (ONNX Runtime PR #33963, "Measured CUDA kernel latency": internal
+ * softmax routing over router logits).
+ *   logits   device f32 [T, E]  router logits
+ *   topk_ids device i32 [T, k]  out: the k experts with the largest logits,
+ *                               in descending logit order; equal logits
+ *                               (-0 == +0 included) go to the lower index
+ *   topk_w   device f32 [T, k]  out: softmax over the k selected logits
+ *                               (sums to 1; the +16/-16 case gives 1/9 each)
+ * Device error: MOE_ERR_NONFINITE if any logit is NaN or infinite. */
+MOE_API moe_status moe_route(const moe_shape* shape, const float* logits, int32_t* topk_ids,
+                     float* topk_w, void* ws, size_t ws_bytes, void* stream);
+
+/* Count-first dispatch (afdEP-comm count-first record, .change: per-expert
+ * counts and their prefix sums come before the payload rows move).
+ *   x           device bf16 [T, H]
+ *   topk_ids    device i32 [T, k]   expert of pair p = t*k + j
+ *   counts      device i32 [E]      out: valid pairs per expert
+ *   offsets     device i32 [E+1]    out: exclusive scan of counts; offsets[E] = valid pairs
+ *   dest        device i32 [T*k]    out: slot of pair p in the expert-contiguous order
+ *                                   (-1 for an invalid pair); stable: inside a bucket,
+ *                                   pairs keep ascending p
+ *   sorted_pair device i32 [T*k]    out: sorted_pair[dest[p]] = p
+ *   x_perm      device bf16 [T*k, H] out: x_perm[dest[p]] = x[p / k]
+ * A pair is invalid when its id is < 0 or >= E, or equals an id earlier in the
+ * same token (afdEP-comm runner: negative / wide / duplicate / dummy routes);
+ * invalid pairs are neither counted nor written and raise MOE_ERR_INVALID_ROUTE.
+ * If a count exceeds `capacity`, counts and offsets are still written,
+ * MOE_ERR_CAPACITY is raised and no payload (dest, sorted_pair, x_perm) moves. */
+MOE_API moe_status moe_dispatch(const moe_shape* shape, const uint16_t* x, const int32_t* topk_ids,
+                        int32_t* counts, int32_t* offsets, int32_t* dest, int32_t* sorted_pair,
+                        uint16_t* x_perm, void* ws, size_t ws_bytes, void* stream);
+
+/* Expert up projection with the fused activation (DeepSeek fleet REPORT.md,
+ * EXPERT_W13_SILU; ONNX Runtime PR #33963, ReLU-square experts).
+ *   x_perm  device bf16 [T*k, H]  rows [offsets[e], offsets[e+1]) belong to expert e
+ *   offsets device i32 [E+1]      as written by moe_dispatch
+ *   w13     device bf16 [E, up, H]  (nn.Linear [out, in] layout per expert)
+ *   h       device bf16 [T*k, I]  out: h = bf16(act(x_perm W13[e]^T)), FP32 accumulation;
+ *                                 rows past offsets[E] are not written
+ *   x, ws13 device bf16 [T, H], [S, shared_up, H]: shared experts (NULL when S == 0);
+ *           their activations go to the workspace for moe_expert_down. */
+MOE_API moe_status moe_expert_up(const moe_shape* shape, const uint16_t* x_perm, const int32_t* offsets,
+                         const uint16_t* w13, const uint16_t* x, const uint16_t* ws13,
+                         uint16_t* h, void* ws, size_t ws_bytes, void* stream);
+
+/* Expert down projection (DeepSeek fleet REPORT.md, EXPERT_W2).
+ *   h        device bf16 [T*k, I]   from moe_expert_up
+ *   w2       device bf16 [E, H, I]
+ *   y_perm   device bf16 [T*k, H]   out: y_perm[r] = bf16(h[r] W2[e]^T), FP32 accumulation
+ *   ws2      device bf16 [S, H, shared_inter] (NULL when S == 0)
+ *   y_shared device bf16 [T, H]     out (S > 0): bf16(sum_s h_s W2s[s]^T), summed over s
+ *                                   in FP32 and rounded once; NULL when S == 0.
+ * moe_expert_up must have run on the same workspace first when S > 0. */
+MOE_API moe_status moe_expert_down(const moe_shape* shape, const uint16_t* h, const int32_t* offsets,
+                           const uint16_t* w2, const uint16_t* ws2, uint16_t* y_perm,
+                           uint16_t* y_shared, void* ws, size_t ws_bytes, void* stream);
+
+/* moe_expert_up followed by moe_expert_down. */
+MOE_API moe_status moe_expert_ffn(const moe_shape* shape, const uint16_t* x_perm, const int32_t* offsets,
+                          const uint16_t* w13, const uint16_t* w2,
+                          const uint16_t* x, const uint16_t* ws13, const uint16_t* ws2,
+                          uint16_t* h, uint16_t* y_perm, uint16_t* y_shared,
+                          void* ws, size_t ws_bytes, void* stream);
+
+/* Weighted combine back to token order (DeepSeek fleet REPORT.md,
+ * MOE_COMBINE_RESIDUAL without the residual; ONNX Runtime PR #33963, "FP32
+ * final routing/reduction"):
+ *   out[t] = bf16( sum_{j<k} topk_w[t,j] * y_perm[dest[t*k+j]]  +  y_shared[t] )
+ * summed in FP32 in j order, then the shared term; pairs with dest < 0 are skipped.
+ *   y_perm device bf16 [T*k, H]; dest device i32 [T*k]; topk_w device f32 [T, k];
+ *   y_shared device bf16 [T, H] or NULL; out device bf16 [T, H]. */
+MOE_API moe_status moe_combine(const moe_shape* shape, const uint16_t* y_perm, const int32_t* dest,
+                       const float* topk_w, const uint16_t* y_shared, uint16_t* out,
+                       void* ws, size_t ws_bytes, void* stream);
+
+/* The whole layer: route (when logits != NULL) or take preselected ids_in /
+ * w_in (device i32 [T,k] / f32 [T,k], used when logits == NULL), then dispatch,
+ * expert FFN and combine, with every intermediate in the workspace.  Given the
+ * ids and weights moe_route returns, the output is bitwise the same either way
+ * (ONNX Runtime PR #33963: internal and preselected routing give bitwise-equal
+ * outputs).  out: device bf16 [T, H]. */
+MOE_API moe_status moe_layer(const moe_shape* shape, const float* logits, const int32_t* ids_in,
+                     const float* w_in, const uint16_t* x, const uint16_t* w13,
+                     const uint16_t* w2, const uint16_t* ws13, const uint16_t* ws2,
+                     uint16_t* out, void* ws, size_t ws_bytes, void* stream);
+
+/* Synchronise `stream`, return in *device_status the largest status code raised
+ * by kernels on this workspace since the last read, and clear it. */
+MOE_API moe_status moe_status_read(void* ws, void* stream, moe_status* device_status);
+
+/* A static, human-readable name for a status code. */
+MOE_API const char* moe_status_string(moe_status status);
+
+/* A description of the last host-side failure (MOE_ERR_CUDA, MOE_ERR_UNSUPPORTED,
+ * MOE_ERR_INVALID_ARG) raised by a call on this host thread, e.g. the CUDA error
+ * name of a failed launch; "" when none.  The pointer stays valid until the next
+ * call on the same thread. */
+MOE_API const char* moe_last_error_message(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

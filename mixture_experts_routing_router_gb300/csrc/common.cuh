@@ -1,0 +1,260 @@
+// common.cuh -- shared definitions of the libmoe.so CUDA sources (sm_103a only):
+// the workspace layout, the device status word, bounded waits, and thin inline-PTX
+// wrappers for mbarrier, TMA (cp.async.bulk.tensor) and tcgen05 (MMA / TMEM).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+#include "../../include/moe.h"
+
+#if defined(__CUDA_ARCH__) && (__CUDA_ARCH__ < 1000)
+#error "libmoe targets sm_103a (Blackwell tcgen05/TMEM); build with -gencode arch=compute_103a,code=sm_103a"
+#endif
+
+namespace moe {
+
+// ---------------------------------------------------------------------------
+// Workspace.  A caller-owned device buffer; regions are 1 KiB aligned.
+// The first 4 KiB hold the header below; the count kernel's look-back flags,
+// the per-pair ranks and the shared-expert activations follow (needed by the
+// stage calls); the whole-layer intermediates come last (moe_layer only).
+// ---------------------------------------------------------------------------
+struct WsHeader {
+    int status;             // sticky: atomicMax of every device-raised moe_status
+    int timeout_site;       // which bounded wait gave up (diagnostic)
+    unsigned tile_counter;  // dynamic tile ids of the count kernel (reset per dispatch)
+    int cap_exceeded;       // this dispatch's capacity verdict (written by the count kernel)
+};
+
+constexpr int kCountChunk = 1024;      // pairs per count tile (one 256-thread block)
+constexpr int kCountThreads = 256;
+constexpr size_t kAlign = 1024;
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+struct WsLayout {
+    size_t hdr, flags, rank, h_shared;        // stage regions
+    size_t stage_end;                         // bytes the stage calls need
+    size_t counts, offsets, ids, w, dest, sorted_pair, x_perm, h, y_perm, y_shared;
+    size_t total;                             // bytes moe_layer needs
+    int count_tiles;
+};
+
+inline WsLayout ws_layout(const moe_shape& s) {
+    WsLayout L{};
+    const size_t T = (size_t)s.tokens, H = (size_t)s.hidden, E = (size_t)s.experts;
+    const size_t R = T * (size_t)s.top_k, I = (size_t)s.inter;
+    L.count_tiles = (int)((R + kCountChunk - 1) / kCountChunk);
+    size_t o = 0;
+    L.hdr = o;          o = align_up(o + 4096, kAlign);
+    L.flags = o;        o = align_up(o + (size_t)L.count_tiles * E * 8, kAlign);
+    L.rank = o;         o = align_up(o + R * 4, kAlign);
+    L.h_shared = o;     o = align_up(o + T * (size_t)s.shared * (size_t)s.shared_inter * 2, kAlign);
+    L.stage_end = o;
+    L.counts = o;       o = align_up(o + E * 4, kAlign);
+    L.offsets = o;      o = align_up(o + (E + 1) * 4, kAlign);
+    L.ids = o;          o = align_up(o + R * 4, kAlign);
+    L.w = o;            o = align_up(o + R * 4, kAlign);
+    L.dest = o;         o = align_up(o + R * 4, kAlign);
+    L.sorted_pair = o;  o = align_up(o + R * 4, kAlign);
+    L.x_perm = o;       o = align_up(o + R * H * 2, kAlign);
+    L.h = o;            o = align_up(o + R * I * 2, kAlign);
+    L.y_perm = o;       o = align_up(o + R * H * 2, kAlign);
+    L.y_shared = o;     o = align_up(o + (s.shared > 0 ? T * H * 2 : 0), kAlign);
+    L.total = o;
+    return L;
+}
+
+// Bounded waits give up after this long and raise MOE_ERR_TIMEOUT.
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;   // 2 s
+
+// Where a bounded wait gave up (WsHeader::timeout_site).
+enum TimeoutSite : int {
+    kSiteNone = 0, kSiteLookback = 1, kSiteGemmProducer = 2, kSiteGemmMma = 3, kSiteGemmEpilogue = 4,
+};
+
+// ---------------------------------------------------------------------------
+// Device helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void raise_status(WsHeader* h, int code) { atomicMax(&h->status, code); }
+
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// 64-bit release store / acquire load at GPU scope (the look-back flags).
+__device__ __forceinline__ void st_release_u64(unsigned long long* p, unsigned long long v) {
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" :: "l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// ---- mbarrier ---------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    return ok != 0;
+}
+// Wait until the phase with parity `parity` of barrier `bar` has completed.
+// Gives up (returns false) when *abort is set by another role of the CTA, or
+// after kWaitLimitNs, in which case it sets *abort itself.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 31u) == 0u) {
+            if (*abort) return false;
+            if (globaltimer_ns() - t0 > kWaitLimitNs) { *abort = 1; return false; }
+        }
+    }
+}
+
+// ---- TMA --------------------------------------------------------------------
+// 2-D tiled bulk tensor load global -> shared, completion counted on `bar`.
+// (x, y) = (inner element index, row index); x * 2 bytes is a multiple of 16.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, uint32_t bar, int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];"
+        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y) : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
+    asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
+}
+
+// ---- tcgen05 / TMEM -----------------------------------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                 :: "r"(dst_smem), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+// Arrive once on `bar` when every tcgen05 op issued so far by this thread is done.
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 :: "r"(bar) : "memory");
+}
+// D[tmem] (+)= A[smem] * B[smem]^T, BF16 inputs, FP32 accumulator.
+__device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        :: "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate) : "memory");
+}
+// 32 consecutive FP32 columns of this warp's 32 TMEM lanes (one lane per thread).
+__device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptor of a K-major tile with 128-byte swizzle:
+// rows of 64 BF16 (128 B), 8-row swizzle atoms of 1 KiB stacked densely
+// (stride byte offset 1 KiB); the tile starts on a 1 KiB boundary.
+__device__ __forceinline__ uint64_t sdesc_k_sw128(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);       // bits  0-13: start address >> 4
+    d |= (uint64_t)1u << 16;                        // bits 16-29: leading byte offset (unused here)
+    d |= (uint64_t)(1024u >> 4) << 32;              // bits 32-45: stride byte offset >> 4
+    d |= (uint64_t)1u << 46;                        // bits 46-47: descriptor version 1
+    d |= (uint64_t)2u << 61;                        // bits 61-63: 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor, kind::f16: BF16 A and B (both K-major), FP32 D, M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+    return (1u << 4)                               // D format: F32
+         | (1u << 7)                               // A format: BF16
+         | (1u << 10)                              // B format: BF16
+         | ((uint32_t)(N >> 3) << 17)              // N >> 3
+         | ((uint32_t)(M >> 4) << 24);             // M >> 4
+}
+
+// ---------------------------------------------------------------------------
+// Host-side launchers (one per translation unit); all return cudaError_t of the launch.
+// ---------------------------------------------------------------------------
+cudaError_t launch_route(const moe_shape& s, const float* logits, int32_t* ids, float* w,
+                         WsHeader* hdr, cudaStream_t st);
+cudaError_t launch_count(const moe_shape& s, const int32_t* ids, int32_t* counts, int32_t* offsets,
+                         int32_t* rank, unsigned long long* flags, int count_tiles,
+                         WsHeader* hdr, cudaStream_t st);
+cudaError_t launch_scatter(const moe_shape& s, const uint16_t* x, const int32_t* ids,
+                           const int32_t* offsets, const int32_t* rank, int32_t* dest,
+                           int32_t* sorted_pair, uint16_t* x_perm, WsHeader* hdr, cudaStream_t st);
+cudaError_t launch_combine(const moe_shape& s, const uint16_t* y_perm, const int32_t* dest,
+                           const float* w, const uint16_t* y_shared, uint16_t* out, cudaStream_t st);
+
+// Grouped GEMM problem (one launch): for every group g and row r of the group,
+// out[row0(g) + r, g*out_group_col + n] = epilogue( sum_seg sum_k A[row0(g)+r, seg*a_seg_col + k]
+//                                                   * B[g*b_group_rows + seg*b_seg_row + n', k] )
+enum GemmMode : int { kGemmSwiGLU = 0, kGemmReLU2 = 1, kGemmPlain = 2 };
+struct GemmProblem {
+    int mode;
+    const void* a; long long a_rows; long long a_cols;    // A [a_rows, a_cols] bf16
+    const void* b; long long b_rows; long long b_cols;    // B [b_rows, b_cols] bf16
+    const int32_t* offsets;                               // [G+1] row bounds, or null
+    int groups;
+    int rows_all;                                         // rows per group when offsets == null
+    int K, nseg, a_seg_col, b_seg_row;
+    int N;                                                // output columns per group
+    int b_group_rows;
+    int up_off;                                           // SwiGLU: rows from gate to up half
+    void* out; long long ldo; int out_group_col;
+};
+// Returns MOE_OK, MOE_ERR_CUDA (tensor map / launch) or MOE_ERR_UNSUPPORTED.
+moe_status launch_grouped_gemm(const GemmProblem& p, WsHeader* hdr, cudaStream_t st);
+
+int device_sm_count();
+
+// Record a host-side failure description for moe_last_error_message (this thread).
+void set_error(const char* fmt, ...);
+void clear_error();
+
+}  // namespace moe

@@ -1,0 +1,108 @@
+// route.cu -- K1, softmax top-k routing: one warp per token.
+//
+// ONNX Runtime PR #33963 ("Measured CUDA kernel latency"): the operator routes
+// internally by softmax over FP32 router logits; the selected weights of the
+// +16/-16 case are 1/9.  DeepSeek fleet REPORT.md (optimisation step 1): top-k
+// as k rounds of a wave-wide max; here a 32-lane warp.
+//
+// Selection is keyed on the logits themselves (softmax is monotone, and keying
+// on rounded probabilities could create false ties): k rounds, each a warp-wide
+// argmax under the order "larger logit first, then lower expert index", so
+// -0 == +0 and every other equality goes to the lower index.  The weights are
+// the softmax over the k selected logits (the full softmax renormalised over
+// the selection), computed in FP32 with the max subtracted.
+#include "common.cuh"
+
+#include <climits>
+
+namespace moe {
+namespace {
+
+__device__ __forceinline__ bool better(float av, int ai, float bv, int bi) {
+    // a ranks before b; bi == INT_MAX marks "nothing yet"
+    return bi == INT_MAX || av > bv || (av == bv && ai < bi);
+}
+
+// EPL = logits per lane (E <= 32 * EPL); lane l holds experts l, l+32, ...
+template <int EPL>
+__global__ void __launch_bounds__(256)
+route_kernel(int T, int E, int k, const float* __restrict__ logits, int32_t* __restrict__ ids,
+             float* __restrict__ w, WsHeader* hdr) {
+    const int lane = threadIdx.x & 31;
+    const int gwarp = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+    const int nwarps = (int)((gridDim.x * blockDim.x) >> 5);
+    for (int t = gwarp; t < T; t += nwarps) {
+        const float* row = logits + (size_t)t * E;
+        float v[EPL];
+        uint32_t taken = 0;   // bit i: slot i already selected or past E
+        bool bad = false;
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+            const int e = lane + 32 * i;
+            float x = -INFINITY;
+            if (e < E) {
+                x = __ldg(row + e);
+                if (!isfinite(x)) { bad = true; x = -INFINITY; }
+            } else {
+                taken |= 1u << i;
+            }
+            v[i] = x;
+        }
+        if (__any_sync(0xffffffffu, bad) && lane == 0) raise_status(hdr, MOE_ERR_NONFINITE);
+
+        float sel_v = 0.f, m = 0.f;
+        int sel_i = 0;
+        for (int j = 0; j < k; ++j) {
+            float bv = 0.f;
+            int bi = INT_MAX;
+#pragma unroll
+            for (int i = 0; i < EPL; ++i)
+                if (!((taken >> i) & 1u) && better(v[i], lane + 32 * i, bv, bi)) { bv = v[i]; bi = lane + 32 * i; }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+                const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+                if (oi != INT_MAX && better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+            }
+            // k <= E, so a winner always exists: every lane holds the same (bv, bi)
+            if (lane == (bi & 31)) taken |= 1u << (bi >> 5);
+            if (j == 0) m = bv;
+            if (lane == j) { sel_v = bv; sel_i = bi; }
+        }
+        const float ex = (lane < k) ? expf(sel_v - m) : 0.f;
+        float z = ex;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+        if (lane < k) {
+            ids[(size_t)t * k + lane] = sel_i;
+            w[(size_t)t * k + lane] = ex / z;
+        }
+    }
+}
+
+template <int EPL>
+cudaError_t launch_epl(const moe_shape& s, const float* logits, int32_t* ids, float* w, WsHeader* hdr,
+                       cudaStream_t st) {
+    const int warps_per_block = 8;
+    long long blocks = ((long long)s.tokens + warps_per_block - 1) / warps_per_block;
+    const long long cap = (long long)device_sm_count() * 8;
+    if (blocks > cap) blocks = cap;
+    route_kernel<EPL><<<(unsigned)blocks, 32 * warps_per_block, 0, st>>>(s.tokens, s.experts, s.top_k,
+                                                                          logits, ids, w, hdr);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_route(const moe_shape& s, const float* logits, int32_t* ids, float* w, WsHeader* hdr,
+                         cudaStream_t st) {
+    const int E = s.experts;
+    if (E <= 32) return launch_epl<1>(s, logits, ids, w, hdr, st);
+    if (E <= 64) return launch_epl<2>(s, logits, ids, w, hdr, st);
+    if (E <= 128) return launch_epl<4>(s, logits, ids, w, hdr, st);
+    if (E <= 256) return launch_epl<8>(s, logits, ids, w, hdr, st);
+    if (E <= 512) return launch_epl<16>(s, logits, ids, w, hdr, st);
+    return launch_epl<32>(s, logits, ids, w, hdr, st);
+}
+
+}  // namespace moe

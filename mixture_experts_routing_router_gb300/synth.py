@@ -146,19 +146,37 @@ def make_inputs(wl: Workload, seed: int = 0, device="cpu", unit_scale: bool = Fa
     and ws13 [S,shared_up,H], ws2 [S,H,Is] when the workload has shared experts."""
     T, H, E, I = wl.tokens, wl.hidden, wl.experts, wl.inter
     x_std = 1.0 if unit_scale else wl.x_std
-    w13_std = 1.0 / math.sqrt(H) if unit_scale else wl.w_std
-    w2_std = 1.0 / math.sqrt(I) if unit_scale else wl.w_std
     d = {"logits": make_logits(wl, seed, device),
          "x": normal((T, H), x_std, seed, "x", device)}
     if weights:
-        d["w13"] = normal((E, wl.up, H), w13_std, seed, "w13", device)
-        d["w2"] = normal((E, H, I), w2_std, seed, "w2", device)
+        d["w13"] = torch.empty((E, wl.up, H), dtype=torch.bfloat16, device=device)
+        d["w2"] = torch.empty((E, H, I), dtype=torch.bfloat16, device=device)
+        for e in range(E):
+            d["w13"][e], d["w2"][e] = expert_weights(wl, e, seed, device, unit_scale)
         if wl.shared > 0:
-            Is = wl.shared_inter
-            ws2_std = 1.0 / math.sqrt(Is) if unit_scale else wl.w_std
-            d["ws13"] = normal((wl.shared, wl.shared_up, H), w13_std, seed, "ws13", device)
-            d["ws2"] = normal((wl.shared, H, Is), ws2_std, seed, "ws2", device)
+            d["ws13"] = torch.empty((wl.shared, wl.shared_up, H), dtype=torch.bfloat16, device=device)
+            d["ws2"] = torch.empty((wl.shared, H, wl.shared_inter), dtype=torch.bfloat16, device=device)
+            for s in range(wl.shared):
+                d["ws13"][s], d["ws2"][s] = shared_expert_weights(wl, s, seed, device, unit_scale)
     return d
+
+
+def expert_weights(wl: Workload, e: int, seed: int = 0, device="cpu", unit_scale: bool = False):
+    """(W13[e] [up,H], W2[e] [H,I]) of routed expert e, drawn from streams of
+    their own, so one expert can be regenerated without the others."""
+    H, I = wl.hidden, wl.inter
+    s13 = 1.0 / math.sqrt(H) if unit_scale else wl.w_std
+    s2 = 1.0 / math.sqrt(I) if unit_scale else wl.w_std
+    return (normal((wl.up, H), s13, seed, f"w13/{e}", device),
+            normal((H, I), s2, seed, f"w2/{e}", device))
+
+
+def shared_expert_weights(wl: Workload, s: int, seed: int = 0, device="cpu", unit_scale: bool = False):
+    H, Is = wl.hidden, wl.shared_inter
+    s13 = 1.0 / math.sqrt(H) if unit_scale else wl.w_std
+    s2 = 1.0 / math.sqrt(Is) if unit_scale else wl.w_std
+    return (normal((wl.shared_up, H), s13, seed, f"ws13/{s}", device),
+            normal((H, Is), s2, seed, f"ws2/{s}", device))
 
 
 def bf16_bits(t: torch.Tensor):
