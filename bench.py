@@ -39,7 +39,8 @@ METRIC = "MoE layer tokens/s; dispatch+combine HBM GB/s; expert GEMM TFLOP/s vs 
 def describe(wl):
     return (f"{wl.name}: {wl.tokens} tokens, hidden {wl.hidden}, {wl.experts} experts top-{wl.top_k}, "
             f"intermediate {wl.inter}, {'SwiGLU' if wl.act == 0 else 'ReLU^2'}, "
-            f"router logits N(0,1) + Zipf({wl.zipf_s}) expert bias, W ~ N(0,0.02), x ~ N(0,1), seed 0")
+            f"router logits N(0,1)" + (f" + Zipf({wl.zipf_s}) expert bias" if wl.logits == "zipf" else "")
+            + ", W ~ N(0,0.02), x ~ N(0,1), seed 0")
 
 
 def algorithmic(wl, counts=None):
@@ -381,7 +382,7 @@ def run_native(args, wl, world, rank, local):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(synth.WORKLOADS))

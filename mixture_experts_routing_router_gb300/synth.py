@@ -79,6 +79,9 @@ WORKLOADS = {
     "count_first": Workload("count_first", 2048, 2048, 128, 8, 768, capacity=2048),
     "deepseek": Workload("deepseek", 1024, 2048, 64, 6, 1408, shared=2, shared_inter=1408),
     "large": Workload("large", 16384, 7168, 256, 8, 2048, logits="zipf"),
+    # profiling case of the large layer's kernels: same hidden / intermediate /
+    # top-k, 32 experts and 4096 tokens (about 3 GB on the device)
+    "large_e32": Workload("large_e32", 4096, 7168, 32, 8, 2048, logits="zipf"),
 }
 for _rows in (1, 8, 16):
     for _kind in ("shared", "distinct"):
