@@ -179,6 +179,32 @@ MOE_API moe_status moe_layer(const moe_shape* shape, const float* logits, const 
                      const uint16_t* w2, const uint16_t* ws13, const uint16_t* ws2,
                      uint16_t* out, void* ws, size_t ws_bytes, void* stream);
 
+/* moe_dispatch for callers that cannot allocate device memory, and so cannot
+ * provide the workspace the other calls take: code that runs where cudaMalloc
+ * is not allowed or not safe (while a CUDA graph is being captured, inside a
+ * custom allocator's own callbacks, on a teardown path), or a host whose device
+ * memory is all handed out by a fixed arena with nothing spare for scratch.
+ * The paper has no counterpart: this is a deployment convenience, not a step
+ * of the method.
+ * Arguments and results are those of moe_dispatch without the workspace; the
+ * device status of this call (0 or a moe_status code) is written to
+ * *device_status (device i32, 4-byte aligned; NULL skips it).
+ * The scratch moe_dispatch keeps in the workspace (status header, per-pair
+ * ranks, look-back flags) lives instead in one static device array of about
+ * 1.5 MiB inside this library; every GPU that loads the library holds its own
+ * copy until the process exits.  Limit: tokens * top_k <= 131072 pairs (with
+ * the usual experts <= 1024); larger calls return MOE_ERR_UNSUPPORTED and say
+ * why in moe_last_error_message, before anything is launched.
+ * The first call on a device looks up the array's device address for that
+ * device, a host-side step: make that first call before any stream capture.
+ * The call allocates nothing (no cudaMalloc, cudaFree or allocating library
+ * routine).  All calls on a device share its one array, and each call clears
+ * what must start at zero; calls that overlap on the same GPU (for example on
+ * two concurrent streams) therefore race and must be serialised. */
+MOE_API moe_status moe_dispatch_noalloc(const moe_shape* shape, const uint16_t* x, const int32_t* topk_ids,
+                                        int32_t* counts, int32_t* offsets, int32_t* dest, int32_t* sorted_pair,
+                                        uint16_t* x_perm, int32_t* device_status, void* stream);
+
 /* Synchronise `stream`, return in *device_status the largest status code raised
  * by kernels on this workspace since the last read, and clear it. */
 MOE_API moe_status moe_status_read(void* ws, void* stream, moe_status* device_status);

@@ -158,6 +158,9 @@ moe_status do_combine(const moe_shape& s, const uint16_t* y_perm, const int32_t*
 }
 
 }  // namespace
+
+moe_status validate_shape(const moe_shape* s) { return check_shape(s); }
+
 }  // namespace moe
 
 using namespace moe;

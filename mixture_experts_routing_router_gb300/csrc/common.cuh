@@ -253,6 +253,9 @@ moe_status launch_grouped_gemm(const GemmProblem& p, WsHeader* hdr, cudaStream_t
 
 int device_sm_count();
 
+// The host-side shape checks every entry point applies (MOE_OK when valid).
+moe_status validate_shape(const moe_shape* s);
+
 // Record a host-side failure description for moe_last_error_message (this thread).
 void set_error(const char* fmt, ...);
 void clear_error();

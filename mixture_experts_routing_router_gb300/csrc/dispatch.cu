@@ -22,6 +22,8 @@
 // row with 16-byte vectors: one read of x[t], k writes.
 #include "common.cuh"
 
+#include <mutex>
+
 namespace moe {
 namespace {
 
@@ -251,3 +253,94 @@ cudaError_t launch_scatter(const moe_shape& s, const uint16_t* x, const int32_t*
 }
 
 }  // namespace moe
+
+// ---------------------------------------------------------------------------
+// moe_dispatch_noalloc: the same count-first dispatch for callers that cannot
+// allocate device memory.  Its scratch -- the status header, the per-pair
+// ranks and the look-back flags that moe_dispatch keeps in the caller's
+// workspace -- lives in one file-scope device array of fixed size instead.
+// Every GPU that loads this library holds that array until the process exits.
+// ---------------------------------------------------------------------------
+namespace moe {
+namespace {
+constexpr long long kNoAllocMaxPairs = 131072;                      // T * k limit
+constexpr int kNoAllocMaxExperts = 1024;
+constexpr size_t kNoAllocHdrBytes = 4096;
+constexpr size_t kNoAllocRankBytes = (size_t)kNoAllocMaxPairs * 4;  // 512 KiB
+constexpr size_t kNoAllocFlagBytes =                                // 1 MiB
+    (size_t)((kNoAllocMaxPairs + kCountChunk - 1) / kCountChunk) * kNoAllocMaxExperts * 8;
+constexpr size_t kNoAllocBytes = kNoAllocHdrBytes + kNoAllocRankBytes + kNoAllocFlagBytes;
+}  // namespace
+}  // namespace moe
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[moe::kNoAllocBytes];
+
+namespace moe {
+namespace {
+// Device address of g_noalloc_scratch per device, looked up once per device
+// with that device current (the host-side name is only a stand-in).
+std::mutex g_noalloc_mu;
+unsigned char* g_noalloc_ptr[64] = {nullptr};
+
+moe_status noalloc_scratch(unsigned char** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        set_error("moe_dispatch_noalloc: no usable current CUDA device");
+        return MOE_ERR_CUDA;
+    }
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || p == nullptr) {
+            set_error("moe_dispatch_noalloc: cudaGetSymbolAddress of the static scratch failed: %s",
+                      cudaGetErrorString(e));
+            return MOE_ERR_CUDA;
+        }
+        g_noalloc_ptr[dev] = static_cast<unsigned char*>(p);
+    }
+    *out = g_noalloc_ptr[dev];
+    return MOE_OK;
+}
+
+bool al16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+}  // namespace
+}  // namespace moe
+
+extern "C" moe_status moe_dispatch_noalloc(const moe_shape* shape, const uint16_t* x, const int32_t* topk_ids,
+                                           int32_t* counts, int32_t* offsets, int32_t* dest, int32_t* sorted_pair,
+                                           uint16_t* x_perm, int32_t* device_status, void* stream) {
+    using namespace moe;
+    clear_error();
+    moe_status r = validate_shape(shape);
+    if (r != MOE_OK) return r;
+    if (!al16(x) || !al16(topk_ids) || !al16(counts) || !al16(offsets) || !al16(dest) || !al16(sorted_pair) ||
+        !al16(x_perm) || (device_status && (reinterpret_cast<uintptr_t>(device_status) & 3u)))
+        return MOE_ERR_INVALID_ARG;
+    const long long R = (long long)shape->tokens * shape->top_k;
+    if (R > kNoAllocMaxPairs) {
+        set_error("moe_dispatch_noalloc: %lld pairs (tokens x top_k) exceed the static scratch limit of %lld",
+                  R, kNoAllocMaxPairs);
+        return MOE_ERR_UNSUPPORTED;
+    }
+    unsigned char* base = nullptr;
+    if ((r = noalloc_scratch(&base)) != MOE_OK) return r;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    WsHeader* hdr = reinterpret_cast<WsHeader*>(base);
+    int32_t* rank = reinterpret_cast<int32_t*>(base + kNoAllocHdrBytes);
+    unsigned long long* flags = reinterpret_cast<unsigned long long*>(base + kNoAllocHdrBytes + kNoAllocRankBytes);
+    const int tiles = (int)((R + kCountChunk - 1) / kCountChunk);
+    // the array keeps the previous call's contents: start from a clear header
+    // (status, timeout site, tile counter, capacity verdict); launch_count
+    // clears the look-back flags it uses
+    cudaError_t e = cudaMemsetAsync(hdr, 0, sizeof(WsHeader), st);
+    if (e == cudaSuccess) e = launch_count(*shape, topk_ids, counts, offsets, rank, flags, tiles, hdr, st);
+    if (e == cudaSuccess) e = launch_scatter(*shape, x, topk_ids, offsets, rank, dest, sorted_pair, x_perm, hdr, st);
+    if (e == cudaSuccess && device_status)
+        e = cudaMemcpyAsync(device_status, &hdr->status, sizeof(int32_t), cudaMemcpyDeviceToDevice, st);
+    if (e != cudaSuccess) {
+        set_error("moe_dispatch_noalloc: %s", cudaGetErrorString(e));
+        return MOE_ERR_CUDA;
+    }
+    return MOE_OK;
+}

@@ -32,7 +32,7 @@ MOE_ACT_RELU2 = 1
 # every symbol include/moe.h declares
 EXPORTS = ("moe_workspace_size", "moe_workspace_init", "moe_route", "moe_dispatch", "moe_expert_up",
            "moe_expert_down", "moe_expert_ffn", "moe_combine", "moe_layer", "moe_status_read",
-           "moe_status_string", "moe_last_error_message")
+           "moe_status_string", "moe_last_error_message", "moe_dispatch_noalloc")
 
 
 class MoEError(RuntimeError):
@@ -85,6 +85,7 @@ def lib():
                 "moe_combine": [SP, P, P, P, P, P, P, S, P],
                 "moe_layer": [SP, P, P, P, P, P, P, P, P, P, P, S, P],
                 "moe_status_read": [P, P, ctypes.POINTER(ctypes.c_int)],
+                "moe_dispatch_noalloc": [SP, P, P, P, P, P, P, P, P, P],
             }
             for name, args in sig.items():
                 fn = getattr(L, name)
@@ -193,6 +194,14 @@ def moe_layer(shape, logits, ids_in, w_in, x, w13, w2, ws13, ws2, out, ws, strea
     _check(lib().moe_layer(ctypes.byref(shape), _ptr(logits), _ptr(ids_in), _ptr(w_in), _ptr(x), _ptr(w13),
                            _ptr(w2), _ptr(ws13), _ptr(ws2), _ptr(out), _ptr(ws), _wsb(ws), _stream(stream)),
            "moe_layer")
+
+
+def moe_dispatch_noalloc(shape, x, topk_ids, counts, offsets, dest, sorted_pair, x_perm, device_status=None,
+                         stream=None):
+    """moe_dispatch without a workspace (static scratch inside the library)."""
+    _check(lib().moe_dispatch_noalloc(ctypes.byref(shape), _ptr(x), _ptr(topk_ids), _ptr(counts), _ptr(offsets),
+                                      _ptr(dest), _ptr(sorted_pair), _ptr(x_perm), _ptr(device_status),
+                                      _stream(stream)), "moe_dispatch_noalloc")
 
 
 def moe_status_read(ws, stream=None) -> int:
