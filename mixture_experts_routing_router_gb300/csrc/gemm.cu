@@ -5,24 +5,32 @@
 // experts, BF16 store boundaries with FP32 accumulation).
 //
 // One persistent CTA per SM walks a tile list built on the device from the
-// bucket bounds (offsets): group g (an expert) owns ceil(m_g / 128) row tiles
+// bucket bounds (offsets): group g (an expert) owns ceil(m_g / BMT) row tiles
 // times ceil(N / BN) column tiles.  The counts never travel to the host, so
 // the layer stays capturable in a CUDA graph.
 //
-// Roles (192 threads):
-//   warp 0  one thread issues TMA loads of A (128 x 64) and B (256 x 64) tiles,
-//           128-byte swizzled, into a 4-stage shared-memory ring;
-//   warp 1  allocates 512 TMEM columns (two 128 x 256 FP32 accumulators) and
-//           one thread issues tcgen05.mma (M 128, N 256, K 16) per 16-wide
-//           slice, committing each stage back to the producer and each
-//           finished accumulator to the epilogue;
-//   warps 2-5  read the accumulator with tcgen05.ld (one TMEM lane = one row
-//           per thread), apply the activation, round to BF16 and store,
-//           masking rows past the bucket end and columns past N.
-// The two accumulators let the epilogue of one tile overlap the main loop of
-// the next.  SwiGLU tiles load 128 gate rows and the matching 128 up rows as
-// the two halves of one 256-row B tile, so gate and up land side by side in
-// one accumulator and the epilogue computes silu(g) * u without a second pass.
+// Roles:
+//   warp 0     one thread issues TMA loads (128-byte swizzle, 64-column K
+//              boxes) of the A rows and the 256-row B tile into a ring of
+//              shared-memory stages;
+//   warp 1     allocates all 512 TMEM columns; one thread issues tcgen05.mma
+//              (M 128, N 256, K 16) per 16-wide K slice, committing each stage
+//              back to the producer and each finished tile to the epilogue;
+//   warps 2..  read the accumulator with tcgen05.ld (one TMEM lane = one row
+//              per thread), apply the activation, round to BF16 and store,
+//              masking rows past the bucket end and columns past N.
+// Two shapes of the same kernel (HALVES):
+//   1: 128-row tiles, two 256-column accumulators in TMEM so the epilogue of
+//      one tile overlaps the main loop of the next; 4 stages of 48 KiB;
+//      4 epilogue warps.  For short K (the down projection).
+//   2: 256-row tiles as two 128-row halves sharing every B tile (two MMAs per
+//      K slice into the two 256-column accumulators), which cuts the operand
+//      traffic per FLOP by a third; a tail whose second half is empty loads
+//      and multiplies only the first.  3 stages of 64 KiB; the epilogue (8
+//      warps, one half each) is not overlapped.  For long K (the up projection).
+// SwiGLU tiles load 128 gate rows and the matching 128 up rows as the two
+// halves of the 256-row B tile, so gate and up land side by side in one
+// accumulator and the epilogue computes silu(g) * u without a second pass.
 //
 // Every wait is bounded; on a timeout the CTA stops issuing work, drains its
 // in-flight tensor-core work, frees TMEM, raises MOE_ERR_TIMEOUT and returns.
@@ -34,21 +42,30 @@
 namespace moe {
 namespace {
 
-constexpr int BM = 128;
+constexpr int BM = 128;                      // rows per MMA / per accumulator
 constexpr int BK = 64;                       // 64 BF16 = 128 B: one swizzle row
 constexpr int BN_MMA = 256;
-constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;         // 16 KiB
 constexpr int B_HALF_BYTES = 128 * BK * 2;   // 16 KiB
 constexpr int B_BYTES = BN_MMA * BK * 2;     // 32 KiB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int THREADS = 192;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN_MMA);
-// Dynamic shared memory ceiling set on the kernels: the 4-stage ring plus the
+// Dynamic shared memory ceiling set on the kernels: the stage ring plus the
 // control block and the per-group tables of up to 1024 groups.  It stays below
 // the 227 KiB opt-in limit minus the kernel's small static shared memory.
 constexpr int MAX_DYN_SMEM = 212 * 1024;
+// Reductions at least this long use the 256-row tile (HALVES = 2).
+constexpr long long kLongK = 4096;
+
+template <int HALVES>
+struct Cfg {
+    static constexpr int STAGES = HALVES == 1 ? 4 : 3;
+    static constexpr int STAGE_BYTES = HALVES * A_BYTES + B_BYTES;   // 48 / 64 KiB
+    static constexpr int NUM_ACC = HALVES == 1 ? 2 : 1;             // accumulator buffers
+    static constexpr int EPI_WARPS = 4 * HALVES;
+    static constexpr int THREADS = 64 + 32 * EPI_WARPS;             // 192 / 320
+    static constexpr int BMT = BM * HALVES;                         // rows per tile
+};
 
 struct KParams {
     const int32_t* offsets;
@@ -62,11 +79,12 @@ struct KParams {
     WsHeader* hdr;
 };
 
+template <int HALVES>
 struct SmemCtl {
-    unsigned long long full[STAGES];
-    unsigned long long empty[STAGES];
-    unsigned long long tfull[2];
-    unsigned long long tempty[2];
+    unsigned long long full[Cfg<HALVES>::STAGES];
+    unsigned long long empty[Cfg<HALVES>::STAGES];
+    unsigned long long tfull[Cfg<HALVES>::NUM_ACC];
+    unsigned long long tempty[Cfg<HALVES>::NUM_ACC];
     unsigned long long drain;
     uint32_t tmem_base;
     int abort;
@@ -98,16 +116,81 @@ __device__ __forceinline__ Tile decode_tile(int tile, const int* prefix, const i
     return t;
 }
 
+// Epilogue of one 128-row accumulator: this warp's 32 TMEM lanes at `tbase`,
+// one row per thread; writes the tile's BN_OUT output columns from col_base.
 template <int MODE>
-__global__ void __launch_bounds__(THREADS, 1)
+__device__ __forceinline__ void epilogue_rows(uint32_t tbase, bool row_ok, __nv_bfloat16* orow, int col_base,
+                                              int N) {
+    if (MODE == kGemmSwiGLU) {
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+            uint32_t gv[32], uv[32];
+            tmem_ld_32cols(tbase + c * 32, gv);
+            tmem_ld_32cols(tbase + 128 + c * 32, uv);
+            tmem_ld_wait();
+            const int col0 = col_base + c * 32;
+            if (row_ok) {
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    if (col0 + v * 8 < N) {
+                        uint32_t o[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            float hv[2];
+#pragma unroll
+                            for (int h = 0; h < 2; ++h) {
+                                const float g = __uint_as_float(gv[v * 8 + 2 * i + h]);
+                                const float u = __uint_as_float(uv[v * 8 + 2 * i + h]);
+                                hv[h] = g / (1.0f + __expf(-g)) * u;
+                            }
+                            o[i] = pack2(hv[0], hv[1]);
+                        }
+                        *reinterpret_cast<uint4*>(orow + col0 + v * 8) = make_uint4(o[0], o[1], o[2], o[3]);
+                    }
+                }
+            }
+        }
+    } else {
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+            uint32_t av[32];
+            tmem_ld_32cols(tbase + c * 32, av);
+            tmem_ld_wait();
+            const int col0 = col_base + c * 32;
+            if (row_ok) {
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    if (col0 + v * 8 < N) {
+                        uint32_t o[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            float a0 = __uint_as_float(av[v * 8 + 2 * i]);
+                            float a1 = __uint_as_float(av[v * 8 + 2 * i + 1]);
+                            if (MODE == kGemmReLU2) {
+                                a0 = a0 > 0.f ? a0 * a0 : 0.f;
+                                a1 = a1 > 0.f ? a1 * a1 : 0.f;
+                            }
+                            o[i] = pack2(a0, a1);
+                        }
+                        *reinterpret_cast<uint4*>(orow + col0 + v * 8) = make_uint4(o[0], o[1], o[2], o[3]);
+                    }
+                }
+            }
+        }
+    }
+}
+
+template <int MODE, int HALVES>
+__global__ void __launch_bounds__(Cfg<HALVES>::THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const KParams p) {
+    using C = Cfg<HALVES>;
     constexpr int BN_OUT = (MODE == kGemmSwiGLU) ? 128 : 256;
     extern __shared__ uint8_t smem_raw[];
     // 1 KiB alignment for the 128-byte swizzle atoms
     const uint32_t raw_u32 = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + ((1024u - (raw_u32 & 1023u)) & 1023u);
-    SmemCtl* ctl = reinterpret_cast<SmemCtl*>(smem + STAGES * STAGE_BYTES);
+    SmemCtl<HALVES>* ctl = reinterpret_cast<SmemCtl<HALVES>*>(smem + C::STAGES * C::STAGE_BYTES);
     int* prefix = reinterpret_cast<int*>(ctl + 1);          // [groups + 1] tiles before group g
     int* rstart = prefix + (p.groups + 1);                  // [groups] first row of group g
     int* rcount = rstart + p.groups;                        // [groups] rows of group g
@@ -118,13 +201,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 
     // ---- set-up: barriers, TMEM, tile prefix -------------------------------
     if (tid == 0) {
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(smem_u32(&ctl->full[s]), 1);
             mbar_init(smem_u32(&ctl->empty[s]), 1);
         }
-        for (int a = 0; a < 2; ++a) {
+        for (int a = 0; a < C::NUM_ACC; ++a) {
             mbar_init(smem_u32(&ctl->tfull[a]), 1);
-            mbar_init(smem_u32(&ctl->tempty[a]), 4);
+            mbar_init(smem_u32(&ctl->tempty[a]), C::EPI_WARPS);
         }
         mbar_init(smem_u32(&ctl->drain), 1);
         ctl->abort = 0;
@@ -139,7 +222,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     }
     // Group rows.  Each bucket is clamped to [0, a_rows] on its own, so even
     // malformed offsets keep every row access inside A and the output.
-    for (int g = tid; g < p.groups; g += THREADS) {
+    for (int g = tid; g < p.groups; g += C::THREADS) {
         if (p.offsets) {
             int lo = p.offsets[g], hi = p.offsets[g + 1];
             lo = lo < 0 ? 0 : (lo > p.a_rows ? p.a_rows : lo);
@@ -155,18 +238,18 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     // exclusive scan of tiles per group -> prefix[0..groups]
     {
         const int n = p.groups;
-        const int per = (n + THREADS - 1) / THREADS;
+        const int per = (n + C::THREADS - 1) / C::THREADS;
         const int g0 = tid * per;
         int loc = 0;
         for (int i = 0; i < per; ++i)
-            if (g0 + i < n) loc += ((rcount[g0 + i] + BM - 1) / BM) * ntn;
+            if (g0 + i < n) loc += ((rcount[g0 + i] + C::BMT - 1) / C::BMT) * ntn;
         int inc = loc;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
             const int v = __shfl_up_sync(0xffffffffu, inc, off);
             if (lane >= off) inc += v;
         }
-        __shared__ int wtot[THREADS / 32];
+        __shared__ int wtot[C::THREADS / 32];
         if (lane == 31) wtot[warp] = inc;
         __syncthreads();
         int run = inc - loc;
@@ -174,10 +257,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         for (int i = 0; i < per; ++i) {
             if (g0 + i < n) {
                 prefix[g0 + i] = run;
-                run += ((rcount[g0 + i] + BM - 1) / BM) * ntn;
+                run += ((rcount[g0 + i] + C::BMT - 1) / C::BMT) * ntn;
             }
         }
-        if (tid == THREADS - 1) { prefix[n] = run; ctl->total_tiles = run; }
+        if (tid == C::THREADS - 1) { prefix[n] = run; ctl->total_tiles = run; }
     }
     tc_fence_before();
     __syncthreads();
@@ -196,7 +279,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             bool ok = true;
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
                 const Tile t = decode_tile(tile, prefix, rstart, rcount, p, ntn);
-                const int a_row = t.row0 + t.mt * BM;
+                const int a_row = t.row0 + t.mt * C::BMT;
+                const bool second = HALVES == 2 && (t.mt * C::BMT + BM < t.mrows);
+                const uint32_t bytes = (second ? 2 : 1) * A_BYTES + B_BYTES;
                 const int n0 = t.nt * BN_OUT;
                 const int b_lo = t.g * p.b_group_rows + n0;
                 const int b_hi = (MODE == kGemmSwiGLU) ? b_lo + p.up_off : b_lo + 128;
@@ -204,12 +289,15 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     const int seg = i / nkb, kb = i - seg * nkb;
                     if (!mbar_wait_bounded(smem_u32(&ctl->empty[stage]), ph ^ 1u, abort)) { ok = false; break; }
                     const uint32_t full = smem_u32(&ctl->full[stage]);
-                    const uint32_t sa = smem_base + stage * STAGE_BYTES;
-                    mbar_arrive_expect_tx(full, STAGE_BYTES);
-                    tma_load_2d(sa, &tmA, full, seg * p.a_seg_col + kb * BK, a_row);
-                    tma_load_2d(sa + A_BYTES, &tmB, full, kb * BK, b_lo + seg * p.b_seg_row);
-                    tma_load_2d(sa + A_BYTES + B_HALF_BYTES, &tmB, full, kb * BK, b_hi + seg * p.b_seg_row);
-                    if (++stage == STAGES) { stage = 0; ph ^= 1u; }
+                    const uint32_t sa = smem_base + stage * C::STAGE_BYTES;
+                    const uint32_t sb = sa + HALVES * A_BYTES;
+                    const int ax = seg * p.a_seg_col + kb * BK;
+                    mbar_arrive_expect_tx(full, bytes);
+                    tma_load_2d(sa, &tmA, full, ax, a_row);
+                    if (second) tma_load_2d(sa + A_BYTES, &tmA, full, ax, a_row + BM);
+                    tma_load_2d(sb, &tmB, full, kb * BK, b_lo + seg * p.b_seg_row);
+                    tma_load_2d(sb + B_HALF_BYTES, &tmB, full, kb * BK, b_hi + seg * p.b_seg_row);
+                    if (++stage == C::STAGES) { stage = 0; ph ^= 1u; }
                 }
             }
             if (!ok) {
@@ -229,26 +317,37 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             uint32_t aph = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+                bool second = false;
+                if (HALVES == 2) {
+                    const Tile t = decode_tile(tile, prefix, rstart, rcount, p, ntn);
+                    second = t.mt * C::BMT + BM < t.mrows;
+                }
                 if (!mbar_wait_bounded(smem_u32(&ctl->tempty[acc]), aph ^ 1u, abort)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t d = tmem_base + (uint32_t)(acc * BN_MMA);
+                const uint32_t d0 = tmem_base + (uint32_t)(acc * BN_MMA);
                 for (int i = 0; i < nk; ++i) {
                     if (!mbar_wait_bounded(smem_u32(&ctl->full[stage]), ph, abort)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t sa = smem_base + stage * STAGE_BYTES;
-                    const uint64_t ad = sdesc_k_sw128(sa);
-                    const uint64_t bd = sdesc_k_sw128(sa + A_BYTES);
+                    const uint32_t sa = smem_base + stage * C::STAGE_BYTES;
+                    const uint64_t bd = sdesc_k_sw128(sa + HALVES * A_BYTES);
+                    const uint64_t ad0 = sdesc_k_sw128(sa);
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk)   // +32 B along K inside the swizzle row
-                        tc_mma_bf16(d, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), IDESC,
+                        tc_mma_bf16(d0, ad0 + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), IDESC,
                                     (i > 0 || kk > 0) ? 1u : 0u);
+                    if (HALVES == 2 && second) {
+                        const uint64_t ad1 = sdesc_k_sw128(sa + A_BYTES);
+#pragma unroll
+                        for (int kk = 0; kk < BK / 16; ++kk)
+                            tc_mma_bf16(d0 + BN_MMA, ad1 + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), IDESC,
+                                        (i > 0 || kk > 0) ? 1u : 0u);
+                    }
                     tc_commit(smem_u32(&ctl->empty[stage]));
-                    if (++stage == STAGES) { stage = 0; ph ^= 1u; }
+                    if (++stage == C::STAGES) { stage = 0; ph ^= 1u; }
                 }
                 if (!ok) break;
                 tc_commit(smem_u32(&ctl->tfull[acc]));
-                acc ^= 1;
-                if (acc == 0) aph ^= 1u;
+                if (++acc == C::NUM_ACC) { acc = 0; aph ^= 1u; }
             }
             // drain: wait until every MMA this thread issued has completed
             tc_commit(smem_u32(&ctl->drain));
@@ -261,8 +360,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             }
         }
     } else {
-        // ---------------- epilogue (warps 2..5) ----------------
-        const int q = warp & 3;                     // TMEM lane quarter of this warp
+        // ---------------- epilogue (warps 2 .. 2 + EPI_WARPS - 1) ----------------
+        const int q = warp & 3;                                   // TMEM lane quarter of this warp
+        const int half = (HALVES == 2) ? (warp - 2) >> 2 : 0;     // which 128-row half
         int acc = 0;
         uint32_t aph = 0;
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
@@ -275,73 +375,20 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 break;
             }
             tc_fence_after();
-            const int r = t.mt * BM + q * 32 + lane;
-            const bool row_ok = r < t.mrows;
-            __nv_bfloat16* orow = p.out + (size_t)(t.row0 + (row_ok ? r : 0)) * p.ldo +
-                                  (size_t)t.g * p.out_group_col;
-            const uint32_t tbase = tmem_base + (uint32_t)(acc * BN_MMA) + ((uint32_t)(q * 32) << 16);
-            if (MODE == kGemmSwiGLU) {
-#pragma unroll 1
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t gv[32], uv[32];
-                    tmem_ld_32cols(tbase + c * 32, gv);
-                    tmem_ld_32cols(tbase + 128 + c * 32, uv);
-                    tmem_ld_wait();
-                    const int col0 = t.nt * BN_OUT + c * 32;
-                    if (row_ok) {
-#pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            if (col0 + v * 8 < p.N) {
-                                uint32_t o[4];
-#pragma unroll
-                                for (int i = 0; i < 4; ++i) {
-                                    float hv[2];
-#pragma unroll
-                                    for (int h = 0; h < 2; ++h) {
-                                        const float g = __uint_as_float(gv[v * 8 + 2 * i + h]);
-                                        const float u = __uint_as_float(uv[v * 8 + 2 * i + h]);
-                                        hv[h] = g / (1.0f + __expf(-g)) * u;
-                                    }
-                                    o[i] = pack2(hv[0], hv[1]);
-                                }
-                                *reinterpret_cast<uint4*>(orow + col0 + v * 8) = make_uint4(o[0], o[1], o[2], o[3]);
-                            }
-                        }
-                    }
-                }
-            } else {
-#pragma unroll 1
-                for (int c = 0; c < 8; ++c) {
-                    uint32_t av[32];
-                    tmem_ld_32cols(tbase + c * 32, av);
-                    tmem_ld_wait();
-                    const int col0 = t.nt * BN_OUT + c * 32;
-                    if (row_ok) {
-#pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            if (col0 + v * 8 < p.N) {
-                                uint32_t o[4];
-#pragma unroll
-                                for (int i = 0; i < 4; ++i) {
-                                    float a0 = __uint_as_float(av[v * 8 + 2 * i]);
-                                    float a1 = __uint_as_float(av[v * 8 + 2 * i + 1]);
-                                    if (MODE == kGemmReLU2) {
-                                        a0 = a0 > 0.f ? a0 * a0 : 0.f;
-                                        a1 = a1 > 0.f ? a1 * a1 : 0.f;
-                                    }
-                                    o[i] = pack2(a0, a1);
-                                }
-                                *reinterpret_cast<uint4*>(orow + col0 + v * 8) = make_uint4(o[0], o[1], o[2], o[3]);
-                            }
-                        }
-                    }
-                }
+            const int r = t.mt * C::BMT + half * BM + q * 32 + lane;
+            const bool half_live = t.mt * C::BMT + half * BM < t.mrows;   // warp-uniform
+            if (half_live) {
+                const bool row_ok = r < t.mrows;
+                __nv_bfloat16* orow = p.out + (size_t)(t.row0 + (row_ok ? r : 0)) * p.ldo +
+                                      (size_t)t.g * p.out_group_col;
+                const uint32_t tbase =
+                    tmem_base + (uint32_t)((acc + half) * BN_MMA) + ((uint32_t)(q * 32) << 16);
+                epilogue_rows<MODE>(tbase, row_ok, orow, t.nt * BN_OUT, p.N);
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[acc]));
-            acc ^= 1;
-            if (acc == 0) aph ^= 1u;
+            if (++acc == C::NUM_ACC) { acc = 0; aph ^= 1u; }
         }
     }
 
@@ -391,23 +438,29 @@ bool make_map(CUtensorMap* m, const void* base, long long rows, long long cols) 
     return true;
 }
 
-template <int MODE>
+template <int MODE, int HALVES>
 cudaError_t launch_mode(const CUtensorMap& ma, const CUtensorMap& mb, const KParams& kp, size_t smem,
                         cudaStream_t st) {
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(grouped_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        MAX_DYN_SMEM);
+        attr_err = cudaFuncSetAttribute(grouped_gemm_kernel<MODE, HALVES>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, MAX_DYN_SMEM);
     });
     if (attr_err != cudaSuccess) {
         set_error("cudaFuncSetAttribute(max dynamic smem %d): %s", MAX_DYN_SMEM, cudaGetErrorString(attr_err));
         return attr_err;
     }
-    grouped_gemm_kernel<MODE><<<device_sm_count(), THREADS, smem, st>>>(ma, mb, kp);
+    grouped_gemm_kernel<MODE, HALVES><<<device_sm_count(), Cfg<HALVES>::THREADS, smem, st>>>(ma, mb, kp);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) set_error("grouped GEMM launch (smem %zu): %s", smem, cudaGetErrorString(e));
     return e;
+}
+
+template <int HALVES>
+size_t smem_bytes(int groups) {
+    return 1024 + (size_t)Cfg<HALVES>::STAGES * Cfg<HALVES>::STAGE_BYTES + sizeof(SmemCtl<HALVES>) +
+           3 * (size_t)(groups + 1) * 4;
 }
 
 }  // namespace
@@ -436,16 +489,27 @@ moe_status launch_grouped_gemm(const GemmProblem& g, WsHeader* hdr, cudaStream_t
     kp.ldo = g.ldo;
     kp.out_group_col = g.out_group_col;
     kp.hdr = hdr;
-    const size_t smem = 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(SmemCtl) + 3 * (size_t)(g.groups + 1) * 4;
+    // Long reductions amortise the un-overlapped epilogue of the 256-row
+    // tile; short ones keep the double-buffered 128-row tile.
+    const int halves = (long long)g.K * g.nseg >= kLongK ? 2 : 1;
+    const size_t smem = halves == 2 ? smem_bytes<2>(g.groups) : smem_bytes<1>(g.groups);
     if (smem > (size_t)MAX_DYN_SMEM) {
         set_error("grouped GEMM needs %zu bytes of shared memory", smem);
         return MOE_ERR_UNSUPPORTED;
     }
     cudaError_t e;
-    switch (g.mode) {
-        case kGemmSwiGLU: e = launch_mode<kGemmSwiGLU>(ma, mb, kp, smem, st); break;
-        case kGemmReLU2: e = launch_mode<kGemmReLU2>(ma, mb, kp, smem, st); break;
-        default: e = launch_mode<kGemmPlain>(ma, mb, kp, smem, st); break;
+    if (halves == 2) {
+        switch (g.mode) {
+            case kGemmSwiGLU: e = launch_mode<kGemmSwiGLU, 2>(ma, mb, kp, smem, st); break;
+            case kGemmReLU2: e = launch_mode<kGemmReLU2, 2>(ma, mb, kp, smem, st); break;
+            default: e = launch_mode<kGemmPlain, 2>(ma, mb, kp, smem, st); break;
+        }
+    } else {
+        switch (g.mode) {
+            case kGemmSwiGLU: e = launch_mode<kGemmSwiGLU, 1>(ma, mb, kp, smem, st); break;
+            case kGemmReLU2: e = launch_mode<kGemmReLU2, 1>(ma, mb, kp, smem, st); break;
+            default: e = launch_mode<kGemmPlain, 1>(ma, mb, kp, smem, st); break;
+        }
     }
     return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

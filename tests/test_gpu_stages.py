@@ -33,6 +33,11 @@ SMALL = {
     "wide_e": synth.Workload("wide_e", 70, 64, 1000, 32, 32),
     "t1": synth.Workload("t1", 1, 256, 16, 4, 128),
     "shared3": synth.Workload("shared3", 50, 128, 12, 2, 64, shared=3, shared_inter=72),
+    # reductions of 4096 and more take the 256-row two-accumulator tile: full
+    # tiles, tails whose second half is partly or wholly empty, a ragged K tail
+    "longk": synth.Workload("longk", 300, 4096, 4, 2, 136),
+    "longk_relu2": synth.Workload("longk_relu2", 200, 4160, 3, 2, 264, act=synth.ACT_RELU2),
+    "longk_shared": synth.Workload("longk_shared", 40, 4096, 6, 2, 64, shared=4, shared_inter=1024),
 }
 for _n in DECODE:
     SMALL[_n] = W[_n]
