@@ -1,6 +1,6 @@
 """Benchmark of the MoE layer hot path on one GB300 (or N data-parallel replicas).
 
-One step = one moe_layer call over the large workload: 16384 tokens, hidden
+One step = one moe_layer call (captured once in a CUDA graph and replayed) over the large workload: 16384 tokens, hidden
 7168, 256 experts top-8, intermediate 2048, SwiGLU, Zipf(1.2)-biased router
 logits -- route, count-first dispatch, grouped expert FFN and combine.  Inputs
 (22.5 GB of weights, 235 MB of x) are larger than the 129 MB L2, so no flush
@@ -234,6 +234,14 @@ def run_reference(args, wl, world, rank):
 # ---------------------------------------------------------------------------
 # the GPU arm
 # ---------------------------------------------------------------------------
+def capture(fn, stream):
+    """A CUDA graph of the work `fn` enqueues on `stream`."""
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        fn()
+    return graph
+
+
 def ws_counts(N, shape, g, ws, stream, dev):
     """Per-expert counts of this workload's routing (one route + dispatch)."""
     T, k, E, H = shape.tokens, shape.top_k, shape.experts, shape.hidden
@@ -284,7 +292,9 @@ def run_native(args, wl, world, rank, local):
         if flush_buf is not None:
             flush_buf.fill_(i & 0xFF)
 
-    # ---- headline: K whole-layer steps ---------------------------------------
+    # ---- headline: K whole-layer steps, each a replay of the captured layer ----
+    # (moe_layer enqueues only: it is captured once in a CUDA graph, so a step
+    # costs the GPU work and one graph launch, not one host call per kernel)
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
             layer()
@@ -292,6 +302,10 @@ def run_native(args, wl, world, rank, local):
     st = N.moe_status_read(ws, stream)
     if st != N.MOE_OK:
         raise RuntimeError(f"device status {st} after warm-up")
+    layer_graph = capture(layer, stream)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            layer_graph.replay()
     barrier(world)
     torch.cuda.synchronize(dev)
     with ClockSampler(local) as clk:
@@ -300,7 +314,7 @@ def run_native(args, wl, world, rank, local):
                 ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 ev0.record(stream)
                 for _ in range(args.steps):
-                    layer()
+                    layer_graph.replay()
                 ev1.record(stream)
                 pairs = [(ev0, ev1)]
             else:
@@ -309,7 +323,7 @@ def run_native(args, wl, world, rank, local):
                     flush_l2(i)
                     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                     a.record(stream)
-                    layer()
+                    layer_graph.replay()
                     b.record(stream)
                     pairs.append((a, b))
         stream.synchronize()
@@ -331,23 +345,28 @@ def run_native(args, wl, world, rank, local):
     y_perm = torch.empty(R, H, dtype=torch.bfloat16, device=dev)
     y_sh = torch.empty(T, H, dtype=torch.bfloat16, device=dev) if wl.shared else None
     names = ["route", "dispatch", "expert_up", "expert_down", "combine"]
+    stage_fns = [
+        lambda: N.moe_route(shape, g["logits"], ids, w, ws, stream),
+        lambda: N.moe_dispatch(shape, g["x"], ids, counts, offsets, dest, sp, x_perm, ws, stream),
+        lambda: N.moe_expert_up(shape, x_perm, offsets, g["w13"], g["x"], g.get("ws13"), h, ws, stream),
+        lambda: N.moe_expert_down(shape, h, offsets, g["w2"], g.get("ws2"), y_perm, y_sh, ws, stream),
+        lambda: N.moe_combine(shape, y_perm, dest, w, y_sh, out, ws, stream),
+    ]
+    with torch.cuda.stream(stream):
+        for fn in stage_fns:
+            fn()
+    stream.synchronize()
+    stage_graphs = [capture(fn, stream) for fn in stage_fns]
     reps = max(3, min(args.steps, 20))
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(reps)]
     with torch.cuda.stream(stream):
         for r in range(reps + 2):
             e = evs[r - 2] if r >= 2 else None
             flush_l2(r)
-            if e: e[0].record(stream)
-            N.moe_route(shape, g["logits"], ids, w, ws, stream)
-            if e: e[1].record(stream)
-            N.moe_dispatch(shape, g["x"], ids, counts, offsets, dest, sp, x_perm, ws, stream)
-            if e: e[2].record(stream)
-            N.moe_expert_up(shape, x_perm, offsets, g["w13"], g["x"], g.get("ws13"), h, ws, stream)
-            if e: e[3].record(stream)
-            N.moe_expert_down(shape, h, offsets, g["w2"], g.get("ws2"), y_perm, y_sh, ws, stream)
-            if e: e[4].record(stream)
-            N.moe_combine(shape, y_perm, dest, w, y_sh, out, ws, stream)
-            if e: e[5].record(stream)
+            for i, sg in enumerate(stage_graphs):
+                if e: e[i].record(stream)
+                sg.replay()
+            if e: e[len(names)].record(stream)
     stream.synchronize()
     stage_ms = {n: statistics.median(evs[r][i].elapsed_time(evs[r][i + 1]) for r in range(reps))
                 for i, n in enumerate(names)}
@@ -407,7 +426,7 @@ def run_native(args, wl, world, rank, local):
         import oracle
         oracle.build()
         rng = np.random.default_rng(0)
-        toks = sorted(rng.choice(T, args.cpu_tokens, replace=False).tolist())
+        toks = sorted(rng.choice(T, min(args.cpu_tokens, T), replace=False).tolist())
         secs, n = oracle_sample(wl, g["logits"].cpu().numpy(), synth.bf16_bits(g["x"]), toks, dev, seed=rank)
         cpu = {"value": n / secs, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                "sample": f"{n} random tokens of the {T}-token batch: routing, their top-{k} expert rows with FP64 "

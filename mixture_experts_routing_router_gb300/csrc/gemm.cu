@@ -50,6 +50,11 @@ constexpr int B_HALF_BYTES = 128 * BK * 2;   // 16 KiB
 constexpr int B_BYTES = BN_MMA * BK * 2;     // 32 KiB
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN_MMA);
+// A 128-row accumulator whose rows of this tile number 64 or fewer is computed
+// with M = 64 MMAs (half the tensor work).  Their D rows sit in TMEM lanes
+// 32q + i, i < 16, for row 16q + i (q = lane quarter).
+constexpr uint32_t IDESC64 = idesc_bf16_f32(64, BN_MMA);
+constexpr int kTailRows = 64;
 // Dynamic shared memory ceiling set on the kernels: the stage ring plus the
 // control block and the per-group tables of up to 1024 groups.  It stays below
 // the 227 KiB opt-in limit minus the kernel's small static shared memory.
@@ -317,11 +322,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             uint32_t aph = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-                bool second = false;
-                if (HALVES == 2) {
-                    const Tile t = decode_tile(tile, prefix, rstart, rcount, p, ntn);
-                    second = t.mt * C::BMT + BM < t.mrows;
-                }
+                const Tile t = decode_tile(tile, prefix, rstart, rcount, p, ntn);
+                const int rows0 = t.mrows - t.mt * C::BMT;                  // rows from the first half on
+                const bool second = HALVES == 2 && rows0 > BM;
+                const uint32_t idesc0 = rows0 <= kTailRows ? IDESC64 : IDESC;
+                const uint32_t idesc1 = rows0 - BM <= kTailRows ? IDESC64 : IDESC;
                 if (!mbar_wait_bounded(smem_u32(&ctl->tempty[acc]), aph ^ 1u, abort)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d0 = tmem_base + (uint32_t)(acc * BN_MMA);
@@ -333,13 +338,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     const uint64_t ad0 = sdesc_k_sw128(sa);
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk)   // +32 B along K inside the swizzle row
-                        tc_mma_bf16(d0, ad0 + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), IDESC,
+                        tc_mma_bf16(d0, ad0 + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc0,
                                     (i > 0 || kk > 0) ? 1u : 0u);
                     if (HALVES == 2 && second) {
                         const uint64_t ad1 = sdesc_k_sw128(sa + A_BYTES);
 #pragma unroll
                         for (int kk = 0; kk < BK / 16; ++kk)
-                            tc_mma_bf16(d0 + BN_MMA, ad1 + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), IDESC,
+                            tc_mma_bf16(d0 + BN_MMA, ad1 + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc1,
                                         (i > 0 || kk > 0) ? 1u : 0u);
                     }
                     tc_commit(smem_u32(&ctl->empty[stage]));
@@ -375,10 +380,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 break;
             }
             tc_fence_after();
-            const int r = t.mt * C::BMT + half * BM + q * 32 + lane;
-            const bool half_live = t.mt * C::BMT + half * BM < t.mrows;   // warp-uniform
+            const int hrow0 = t.mt * C::BMT + half * BM;                  // first row of this half
+            const bool half_live = hrow0 < t.mrows;                       // warp-uniform
             if (half_live) {
-                const bool row_ok = r < t.mrows;
+                // M = 64 halves keep row 16q + i in lane 32q + i (i < 16)
+                const bool m64 = t.mrows - hrow0 <= kTailRows;
+                const int r = m64 ? hrow0 + q * 16 + lane : hrow0 + q * 32 + lane;
+                const bool row_ok = (!m64 || lane < 16) && r < t.mrows;
                 __nv_bfloat16* orow = p.out + (size_t)(t.row0 + (row_ok ? r : 0)) * p.ldo +
                                       (size_t)t.g * p.out_group_col;
                 const uint32_t tbase =
