@@ -19,18 +19,23 @@
 //   warps 2..  read the accumulator with tcgen05.ld (one TMEM lane = one row
 //              per thread), apply the activation, round to BF16 and store,
 //              masking rows past the bucket end and columns past N.
-// Two shapes of the same kernel (HALVES):
-//   1: 128-row tiles, two 256-column accumulators in TMEM so the epilogue of
-//      one tile overlaps the main loop of the next; 4 stages of 48 KiB;
-//      4 epilogue warps.  For short K (the down projection).
-//   2: 256-row tiles as two 128-row halves sharing every B tile (two MMAs per
-//      K slice into the two 256-column accumulators), which cuts the operand
-//      traffic per FLOP by a third; a tail whose second half is empty loads
-//      and multiplies only the first.  3 stages of 64 KiB; the epilogue (8
-//      warps, one half each) is not overlapped.  For long K (the up projection).
-// SwiGLU tiles load 128 gate rows and the matching 128 up rows as the two
-// halves of the 256-row B tile, so gate and up land side by side in one
-// accumulator and the epilogue computes silu(g) * u without a second pass.
+// Three tile shapes, chosen per launch:
+//   * CTA pair (groups averaging >= 256 rows, e.g. the large layer's experts):
+//     two SMs share a 256-row tile through tcgen05.mma.cta_group::2, each
+//     loading its own A rows and half of B -- see grouped_gemm_pair_kernel.
+//   * single CTA, HALVES = 1 (fewer rows per group, K < 4096): 128-row tiles,
+//     two 256-column accumulators in TMEM so the epilogue of one tile overlaps
+//     the main loop of the next; 4 stages of 48 KiB; 4 epilogue warps.
+//   * single CTA, HALVES = 2 (fewer rows per group, K >= 4096): 256-row tiles as
+//     two 128-row halves sharing every B tile (two MMAs per K slice into the two
+//     accumulators), which cuts the operand traffic per FLOP by a third; a tail
+//     whose second half is empty loads and multiplies only the first.  3 stages
+//     of 64 KiB; the epilogue (8 warps, one half each) is not overlapped.
+// A 128-row accumulator with 64 rows or fewer in its tile uses M = 64 MMAs.
+// In the single-CTA shapes a SwiGLU B tile is 128 gate rows and the matching
+// 128 up rows, so gate and up land side by side in one accumulator and the
+// epilogue computes silu(g) * u without a second pass (the pair kernel splits
+// them as two [64 gate | 64 up] halves, one per CTA).
 //
 // Every wait is bounded; on a timeout the CTA stops issuing work, drains its
 // in-flight tensor-core work, frees TMEM, raises MOE_ERR_TIMEOUT and returns.
@@ -61,6 +66,10 @@ constexpr int kTailRows = 64;
 constexpr int MAX_DYN_SMEM = 212 * 1024;
 // Reductions at least this long use the 256-row tile (HALVES = 2).
 constexpr long long kLongK = 4096;
+// Groups averaging at least this many rows use the CTA-pair kernel (compute
+// bound: the halved operand traffic pays); fewer rows per group -- weight
+// streaming at decode or at a few hundred tokens -- use the single-CTA shapes.
+constexpr long long kPairRows = 256;
 
 template <int HALVES>
 struct Cfg {
@@ -103,9 +112,15 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 
 struct Tile { int g, mt, nt, row0, mrows; };
 
-// Largest g with prefix[g] <= tile (empty groups share their prefix value).
+// Tile order inside a group: bands of kRasterBand column tiles, row tiles
+// fastest inside a band.  The CTAs running at the same time then share a few
+// weight tiles across many row tiles, which keeps fewer distinct bytes live in
+// L2 than walking all column tiles of one row tile first.
+constexpr int kRasterBand = 8;
+
+// Group = largest g with prefix[g] <= tile (empty groups share their prefix value).
 __device__ __forceinline__ Tile decode_tile(int tile, const int* prefix, const int* rstart, const int* rcount,
-                                            const KParams& p, int ntn) {
+                                            const KParams& p, int ntn, int bmt) {
     int lo = 0, hi = p.groups;
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
@@ -114,74 +129,67 @@ __device__ __forceinline__ Tile decode_tile(int tile, const int* prefix, const i
     Tile t;
     t.g = lo;
     const int local = tile - prefix[lo];
-    t.mt = local / ntn;
-    t.nt = local - t.mt * ntn;
+    const int mtiles = (rcount[lo] + bmt - 1) / bmt;
+    const int band = local / (mtiles * kRasterBand);
+    const int idx = local - band * mtiles * kRasterBand;
+    t.mt = idx % mtiles;
+    t.nt = band * kRasterBand + idx / mtiles;
     t.row0 = rstart[lo];
     t.mrows = rcount[lo];
     return t;
 }
 
-// Epilogue of one 128-row accumulator: this warp's 32 TMEM lanes at `tbase`,
-// one row per thread; writes the tile's BN_OUT output columns from col_base.
+// One 32-column chunk of the epilogue for this thread's row: read the
+// accumulator columns at `tg` (and the matching up columns at `tu` for SwiGLU),
+// apply the activation, round to BF16 and store output columns col0..col0+31
+// (whole 16-byte groups below N; N is a multiple of 8).
+template <int MODE>
+__device__ __forceinline__ void epilogue_chunk(uint32_t tg, uint32_t tu, bool row_ok, __nv_bfloat16* orow,
+                                               int col0, int N) {
+    uint32_t gv[32], uv[32];
+    tmem_ld_32cols(tg, gv);
+    if (MODE == kGemmSwiGLU) tmem_ld_32cols(tu, uv);
+    tmem_ld_wait();
+    if (!row_ok) return;
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+        if (col0 + v * 8 < N) {
+            uint32_t o[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                float a[2];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const float x = __uint_as_float(gv[v * 8 + 2 * i + h]);
+                    if (MODE == kGemmSwiGLU) {
+                        const float u = __uint_as_float(uv[v * 8 + 2 * i + h]);
+                        a[h] = x / (1.0f + __expf(-x)) * u;
+                    } else if (MODE == kGemmReLU2) {
+                        a[h] = x > 0.f ? x * x : 0.f;
+                    } else {
+                        a[h] = x;
+                    }
+                }
+                o[i] = pack2(a[0], a[1]);
+            }
+            *reinterpret_cast<uint4*>(orow + col0 + v * 8) = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+    }
+}
+
+// Epilogue of one 128-row accumulator of the single-CTA kernel: this warp's 32
+// TMEM lanes at `tbase`, one row per thread.  SwiGLU accumulators hold 128 gate
+// columns then the 128 matching up columns.
 template <int MODE>
 __device__ __forceinline__ void epilogue_rows(uint32_t tbase, bool row_ok, __nv_bfloat16* orow, int col_base,
                                               int N) {
     if (MODE == kGemmSwiGLU) {
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-            uint32_t gv[32], uv[32];
-            tmem_ld_32cols(tbase + c * 32, gv);
-            tmem_ld_32cols(tbase + 128 + c * 32, uv);
-            tmem_ld_wait();
-            const int col0 = col_base + c * 32;
-            if (row_ok) {
-#pragma unroll
-                for (int v = 0; v < 4; ++v) {
-                    if (col0 + v * 8 < N) {
-                        uint32_t o[4];
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            float hv[2];
-#pragma unroll
-                            for (int h = 0; h < 2; ++h) {
-                                const float g = __uint_as_float(gv[v * 8 + 2 * i + h]);
-                                const float u = __uint_as_float(uv[v * 8 + 2 * i + h]);
-                                hv[h] = g / (1.0f + __expf(-g)) * u;
-                            }
-                            o[i] = pack2(hv[0], hv[1]);
-                        }
-                        *reinterpret_cast<uint4*>(orow + col0 + v * 8) = make_uint4(o[0], o[1], o[2], o[3]);
-                    }
-                }
-            }
-        }
+        for (int c = 0; c < 4; ++c)
+            epilogue_chunk<MODE>(tbase + c * 32, tbase + 128 + c * 32, row_ok, orow, col_base + c * 32, N);
     } else {
 #pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
-            uint32_t av[32];
-            tmem_ld_32cols(tbase + c * 32, av);
-            tmem_ld_wait();
-            const int col0 = col_base + c * 32;
-            if (row_ok) {
-#pragma unroll
-                for (int v = 0; v < 4; ++v) {
-                    if (col0 + v * 8 < N) {
-                        uint32_t o[4];
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            float a0 = __uint_as_float(av[v * 8 + 2 * i]);
-                            float a1 = __uint_as_float(av[v * 8 + 2 * i + 1]);
-                            if (MODE == kGemmReLU2) {
-                                a0 = a0 > 0.f ? a0 * a0 : 0.f;
-                                a1 = a1 > 0.f ? a1 * a1 : 0.f;
-                            }
-                            o[i] = pack2(a0, a1);
-                        }
-                        *reinterpret_cast<uint4*>(orow + col0 + v * 8) = make_uint4(o[0], o[1], o[2], o[3]);
-                    }
-                }
-            }
-        }
+        for (int c = 0; c < 8; ++c) epilogue_chunk<MODE>(tbase + c * 32, 0, row_ok, orow, col_base + c * 32, N);
     }
 }
 
@@ -283,7 +291,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             uint32_t ph = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-                const Tile t = decode_tile(tile, prefix, rstart, rcount, p, ntn);
+                const Tile t = decode_tile(tile, prefix, rstart, rcount, p, ntn, C::BMT);
                 const int a_row = t.row0 + t.mt * C::BMT;
                 const bool second = HALVES == 2 && (t.mt * C::BMT + BM < t.mrows);
                 const uint32_t bytes = (second ? 2 : 1) * A_BYTES + B_BYTES;
@@ -322,7 +330,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             uint32_t aph = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-                const Tile t = decode_tile(tile, prefix, rstart, rcount, p, ntn);
+                const Tile t = decode_tile(tile, prefix, rstart, rcount, p, ntn, C::BMT);
                 const int rows0 = t.mrows - t.mt * C::BMT;                  // rows from the first half on
                 const bool second = HALVES == 2 && rows0 > BM;
                 const uint32_t idesc0 = rows0 <= kTailRows ? IDESC64 : IDESC;
@@ -371,7 +379,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         int acc = 0;
         uint32_t aph = 0;
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-            const Tile t = decode_tile(tile, prefix, rstart, rcount, p, ntn);
+            const Tile t = decode_tile(tile, prefix, rstart, rcount, p, ntn, C::BMT);
             if (!mbar_wait_bounded(smem_u32(&ctl->tfull[acc]), aph, abort)) {
                 if (lane == 0) {
                     raise_status(p.hdr, MOE_ERR_TIMEOUT);
@@ -409,6 +417,272 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     }
 }
 
+// ---------------------------------------------------------------------------
+// The CTA-pair shape.  A cluster of two CTAs (two SMs) owns a 256-row tile:
+// each CTA TMA-loads its own 128 A rows and its half of the 256-row B tile
+// (gate rows in CTA 0 and up rows in CTA 1 for SwiGLU), so a CTA moves 32 KiB
+// per 64-wide K step instead of 48, and six stages fit.  The leader CTA's MMA
+// thread issues tcgen05.mma.cta_group::2 (M 256, N 256; M 128 -- 64 rows per
+// CTA -- for a tile of 128 rows or fewer) reading both CTAs' shared memory and
+// writing both CTAs' TMEM; its commits arrive on the same barrier offsets in
+// both CTAs.  Each CTA keeps two 256-column accumulators, so the epilogue of
+// one tile overlaps the next tile's main loop.  Both CTAs' TMA loads count on
+// the leader's stage barrier; both CTAs' epilogues release the leader's
+// accumulator barrier.  No multicast load: each CTA reads only its own part.
+// ---------------------------------------------------------------------------
+constexpr int P_STAGES = 6;
+constexpr int P_STAGE_BYTES = A_BYTES + B_HALF_BYTES;   // 32 KiB per CTA
+constexpr int P_THREADS = 192;
+constexpr int P_BMT = 256;
+constexpr uint32_t P_IDESC_FULL = idesc_bf16_f32(256, BN_MMA);
+constexpr uint32_t P_IDESC_TAIL = idesc_bf16_f32(128, BN_MMA);
+
+struct PairCtl {
+    unsigned long long full[P_STAGES];
+    unsigned long long empty[P_STAGES];
+    unsigned long long tfull[2];
+    unsigned long long tempty[2];
+    unsigned long long drain;
+    uint32_t tmem_base;
+    int abort;
+    int total_tiles;
+};
+
+template <int MODE>
+__global__ void __launch_bounds__(P_THREADS, 1)
+grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                         const KParams p) {
+    constexpr int BN_OUT = (MODE == kGemmSwiGLU) ? 128 : 256;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_u32 = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + ((1024u - (raw_u32 & 1023u)) & 1023u);
+    PairCtl* ctl = reinterpret_cast<PairCtl*>(smem + P_STAGES * P_STAGE_BYTES);
+    int* prefix = reinterpret_cast<int*>(ctl + 1);
+    int* rstart = prefix + (p.groups + 1);
+    int* rcount = rstart + p.groups;
+    const uint32_t smem_base = smem_u32(smem);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t rank = cluster_ctarank();                 // 0: leader, 1: peer
+    const int pair = (int)(blockIdx.x >> 1), npairs = (int)(gridDim.x >> 1);
+    const int ntn = (p.N + BN_OUT - 1) / BN_OUT;
+
+    if (tid == 0) {
+        for (int s = 0; s < P_STAGES; ++s) {
+            mbar_init(smem_u32(&ctl->full[s]), 1);
+            mbar_init(smem_u32(&ctl->empty[s]), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(smem_u32(&ctl->tfull[a]), 1);
+            mbar_init(smem_u32(&ctl->tempty[a]), 8);            // 4 epilogue warps x 2 CTAs
+        }
+        mbar_init(smem_u32(&ctl->drain), 1);
+        ctl->abort = 0;
+        fence_mbar_init();
+        fence_proxy_async_smem();
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_u32(&ctl->tmem_base), TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    for (int g = tid; g < p.groups; g += P_THREADS) {
+        if (p.offsets) {
+            int lo = p.offsets[g], hi = p.offsets[g + 1];
+            lo = lo < 0 ? 0 : (lo > p.a_rows ? p.a_rows : lo);
+            hi = hi < lo ? lo : (hi > p.a_rows ? p.a_rows : hi);
+            rstart[g] = lo;
+            rcount[g] = hi - lo;
+        } else {
+            rstart[g] = 0;
+            rcount[g] = p.rows_all;
+        }
+    }
+    __syncthreads();
+    {
+        const int n = p.groups;
+        const int per = (n + P_THREADS - 1) / P_THREADS;
+        const int g0 = tid * per;
+        int loc = 0;
+        for (int i = 0; i < per; ++i)
+            if (g0 + i < n) loc += ((rcount[g0 + i] + P_BMT - 1) / P_BMT) * ntn;
+        int inc = loc;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, inc, off);
+            if (lane >= off) inc += v;
+        }
+        __shared__ int wtot[P_THREADS / 32];
+        if (lane == 31) wtot[warp] = inc;
+        __syncthreads();
+        int run = inc - loc;
+        for (int w = 0; w < warp; ++w) run += wtot[w];
+        for (int i = 0; i < per; ++i) {
+            if (g0 + i < n) {
+                prefix[g0 + i] = run;
+                run += ((rcount[g0 + i] + P_BMT - 1) / P_BMT) * ntn;
+            }
+        }
+        if (tid == P_THREADS - 1) { prefix[n] = run; ctl->total_tiles = run; }
+    }
+    tc_fence_before();
+    __syncthreads();
+    // both CTAs' barriers are initialised before any cross-CTA arrive
+    cluster_sync();
+    tc_fence_after();
+    const uint32_t tmem_base = ctl->tmem_base;
+    const int total = ctl->total_tiles;
+    volatile int* abort = &ctl->abort;
+    const int nkb = (p.K + BK - 1) / BK;
+    const int nk = nkb * p.nseg;
+
+    if (warp == 0) {
+        // ---------------- TMA producer (both CTAs) ----------------
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            for (int tile = pair; tile < total && ok; tile += npairs) {
+                const Tile t = decode_tile(tile, prefix, rstart, rcount, p, ntn, P_BMT);
+                const bool tail = t.mrows - t.mt * P_BMT <= BM;
+                const int a_row = t.row0 + t.mt * P_BMT + (int)rank * (tail ? 64 : BM);
+                const int n0 = t.nt * BN_OUT;
+                // B half of this CTA: SwiGLU -- 64 gate rows and the matching 64 up
+                // rows of output columns n0 + 64*rank ..; otherwise 128 rows
+                const int b_row = t.g * p.b_group_rows + n0 + (int)rank * ((MODE == kGemmSwiGLU) ? 64 : 128);
+                for (int i = 0; i < nk; ++i) {
+                    const int seg = i / nkb, kb = i - seg * nkb;
+                    if (!mbar_wait_bounded(smem_u32(&ctl->empty[stage]), ph ^ 1u, abort)) { ok = false; break; }
+                    const uint32_t full_local = smem_u32(&ctl->full[stage]);
+                    const uint32_t full_leader = mapa_shared(full_local, 0);
+                    if (rank == 0) mbar_arrive_expect_tx(full_local, 2 * P_STAGE_BYTES);
+                    const uint32_t sa = smem_base + stage * P_STAGE_BYTES;
+                    tma_load_2d_pair(sa, &tmA, full_leader, seg * p.a_seg_col + kb * BK, a_row);
+                    if (MODE == kGemmSwiGLU) {   // two 64-row boxes: gate, then up
+                        tma_load_2d_pair(sa + A_BYTES, &tmB, full_leader, kb * BK, b_row + seg * p.b_seg_row);
+                        tma_load_2d_pair(sa + A_BYTES + B_HALF_BYTES / 2, &tmB, full_leader, kb * BK,
+                                         b_row + p.up_off + seg * p.b_seg_row);
+                    } else {
+                        tma_load_2d_pair(sa + A_BYTES, &tmB, full_leader, kb * BK, b_row + seg * p.b_seg_row);
+                    }
+                    if (++stage == P_STAGES) { stage = 0; ph ^= 1u; }
+                }
+            }
+            if (!ok) {
+                const unsigned long long t0 = globaltimer_ns();
+                while (globaltimer_ns() - t0 < 1000000ull) { }
+                raise_status(p.hdr, MOE_ERR_TIMEOUT);
+                p.hdr->timeout_site = kSiteGemmProducer;
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer (leader CTA) ----------------
+        if (lane == 0 && rank == 0) {
+            int stage = 0;
+            uint32_t ph = 0;
+            int acc = 0;
+            uint32_t aph = 0;
+            bool ok = true;
+            for (int tile = pair; tile < total && ok; tile += npairs) {
+                const Tile t = decode_tile(tile, prefix, rstart, rcount, p, ntn, P_BMT);
+                const bool tail = t.mrows - t.mt * P_BMT <= BM;
+                const uint32_t idesc = tail ? P_IDESC_TAIL : P_IDESC_FULL;
+                if (!mbar_wait_bounded(smem_u32(&ctl->tempty[acc]), aph ^ 1u, abort)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t d = tmem_base + (uint32_t)(acc * BN_MMA);
+                for (int i = 0; i < nk; ++i) {
+                    if (!mbar_wait_bounded(smem_u32(&ctl->full[stage]), ph, abort)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t sa = smem_base + stage * P_STAGE_BYTES;
+                    const uint64_t ad = sdesc_k_sw128(sa);
+                    const uint64_t bd = sdesc_k_sw128(sa + A_BYTES);
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk)
+                        tc_mma_bf16_pair(d, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc,
+                                         (i > 0 || kk > 0) ? 1u : 0u);
+                    tc_commit_pair_mc(smem_u32(&ctl->empty[stage]), (uint16_t)3);
+                    if (++stage == P_STAGES) { stage = 0; ph ^= 1u; }
+                }
+                if (!ok) break;
+                tc_commit_pair_mc(smem_u32(&ctl->tfull[acc]), (uint16_t)3);
+                acc ^= 1;
+                if (acc == 0) aph ^= 1u;
+            }
+            tc_commit_pair(smem_u32(&ctl->drain));
+            volatile int never = 0;
+            const bool drained = mbar_wait_bounded(smem_u32(&ctl->drain), 0, &never);
+            if (!ok || !drained) {
+                raise_status(p.hdr, MOE_ERR_TIMEOUT);
+                p.hdr->timeout_site = kSiteGemmMma;
+                *abort = 1;
+            }
+        }
+    } else {
+        // ---------------- epilogue (warps 2..5, both CTAs) ----------------
+        const int q = warp & 3;
+        int acc = 0;
+        uint32_t aph = 0;
+        for (int tile = pair; tile < total; tile += npairs) {
+            const Tile t = decode_tile(tile, prefix, rstart, rcount, p, ntn, P_BMT);
+            const bool tail = t.mrows - t.mt * P_BMT <= BM;
+            if (!mbar_wait_bounded(smem_u32(&ctl->tfull[acc]), aph, abort)) {
+                if (lane == 0) {
+                    raise_status(p.hdr, MOE_ERR_TIMEOUT);
+                    p.hdr->timeout_site = kSiteGemmEpilogue;
+                }
+                break;
+            }
+            tc_fence_after();
+            // D columns 0..127 come from CTA 0's B half, 128..255 from CTA 1's.
+            // Full tile (M 256): this CTA's 128 rows, lane = row, all 256 columns.
+            // Tail (M 128): this CTA's 64 rows; lanes 0..63 hold columns 0..127 and
+            // lanes 64..127 the same rows' columns 128..255.
+            const int bb = tail ? (q >> 1) : 0;                            // column block of the lanes
+            const int rin = tail ? (int)rank * 64 + (q & 1) * 32 + lane : (int)rank * BM + q * 32 + lane;
+            const int r = t.mt * P_BMT + rin;
+            const bool live = t.mt * P_BMT + (tail ? (int)rank * 64 + (q & 1) * 32 : (int)rank * BM + q * 32) < t.mrows;
+            if (live) {
+                const bool row_ok = r < t.mrows;
+                __nv_bfloat16* orow = p.out + (size_t)(t.row0 + (row_ok ? r : 0)) * p.ldo +
+                                      (size_t)t.g * p.out_group_col;
+                const uint32_t tl = tmem_base + (uint32_t)(acc * BN_MMA) + ((uint32_t)(q * 32) << 16);
+                const int n0 = t.nt * BN_OUT;
+                if (MODE == kGemmSwiGLU) {
+                    // each 128-column block is [64 gate | 64 up] of output columns 64 * block ..
+                    const int nblk = tail ? 1 : 2;
+#pragma unroll 1
+                    for (int b = 0; b < nblk; ++b)
+#pragma unroll 1
+                        for (int i0 = 0; i0 < 64; i0 += 32)
+                            epilogue_chunk<MODE>(tl + b * 128 + i0, tl + b * 128 + 64 + i0, row_ok, orow,
+                                                 n0 + 64 * (b + bb) + i0, p.N);
+                } else {
+                    const int nch = tail ? 4 : 8;
+#pragma unroll 1
+                    for (int c = 0; c < nch; ++c)
+                        epilogue_chunk<MODE>(tl + c * 32, 0, row_ok, orow, n0 + 128 * bb + c * 32, p.N);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&ctl->tempty[acc]), 0));
+            acc ^= 1;
+            if (acc == 0) aph ^= 1u;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    // the leader's MMAs have drained before either CTA frees its TMEM
+    cluster_sync();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    }
+}
+
 // ---- host side ---------------------------------------------------------------
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -424,8 +698,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// Row-major [rows, cols] BF16, 64 x 128 boxes, 128-byte swizzle, zero fill out of bounds.
-bool make_map(CUtensorMap* m, const void* base, long long rows, long long cols) {
+// Row-major [rows, cols] BF16, 64-column x box_rows boxes, 128-byte swizzle, zero fill out of bounds.
+bool make_map(CUtensorMap* m, const void* base, long long rows, long long cols, unsigned box_rows = 128) {
     auto enc = encode_fn();
     if (!enc) {
         set_error("cuTensorMapEncodeTiled is not available from the driver");
@@ -433,7 +707,7 @@ bool make_map(CUtensorMap* m, const void* base, long long rows, long long cols) 
     }
     cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-    cuuint32_t box[2] = {(cuuint32_t)BK, 128u};
+    cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1u, 1u};
     const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
                            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -465,6 +739,40 @@ cudaError_t launch_mode(const CUtensorMap& ma, const CUtensorMap& mb, const KPar
     return e;
 }
 
+template <int MODE>
+cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const KParams& kp, size_t smem,
+                        cudaStream_t st) {
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [] {
+        attr_err = cudaFuncSetAttribute(grouped_gemm_pair_kernel<MODE>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, MAX_DYN_SMEM);
+    });
+    if (attr_err != cudaSuccess) {
+        set_error("cudaFuncSetAttribute(max dynamic smem %d): %s", MAX_DYN_SMEM, cudaGetErrorString(attr_err));
+        return attr_err;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(device_sm_count() & ~1), 1, 1);
+    cfg.blockDim = dim3(P_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel<MODE>, ma, mb, kp);
+    if (e != cudaSuccess) set_error("grouped GEMM pair launch (smem %zu): %s", smem, cudaGetErrorString(e));
+    return e;
+}
+
+size_t pair_smem_bytes(int groups) {
+    return 1024 + (size_t)P_STAGES * P_STAGE_BYTES + sizeof(PairCtl) + 3 * (size_t)(groups + 1) * 4;
+}
+
 template <int HALVES>
 size_t smem_bytes(int groups) {
     return 1024 + (size_t)Cfg<HALVES>::STAGES * Cfg<HALVES>::STAGE_BYTES + sizeof(SmemCtl<HALVES>) +
@@ -478,9 +786,13 @@ moe_status launch_grouped_gemm(const GemmProblem& g, WsHeader* hdr, cudaStream_t
         set_error("grouped GEMM: unsupported problem (groups %d, K %d, N %d)", g.groups, g.K, g.N);
         return MOE_ERR_UNSUPPORTED;
     }
+    const long long avg_rows = g.offsets ? g.a_rows / g.groups : g.rows_all;
+    const bool pairs = avg_rows >= kPairRows && device_sm_count() >= 2;
     CUtensorMap ma, mb;
     if (!make_map(&ma, g.a, g.a_rows, g.a_cols)) return MOE_ERR_CUDA;
-    if (!make_map(&mb, g.b, g.b_rows, g.b_cols)) return MOE_ERR_CUDA;
+    // the pair kernel loads a SwiGLU B half as 64 gate rows + 64 up rows
+    if (!make_map(&mb, g.b, g.b_rows, g.b_cols, (pairs && g.mode == kGemmSwiGLU) ? 64u : 128u))
+        return MOE_ERR_CUDA;
     KParams kp;
     kp.offsets = g.offsets;
     kp.groups = g.groups;
@@ -497,6 +809,20 @@ moe_status launch_grouped_gemm(const GemmProblem& g, WsHeader* hdr, cudaStream_t
     kp.ldo = g.ldo;
     kp.out_group_col = g.out_group_col;
     kp.hdr = hdr;
+    if (pairs) {
+        const size_t smem = pair_smem_bytes(g.groups);
+        if (smem > (size_t)MAX_DYN_SMEM) {
+            set_error("grouped GEMM needs %zu bytes of shared memory", smem);
+            return MOE_ERR_UNSUPPORTED;
+        }
+        cudaError_t e;
+        switch (g.mode) {
+            case kGemmSwiGLU: e = launch_pair<kGemmSwiGLU>(ma, mb, kp, smem, st); break;
+            case kGemmReLU2: e = launch_pair<kGemmReLU2>(ma, mb, kp, smem, st); break;
+            default: e = launch_pair<kGemmPlain>(ma, mb, kp, smem, st); break;
+        }
+        return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+    }
     // Long reductions amortise the un-overlapped epilogue of the 256-row
     // tile; short ones keep the double-buffered 128-row tile.
     const int halves = (long long)g.K * g.nseg >= kLongK ? 2 : 1;

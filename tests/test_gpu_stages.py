@@ -38,6 +38,12 @@ SMALL = {
     "longk": synth.Workload("longk", 300, 4096, 4, 2, 136),
     "longk_relu2": synth.Workload("longk_relu2", 200, 4160, 3, 2, 264, act=synth.ACT_RELU2),
     "longk_shared": synth.Workload("longk_shared", 40, 4096, 6, 2, 64, shared=4, shared_inter=1024),
+    # 256 or more rows per group take the CTA-pair kernel: full 256-row tiles,
+    # 128-row tails, ragged N and K, ReLU^2, long K, shared experts
+    "pair_swiglu": synth.Workload("pair_swiglu", 640, 256, 4, 2, 200),
+    "pair_relu2": synth.Workload("pair_relu2", 600, 200, 3, 2, 264, act=synth.ACT_RELU2),
+    "pair_shared": synth.Workload("pair_shared", 300, 128, 2, 2, 64, shared=2, shared_inter=72),
+    "pair_longk": synth.Workload("pair_longk", 300, 4096, 2, 2, 136),
 }
 for _n in DECODE:
     SMALL[_n] = W[_n]
