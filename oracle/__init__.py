@@ -33,6 +33,19 @@ ST_CAPACITY = 3
 ST_NONFINITE = 4
 
 
+def variant(lib_path: str, src_path: str):
+    """A second instance of this module bound to another build of the oracle
+    (used by the test that plants mistakes in copies of the oracle source)."""
+    import importlib.util
+    spec = importlib.util.spec_from_file_location(f"oracle_variant_{abs(hash(lib_path))}", __file__)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    mod._LIB_PATH = lib_path
+    mod._SRC = src_path
+    mod._lib = None
+    return mod
+
+
 def build(force: bool = False) -> str:
     """Compile the oracle with the host C++ compiler (no CUDA involved)."""
     if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
