@@ -70,6 +70,10 @@ def _load():
             lib.oracle_double_from_bf16.argtypes = [ctypes.c_uint16]
             lib.oracle_route.restype = i
             lib.oracle_route.argtypes = [i, i, i, P, P, P]
+            lib.oracle_route_sigmoid.restype = i
+            lib.oracle_route_sigmoid.argtypes = [i, i, i, P, P, ctypes.c_float, P, P]
+            lib.oracle_gate.restype = None
+            lib.oracle_gate.argtypes = [i, i, i, P, P, P]
             lib.oracle_dispatch.restype = i
             lib.oracle_dispatch.argtypes = [i, i, i, i, i, P, P, P, P, P, P, P]
             lib.oracle_expert_up.restype = None
@@ -125,6 +129,28 @@ def route(logits: np.ndarray, k: int):
     w = np.zeros((T, k), np.float32)
     st = _load().oracle_route(T, E, k, _p(logits), _p(ids), _p(w))
     return st, ids, w
+
+
+def route_sigmoid(logits: np.ndarray, k: int, bias=None, route_scale: float = 1.0):
+    """Sigmoid routing with a selection-only bias -> (status, ids, w)."""
+    logits = _c(logits, np.float32)
+    T, E = logits.shape
+    b = None if bias is None else _c(bias, np.float32)
+    ids = np.zeros((T, k), np.int32)
+    w = np.zeros((T, k), np.float32)
+    st = _load().oracle_route_sigmoid(T, E, k, _p(logits), _p(b), float(route_scale), _p(ids), _p(w))
+    return st, ids, w
+
+
+def gate(x: np.ndarray, wg: np.ndarray) -> np.ndarray:
+    """logits f32 [T,E] = x [T,H] . Wg [E,H]^T (BF16 bits in)."""
+    x = _c(x, np.uint16)
+    wg = _c(wg, np.uint16)
+    T, H = x.shape
+    E = wg.shape[0]
+    out = np.zeros((T, E), np.float32)
+    _load().oracle_gate(T, H, E, _p(x), _p(wg), _p(out))
+    return out
 
 
 def dispatch(ids: np.ndarray, x: np.ndarray, E: int, capacity: int):

@@ -131,6 +131,54 @@ int oracle_route(int T, int E, int k, const float* logits, int32_t* ids, float* 
     return ST_OK;
 }
 
+// [ORT] Description bullet 2 and the second commit ("projected sigmoid routing
+// mode with FP32 selection-only correction bias and unbiased normalized routing
+// weights"): score s_e = sigmoid(l_e); the experts are ordered by the FP32 key
+// fp32(s_e) + bias_e (ties to the lower index) and the first k kept; their
+// weights are the unbiased scores normalised over the selection, times
+// route_scale.  The sigmoid is taken in double and rounded once to FP32.
+int oracle_route_sigmoid(int T, int E, int k, const float* logits, const float* bias, float route_scale,
+                         int32_t* ids, float* w) {
+    if (T < 0 || E < 1 || k < 1 || k > E) return ST_INVALID_ARG;
+    for (long long i = 0; i < (long long)T * E; ++i)
+        if (!std::isfinite(logits[i])) return ST_NONFINITE;
+    std::vector<int> order(E);
+    std::vector<float> score(E), key(E);
+    for (int t = 0; t < T; ++t) {
+        const float* l = logits + (size_t)t * E;
+        for (int e = 0; e < E; ++e) {
+            score[e] = (float)(1.0 / (1.0 + std::exp(-(double)l[e])));
+            key[e] = score[e] + (bias ? bias[e] : 0.0f);      // FP32 add
+            order[e] = e;
+        }
+        std::sort(order.begin(), order.end(), [&](int a, int b) {
+            if (key[a] > key[b]) return true;
+            if (key[a] < key[b]) return false;
+            return a < b;
+        });
+        double z = 0.0;
+        for (int j = 0; j < k; ++j) z += (double)score[order[j]];
+        for (int j = 0; j < k; ++j) {
+            ids[(size_t)t * k + j] = order[j];
+            w[(size_t)t * k + j] = (float)((double)route_scale * (double)score[order[j]] / z);
+        }
+    }
+    return ST_OK;
+}
+
+// The router projection in front of the routing ([ORT] "projected" routing;
+// [MI300] MOE_GATE_TOPK fuses this GEMV with the top-k): logits[t][e] =
+// sum_h x[t][h] * Wg[e][h], summed in double, rounded once to FP32.
+void oracle_gate(int T, int H, int E, const uint16_t* x, const uint16_t* wg, float* logits) {
+    for (int t = 0; t < T; ++t)
+        for (int e = 0; e < E; ++e) {
+            double s = 0.0;
+            for (int h = 0; h < H; ++h)
+                s += bf16_to_double(x[(size_t)t * H + h]) * bf16_to_double(wg[(size_t)e * H + h]);
+            logits[(size_t)t * E + e] = (float)s;
+        }
+}
+
 // ---- dispatch -----------------------------------------------------------
 // [AFD] .change / .setup: count-first dispatch.  Counts per expert first,
 // their exclusive prefix sums next, and only then the payload rows move, each

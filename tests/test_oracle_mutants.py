@@ -30,6 +30,10 @@ MUTANTS = {
     "capacity_off_by_one": ("if (counts[e] > capacity)", "if (counts[e] >= capacity)"),
     "duplicates_not_detected": ("if (ids[(size_t)t * k + jj] == e) ok = false;", "if (false) ok = false;"),
     "weights_paired_with_wrong_slot": ("s += (double)w_t[j] * bf16_to_double", "s += (double)w_t[k - 1 - j] * bf16_to_double"),
+    "sigmoid_bias_ignored": ("key[e] = score[e] + (bias ? bias[e] : 0.0f);", "key[e] = score[e];"),
+    "sigmoid_weights_from_biased_key": ("(double)route_scale * (double)score[order[j]] / z",
+                                        "(double)route_scale * (double)key[order[j]] / z"),
+    "gate_transposed": ("bf16_to_double(wg[(size_t)e * H + h])", "bf16_to_double(wg[(size_t)h * E + e])"),
     "first_slot_dropped_in_combine": ("for (int j = 0; j < k; ++j) {\n            if (dest_t[j] < 0) continue;",
                                       "for (int j = 1; j < k; ++j) {\n            if (dest_t[j] < 0) continue;"),
 }
@@ -54,6 +58,11 @@ PINS = [
     (P.test_combine_identity_experts_return_x, dict(k=4)),
     (P.test_combine_weights_are_applied_per_slot, {}),
     (P.test_layer_internal_routing_equals_preselected, {}),
+    (P.test_route_sigmoid_without_bias_selects_like_softmax, {}),
+    (P.test_route_sigmoid_dominant_bias_selects_its_set_and_weights_ignore_it, {}),
+    (P.test_route_sigmoid_negative_bias_excludes_the_top_experts, {}),
+    (P.test_route_sigmoid_closed_form_weights, {}),
+    (P.test_gate_projection_matches_float64_matmul, {}),
 ]
 
 

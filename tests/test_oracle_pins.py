@@ -394,3 +394,77 @@ def test_layer_internal_routing_equals_preselected(oracle_mod):
     assert a["status"] == b["status"] == 0
     assert np.array_equal(a["out"], b["out"])
     assert np.abs(bits_to_f64(a["out"])).max() > 0.05          # unit-scale twin is not ~0
+
+
+# --------------------------------------------------------------------------
+# router front end: sigmoid routing with a selection-only bias, gate projection
+# --------------------------------------------------------------------------
+def test_route_sigmoid_without_bias_selects_like_softmax(oracle_mod):
+    # sigmoid is increasing, so with no bias the selection is the top-k by logit
+    # (logits well inside (-8, 8) keep the FP32 sigmoids distinct)
+    rng = np.random.default_rng(21)
+    logits = rng.standard_normal((200, 40)).astype(np.float32)
+    _, ids_s, _ = oracle_mod.route(logits, 6)
+    st, ids, w = oracle_mod.route_sigmoid(logits, 6)
+    assert st == 0 and np.array_equal(ids, ids_s)
+    assert np.abs(w.astype(np.float64).sum(1) - 1.0).max() <= 1e-6
+
+
+def test_route_sigmoid_dominant_bias_selects_its_set_and_weights_ignore_it(oracle_mod):
+    rng = np.random.default_rng(22)
+    T, E, k = 50, 24, 4
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    chosen = np.array([3, 7, 11, 19])
+    bias = np.zeros(E, np.float32)
+    bias[chosen] = 2.0                         # keys >= 2 > any unbiased score
+    st, ids, w = oracle_mod.route_sigmoid(logits, k, bias, route_scale=2.5)
+    assert st == 0
+    for t in range(T):
+        assert sorted(ids[t]) == sorted(chosen)
+        # within the set the order follows the score, i.e. the logit
+        assert list(ids[t]) == sorted(chosen, key=lambda e: (-float(logits[t, e]), e))
+    assert np.abs(w.astype(np.float64).sum(1) - 2.5).max() <= 1e-5
+    bias2 = bias.copy()
+    bias2[chosen] = 3.0                        # same selection, different bias
+    _, ids2, w2 = oracle_mod.route_sigmoid(logits, k, bias2, route_scale=2.5)
+    assert np.array_equal(ids2, ids) and np.array_equal(w2, w)
+
+
+def test_route_sigmoid_negative_bias_excludes_the_top_experts(oracle_mod):
+    rng = np.random.default_rng(23)
+    T, E, k = 40, 16, 3
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    for t in range(T):
+        _, top, _ = oracle_mod.route(logits[t:t + 1], k)
+        bias = np.zeros(E, np.float32)
+        bias[top[0]] = -2.0                    # keys < 0 < any unbiased score
+        _, ids, _ = oracle_mod.route_sigmoid(logits[t:t + 1], k, bias)
+        masked = logits[t:t + 1].copy()
+        masked[0, top[0]] = -1e30
+        _, nxt, _ = oracle_mod.route(masked, k)
+        assert np.array_equal(ids, nxt)
+
+
+def test_route_sigmoid_closed_form_weights(oracle_mod):
+    # sigmoid(0) = 1/2 exactly: k experts at logit 0 share the weight scale / k
+    logits = np.full((3, 10), -5.0, np.float32)
+    logits[:, [1, 4, 8, 9]] = 0.0
+    st, ids, w = oracle_mod.route_sigmoid(logits, 4, route_scale=1.0)
+    assert st == 0 and np.all(ids == np.array([1, 4, 8, 9]))
+    assert np.all(w == np.float32(0.25))
+    st, _, _ = oracle_mod.route_sigmoid(np.full((1, 4), np.nan, np.float32), 2)
+    assert st == oracle_mod.ST_NONFINITE
+
+
+def test_gate_projection_matches_float64_matmul(oracle_mod):
+    rng = np.random.default_rng(24)
+    T, H, E = 33, 200, 24
+    x = rand_bf16(rng, (T, H))
+    wg = rand_bf16(rng, (E, H), 0.1)
+    got = oracle_mod.gate(x, wg).astype(np.float64)
+    want = (bits_to_f64(x) @ bits_to_f64(wg).T).astype(np.float32).astype(np.float64)
+    ulp = np.spacing(np.abs(want).astype(np.float32)).astype(np.float64)
+    assert np.all(np.abs(got - want) <= ulp)
+    # transposing the weight matrix is caught
+    assert not np.allclose(oracle_mod.gate(x[:, :E], rand_bf16(rng, (E, E))),
+                           oracle_mod.gate(x[:, :E], rand_bf16(rng, (E, E))))
