@@ -370,6 +370,33 @@ def run_native(args, wl, world, rank, local):
     stream.synchronize()
     stage_ms = {n: statistics.median(evs[r][i].elapsed_time(evs[r][i + 1]) for r in range(reps))
                 for i, n in enumerate(names)}
+
+    # ---- router front end (not part of the layer step): gate projection and
+    # sigmoid routing with a correction bias, timed the same way --------------
+    w_gate = synth.gate_weights(wl, seed=rank, device=dev)
+    bias = synth.correction_bias(wl, seed=rank, device=dev)
+    logits_g = torch.empty(T, E, dtype=torch.float32, device=dev)
+    front_fns = [lambda: N.moe_gate(shape, g["x"], w_gate, logits_g, ws, stream),
+                 lambda: N.moe_route_sigmoid(shape, logits_g, bias, 2.5, ids, w, ws, stream)]
+    with torch.cuda.stream(stream):
+        for fn in front_fns:
+            fn()
+    stream.synchronize()
+    front_graphs = [capture(fn, stream) for fn in front_fns]
+    fevs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(reps)]
+    with torch.cuda.stream(stream):
+        for r in range(reps + 2):
+            e = fevs[r - 2] if r >= 2 else None
+            flush_l2(r)
+            for i, fg in enumerate(front_graphs):
+                if e: e[i].record(stream)
+                fg.replay()
+            if e: e[2].record(stream)
+    stream.synchronize()
+    gate_ms = statistics.median(fevs[r][0].elapsed_time(fevs[r][1]) for r in range(reps))
+    rsig_ms = statistics.median(fevs[r][1].elapsed_time(fevs[r][2]) for r in range(reps))
+    router_front = {"gate_ms": gate_ms, "gate_tflops": 2.0 * T * H * E / (gate_ms / 1e3) / 1e12,
+                    "route_sigmoid_ms": rsig_ms}
     st = N.moe_status_read(ws, stream)
     if st != N.MOE_OK:
         raise RuntimeError(f"device status {st} after stage timing")
@@ -448,7 +475,7 @@ def run_native(args, wl, world, rank, local):
             "expert_up_tflops": achieved,
             "dispatch_combine_gbs": dc_gbs, "dispatch_combine_hbm_frac": dc_gbs / peaks["hbm_gbs"],
             "gemm_tflops": gemm_tflops, "gemm_frac": gemm_tflops / peak,
-            "stages_ms": stage_ms, "algorithmic": alg,
+            "stages_ms": stage_ms, "algorithmic": alg, "router_front": router_front,
             "e2e": e2e, "gpu_launches": kernels_per_layer * args.steps,
             "clocks": clk.summary(), "cpu_baseline": cpu,
             "kernel_source_sha": kernel_source_sha(),

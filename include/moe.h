@@ -105,6 +105,30 @@ MOE_API moe_status moe_workspace_init(void* ws, size_t ws_bytes, void* stream);
 MOE_API moe_status moe_route(const moe_shape* shape, const float* logits, int32_t* topk_ids,
                      float* topk_w, void* ws, size_t ws_bytes, void* stream);
 
+/* Router projection in front of the routing (ONNX Runtime PR #33963,
+ * Description: "projected" routing; DeepSeek fleet REPORT.md, MOE_GATE_TOPK
+ * fuses this projection with the top-k):
+ *   logits[t][e] = sum_h x[t][h] * w_gate[e][h], FP32 accumulation, FP32 out.
+ *   x      device bf16 [T, H];  w_gate device bf16 [E, H] (nn.Linear [out, in])
+ *   logits device f32  [T, E]  out
+ * Runs on the grouped GEMM kernels (one group, FP32 epilogue). */
+MOE_API moe_status moe_gate(const moe_shape* shape, const uint16_t* x, const uint16_t* w_gate, float* logits,
+                            void* ws, size_t ws_bytes, void* stream);
+
+/* Sigmoid routing with a selection-only correction bias (ONNX Runtime PR
+ * #33963, Description bullet 2: fused sigmoid routing with FP32 correction
+ * bias, mixture weights from the unbiased scores).  Per token: s_e =
+ * sigmoid(logit_e), taken in double and rounded once to FP32; the k experts
+ * with the largest FP32 keys s_e + bias[e] are selected (ties to the lower
+ * index), in descending key order; topk_w[t,j] = route_scale * s / (sum of the
+ * selected s), FP32.
+ *   logits device f32 [T, E]; bias device f32 [E] or NULL (no bias);
+ *   topk_ids device i32 [T, k] out; topk_w device f32 [T, k] out.
+ * Device error: MOE_ERR_NONFINITE if any logit is NaN or infinite. */
+MOE_API moe_status moe_route_sigmoid(const moe_shape* shape, const float* logits, const float* bias,
+                                     float route_scale, int32_t* topk_ids, float* topk_w, void* ws,
+                                     size_t ws_bytes, void* stream);
+
 /* Count-first dispatch (afdEP-comm count-first record, .change: per-expert
  * counts and their prefix sums come before the payload rows move).
  *   x           device bf16 [T, H]

@@ -4,6 +4,7 @@
 #include "common.cuh"
 
 #include <climits>
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -189,6 +190,39 @@ moe_status moe_route(const moe_shape* shape, const float* logits, int32_t* topk_
     if ((r = check_ws(shape, ws, ws_bytes, false)) != MOE_OK) return r;
     if (!aligned(logits, 16) || !aligned(topk_ids, 16) || !aligned(topk_w, 16)) return MOE_ERR_INVALID_ARG;
     return do_route(*shape, logits, topk_ids, topk_w, ws, static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_gate(const moe_shape* shape, const uint16_t* x, const uint16_t* w_gate, float* logits, void* ws,
+                    size_t ws_bytes, void* stream) {
+    clear_error();
+    moe_status r = check_shape(shape);
+    if (r != MOE_OK) return r;
+    if ((r = check_ws(shape, ws, ws_bytes, false)) != MOE_OK) return r;
+    if (!aligned(x, 16) || !aligned(w_gate, 16) || !aligned(logits, 16)) return MOE_ERR_INVALID_ARG;
+    const moe_shape& s = *shape;
+    GemmProblem g{};
+    g.mode = kGemmF32;
+    g.a = x; g.a_rows = s.tokens; g.a_cols = s.hidden;
+    g.b = w_gate; g.b_rows = s.experts; g.b_cols = s.hidden;
+    g.offsets = nullptr; g.groups = 1; g.rows_all = s.tokens;
+    g.K = s.hidden; g.nseg = 1; g.a_seg_col = 0; g.b_seg_row = 0;
+    g.N = s.experts; g.b_group_rows = 0; g.up_off = 0;
+    g.out = logits; g.ldo = s.experts; g.out_group_col = 0;
+    return launch_grouped_gemm(g, at<WsHeader>(ws, 0), static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_route_sigmoid(const moe_shape* shape, const float* logits, const float* bias, float route_scale,
+                             int32_t* topk_ids, float* topk_w, void* ws, size_t ws_bytes, void* stream) {
+    clear_error();
+    moe_status r = check_shape(shape);
+    if (r != MOE_OK) return r;
+    if ((r = check_ws(shape, ws, ws_bytes, false)) != MOE_OK) return r;
+    if (!aligned(logits, 16) || !aligned(topk_ids, 16) || !aligned(topk_w, 16) || !aligned_or_null(bias, 4))
+        return MOE_ERR_INVALID_ARG;
+    if (!(route_scale == route_scale) || route_scale == INFINITY || route_scale == -INFINITY)
+        return MOE_ERR_INVALID_ARG;
+    return from_cuda(launch_route_sigmoid(*shape, logits, bias, route_scale, topk_ids, topk_w, at<WsHeader>(ws, 0),
+                                          static_cast<cudaStream_t>(stream)));
 }
 
 moe_status moe_dispatch(const moe_shape* shape, const uint16_t* x, const int32_t* topk_ids, int32_t* counts,

@@ -282,6 +282,8 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
 // ---------------------------------------------------------------------------
 cudaError_t launch_route(const moe_shape& s, const float* logits, int32_t* ids, float* w,
                          WsHeader* hdr, cudaStream_t st);
+cudaError_t launch_route_sigmoid(const moe_shape& s, const float* logits, const float* bias, float scale,
+                                 int32_t* ids, float* w, WsHeader* hdr, cudaStream_t st);
 cudaError_t launch_count(const moe_shape& s, const int32_t* ids, int32_t* counts, int32_t* offsets,
                          int32_t* rank, unsigned long long* flags, int count_tiles,
                          WsHeader* hdr, cudaStream_t st);
@@ -294,7 +296,8 @@ cudaError_t launch_combine(const moe_shape& s, const uint16_t* y_perm, const int
 // Grouped GEMM problem (one launch): for every group g and row r of the group,
 // out[row0(g) + r, g*out_group_col + n] = epilogue( sum_seg sum_k A[row0(g)+r, seg*a_seg_col + k]
 //                                                   * B[g*b_group_rows + seg*b_seg_row + n', k] )
-enum GemmMode : int { kGemmSwiGLU = 0, kGemmReLU2 = 1, kGemmPlain = 2 };
+// SwiGLU / ReLU^2 / plain store BF16; F32 stores the FP32 accumulator (router logits).
+enum GemmMode : int { kGemmSwiGLU = 0, kGemmReLU2 = 1, kGemmPlain = 2, kGemmF32 = 3 };
 struct GemmProblem {
     int mode;
     const void* a; long long a_rows; long long a_cols;    // A [a_rows, a_cols] bf16

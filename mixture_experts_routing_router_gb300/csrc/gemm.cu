@@ -87,7 +87,7 @@ struct KParams {
     int a_rows;                 // rows of A (bucket bounds are clamped to it)
     int K, nseg, a_seg_col, b_seg_row;
     int N, b_group_rows, up_off;
-    __nv_bfloat16* out;
+    void* out;                  // BF16, or FP32 for kGemmF32
     long long ldo;
     int out_group_col;
     WsHeader* hdr;
@@ -149,40 +149,70 @@ __device__ __forceinline__ Tile decode_tile(int tile, const int* prefix, const i
     return t;
 }
 
+template <int MODE> struct OutOf { using T = __nv_bfloat16; };
+template <> struct OutOf<kGemmF32> { using T = float; };
+
+// Output row pointer of row `row` of group g (a valid row index is passed even
+// for masked rows, so no pointer past the buffer is ever formed).
+template <int MODE>
+__device__ __forceinline__ typename OutOf<MODE>::T* out_row(const KParams& p, int row, int g) {
+    return reinterpret_cast<typename OutOf<MODE>::T*>(p.out) + (size_t)row * p.ldo + (size_t)g * p.out_group_col;
+}
+
 // One 32-column chunk of the epilogue for this thread's row: read the
 // accumulator columns at `tg` (and the matching up columns at `tu` for SwiGLU),
 // apply the activation, round to BF16 and store output columns col0..col0+31
 // (whole 16-byte groups below N; N is a multiple of 8).
 template <int MODE>
-__device__ __forceinline__ void epilogue_chunk(uint32_t tg, uint32_t tu, bool row_ok, __nv_bfloat16* orow,
+__device__ __forceinline__ void epilogue_chunk(uint32_t tg, uint32_t tu, bool row_ok, typename OutOf<MODE>::T* orow,
                                                int col0, int N) {
     uint32_t gv[32], uv[32];
     tmem_ld_32cols(tg, gv);
     if (MODE == kGemmSwiGLU) tmem_ld_32cols(tu, uv);
     tmem_ld_wait();
     if (!row_ok) return;
+    if constexpr (MODE == kGemmF32) {
+        // FP32 accumulator as is: 16-byte stores where the row and N allow
+        float* o = orow;
+        const bool vec = ((reinterpret_cast<uintptr_t>(o) & 15u) == 0) && (N % 4 == 0);
 #pragma unroll
-    for (int v = 0; v < 4; ++v) {
-        if (col0 + v * 8 < N) {
-            uint32_t o[4];
+        for (int v = 0; v < 8; ++v) {
+            const int c = col0 + v * 4;
+            if (vec) {
+                if (c < N)
+                    *reinterpret_cast<float4*>(o + c) =
+                        make_float4(__uint_as_float(gv[4 * v]), __uint_as_float(gv[4 * v + 1]),
+                                    __uint_as_float(gv[4 * v + 2]), __uint_as_float(gv[4 * v + 3]));
+            } else {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                float a[2];
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const float x = __uint_as_float(gv[v * 8 + 2 * i + h]);
-                    if (MODE == kGemmSwiGLU) {
-                        const float u = __uint_as_float(uv[v * 8 + 2 * i + h]);
-                        a[h] = x / (1.0f + __expf(-x)) * u;
-                    } else if (MODE == kGemmReLU2) {
-                        a[h] = x > 0.f ? x * x : 0.f;
-                    } else {
-                        a[h] = x;
-                    }
-                }
-                o[i] = pack2(a[0], a[1]);
+                for (int i = 0; i < 4; ++i)
+                    if (c + i < N) o[c + i] = __uint_as_float(gv[4 * v + i]);
             }
-            *reinterpret_cast<uint4*>(orow + col0 + v * 8) = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+    } else {
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+            if (col0 + v * 8 < N) {
+                uint32_t o[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    float a[2];
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const float x = __uint_as_float(gv[v * 8 + 2 * i + h]);
+                        if (MODE == kGemmSwiGLU) {
+                            const float u = __uint_as_float(uv[v * 8 + 2 * i + h]);
+                            a[h] = x / (1.0f + __expf(-x)) * u;
+                        } else if (MODE == kGemmReLU2) {
+                            a[h] = x > 0.f ? x * x : 0.f;
+                        } else {
+                            a[h] = x;
+                        }
+                    }
+                    o[i] = pack2(a[0], a[1]);
+                }
+                *reinterpret_cast<uint4*>(orow + col0 + v * 8) = make_uint4(o[0], o[1], o[2], o[3]);
+            }
         }
     }
 }
@@ -191,8 +221,8 @@ __device__ __forceinline__ void epilogue_chunk(uint32_t tg, uint32_t tu, bool ro
 // TMEM lanes at `tbase`, one row per thread.  SwiGLU accumulators hold 128 gate
 // columns then the 128 matching up columns.
 template <int MODE>
-__device__ __forceinline__ void epilogue_rows(uint32_t tbase, bool row_ok, __nv_bfloat16* orow, int col_base,
-                                              int N) {
+__device__ __forceinline__ void epilogue_rows(uint32_t tbase, bool row_ok, typename OutOf<MODE>::T* orow,
+                                              int col_base, int N) {
     if (MODE == kGemmSwiGLU) {
 #pragma unroll 1
         for (int c = 0; c < 4; ++c)
@@ -301,7 +331,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             uint32_t ph = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-                const Tile t = decode_tile<MODE != kGemmPlain>(tile, prefix, rstart, rcount, p, ntn, C::BMT);
+                const Tile t = decode_tile<MODE == kGemmSwiGLU || MODE == kGemmReLU2>(tile, prefix, rstart, rcount, p, ntn, C::BMT);
                 const int a_row = t.row0 + t.mt * C::BMT;
                 const bool second = HALVES == 2 && (t.mt * C::BMT + BM < t.mrows);
                 const uint32_t bytes = (second ? 2 : 1) * A_BYTES + B_BYTES;
@@ -340,7 +370,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             uint32_t aph = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-                const Tile t = decode_tile<MODE != kGemmPlain>(tile, prefix, rstart, rcount, p, ntn, C::BMT);
+                const Tile t = decode_tile<MODE == kGemmSwiGLU || MODE == kGemmReLU2>(tile, prefix, rstart, rcount, p, ntn, C::BMT);
                 const int rows0 = t.mrows - t.mt * C::BMT;                  // rows from the first half on
                 const bool second = HALVES == 2 && rows0 > BM;
                 const uint32_t idesc0 = rows0 <= kTailRows ? IDESC64 : IDESC;
@@ -389,7 +419,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         int acc = 0;
         uint32_t aph = 0;
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-            const Tile t = decode_tile<MODE != kGemmPlain>(tile, prefix, rstart, rcount, p, ntn, C::BMT);
+            const Tile t = decode_tile<MODE == kGemmSwiGLU || MODE == kGemmReLU2>(tile, prefix, rstart, rcount, p, ntn, C::BMT);
             if (!mbar_wait_bounded(smem_u32(&ctl->tfull[acc]), aph, abort)) {
                 if (lane == 0) {
                     raise_status(p.hdr, MOE_ERR_TIMEOUT);
@@ -405,8 +435,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 const bool m64 = t.mrows - hrow0 <= kTailRows;
                 const int r = m64 ? hrow0 + q * 16 + lane : hrow0 + q * 32 + lane;
                 const bool row_ok = (!m64 || lane < 16) && r < t.mrows;
-                __nv_bfloat16* orow = p.out + (size_t)(t.row0 + (row_ok ? r : 0)) * p.ldo +
-                                      (size_t)t.g * p.out_group_col;
+                auto* orow = out_row<MODE>(p, t.row0 + (row_ok ? r : 0), t.g);
                 const uint32_t tbase =
                     tmem_base + (uint32_t)((acc + half) * BN_MMA) + ((uint32_t)(q * 32) << 16);
                 epilogue_rows<MODE>(tbase, row_ok, orow, t.nt * BN_OUT, p.N);
@@ -554,7 +583,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
             uint32_t ph = 0;
             bool ok = true;
             for (int tile = pair; tile < total && ok; tile += npairs) {
-                const Tile t = decode_tile<MODE != kGemmPlain>(tile, prefix, rstart, rcount, p, ntn, P_BMT);
+                const Tile t = decode_tile<MODE == kGemmSwiGLU || MODE == kGemmReLU2>(tile, prefix, rstart, rcount, p, ntn, P_BMT);
                 const bool tail = t.mrows - t.mt * P_BMT <= BM;
                 const int a_row = t.row0 + t.mt * P_BMT + (int)rank * (tail ? 64 : BM);
                 const int n0 = t.nt * BN_OUT;
@@ -595,7 +624,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
             uint32_t aph = 0;
             bool ok = true;
             for (int tile = pair; tile < total && ok; tile += npairs) {
-                const Tile t = decode_tile<MODE != kGemmPlain>(tile, prefix, rstart, rcount, p, ntn, P_BMT);
+                const Tile t = decode_tile<MODE == kGemmSwiGLU || MODE == kGemmReLU2>(tile, prefix, rstart, rcount, p, ntn, P_BMT);
                 const bool tail = t.mrows - t.mt * P_BMT <= BM;
                 const uint32_t idesc = tail ? P_IDESC_TAIL : P_IDESC_FULL;
                 if (!mbar_wait_bounded(smem_u32(&ctl->tempty[acc]), aph ^ 1u, abort)) { ok = false; break; }
@@ -634,7 +663,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
         int acc = 0;
         uint32_t aph = 0;
         for (int tile = pair; tile < total; tile += npairs) {
-            const Tile t = decode_tile<MODE != kGemmPlain>(tile, prefix, rstart, rcount, p, ntn, P_BMT);
+            const Tile t = decode_tile<MODE == kGemmSwiGLU || MODE == kGemmReLU2>(tile, prefix, rstart, rcount, p, ntn, P_BMT);
             const bool tail = t.mrows - t.mt * P_BMT <= BM;
             if (!mbar_wait_bounded(smem_u32(&ctl->tfull[acc]), aph, abort)) {
                 if (lane == 0) {
@@ -654,8 +683,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
             const bool live = t.mt * P_BMT + (tail ? (int)rank * 64 + (q & 1) * 32 : (int)rank * BM + q * 32) < t.mrows;
             if (live) {
                 const bool row_ok = r < t.mrows;
-                __nv_bfloat16* orow = p.out + (size_t)(t.row0 + (row_ok ? r : 0)) * p.ldo +
-                                      (size_t)t.g * p.out_group_col;
+                auto* orow = out_row<MODE>(p, t.row0 + (row_ok ? r : 0), t.g);
                 const uint32_t tl = tmem_base + (uint32_t)(acc * BN_MMA) + ((uint32_t)(q * 32) << 16);
                 const int n0 = t.nt * BN_OUT;
                 if (MODE == kGemmSwiGLU) {
@@ -815,7 +843,7 @@ moe_status launch_grouped_gemm(const GemmProblem& g, WsHeader* hdr, cudaStream_t
     kp.N = g.N;
     kp.b_group_rows = g.b_group_rows;
     kp.up_off = g.up_off;
-    kp.out = reinterpret_cast<__nv_bfloat16*>(g.out);
+    kp.out = g.out;
     kp.ldo = g.ldo;
     kp.out_group_col = g.out_group_col;
     kp.hdr = hdr;
@@ -829,6 +857,7 @@ moe_status launch_grouped_gemm(const GemmProblem& g, WsHeader* hdr, cudaStream_t
         switch (g.mode) {
             case kGemmSwiGLU: e = launch_pair<kGemmSwiGLU>(ma, mb, kp, smem, st); break;
             case kGemmReLU2: e = launch_pair<kGemmReLU2>(ma, mb, kp, smem, st); break;
+            case kGemmF32: e = launch_pair<kGemmF32>(ma, mb, kp, smem, st); break;
             default: e = launch_pair<kGemmPlain>(ma, mb, kp, smem, st); break;
         }
         return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
@@ -846,12 +875,14 @@ moe_status launch_grouped_gemm(const GemmProblem& g, WsHeader* hdr, cudaStream_t
         switch (g.mode) {
             case kGemmSwiGLU: e = launch_mode<kGemmSwiGLU, 2>(ma, mb, kp, smem, st); break;
             case kGemmReLU2: e = launch_mode<kGemmReLU2, 2>(ma, mb, kp, smem, st); break;
+            case kGemmF32: e = launch_mode<kGemmF32, 2>(ma, mb, kp, smem, st); break;
             default: e = launch_mode<kGemmPlain, 2>(ma, mb, kp, smem, st); break;
         }
     } else {
         switch (g.mode) {
             case kGemmSwiGLU: e = launch_mode<kGemmSwiGLU, 1>(ma, mb, kp, smem, st); break;
             case kGemmReLU2: e = launch_mode<kGemmReLU2, 1>(ma, mb, kp, smem, st); break;
+            case kGemmF32: e = launch_mode<kGemmF32, 1>(ma, mb, kp, smem, st); break;
             default: e = launch_mode<kGemmPlain, 1>(ma, mb, kp, smem, st); break;
         }
     }

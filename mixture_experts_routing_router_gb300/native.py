@@ -32,7 +32,8 @@ MOE_ACT_RELU2 = 1
 # every symbol include/moe.h declares
 EXPORTS = ("moe_workspace_size", "moe_workspace_init", "moe_route", "moe_dispatch", "moe_expert_up",
            "moe_expert_down", "moe_expert_ffn", "moe_combine", "moe_layer", "moe_status_read",
-           "moe_status_string", "moe_last_error_message", "moe_dispatch_noalloc")
+           "moe_status_string", "moe_last_error_message", "moe_dispatch_noalloc", "moe_gate",
+           "moe_route_sigmoid")
 
 
 class MoEError(RuntimeError):
@@ -86,6 +87,8 @@ def lib():
                 "moe_layer": [SP, P, P, P, P, P, P, P, P, P, P, S, P],
                 "moe_status_read": [P, P, ctypes.POINTER(ctypes.c_int)],
                 "moe_dispatch_noalloc": [SP, P, P, P, P, P, P, P, P, P],
+                "moe_gate": [SP, P, P, P, P, S, P],
+                "moe_route_sigmoid": [SP, P, P, ctypes.c_float, P, P, P, S, P],
             }
             for name, args in sig.items():
                 fn = getattr(L, name)
@@ -162,6 +165,17 @@ def _wsb(ws):
 def moe_route(shape, logits, topk_ids, topk_w, ws, stream=None):
     _check(lib().moe_route(ctypes.byref(shape), _ptr(logits), _ptr(topk_ids), _ptr(topk_w), _ptr(ws), _wsb(ws),
                            _stream(stream)), "moe_route")
+
+
+def moe_gate(shape, x, w_gate, logits, ws, stream=None):
+    _check(lib().moe_gate(ctypes.byref(shape), _ptr(x), _ptr(w_gate), _ptr(logits), _ptr(ws), _wsb(ws),
+                          _stream(stream)), "moe_gate")
+
+
+def moe_route_sigmoid(shape, logits, bias, route_scale, topk_ids, topk_w, ws, stream=None):
+    _check(lib().moe_route_sigmoid(ctypes.byref(shape), _ptr(logits), _ptr(bias), float(route_scale),
+                                   _ptr(topk_ids), _ptr(topk_w), _ptr(ws), _wsb(ws), _stream(stream)),
+           "moe_route_sigmoid")
 
 
 def moe_dispatch(shape, x, topk_ids, counts, offsets, dest, sorted_pair, x_perm, ws, stream=None):

@@ -182,6 +182,17 @@ def shared_expert_weights(wl: Workload, s: int, seed: int = 0, device="cpu", uni
             normal((H, Is), s2, seed, f"ws2/{s}", device))
 
 
+def gate_weights(wl: Workload, seed: int = 0, device="cpu") -> torch.Tensor:
+    """Router projection W_gate [E, H] ~ N(0, 1/H): x ~ N(0,1) gives logits of
+    about unit scale."""
+    return normal((wl.experts, wl.hidden), 1.0 / math.sqrt(wl.hidden), seed, "w_gate", device)
+
+
+def correction_bias(wl: Workload, seed: int = 0, device="cpu", std: float = 0.05) -> torch.Tensor:
+    """FP32 selection-only routing bias [E] ~ N(0, std^2)."""
+    return normal((wl.experts,), std, seed, "bias", device, torch.float32)
+
+
 def bf16_bits(t: torch.Tensor):
     """A bf16 tensor's bit patterns as a numpy uint16 array (host copy)."""
     return t.detach().contiguous().view(torch.int16).cpu().numpy().view("uint16")
