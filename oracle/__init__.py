@@ -87,11 +87,11 @@ def _load():
             lib.oracle_expert_ffn.restype = None
             lib.oracle_expert_ffn.argtypes = [i, i, i, i, i, i, i] + [P] * 11
             lib.oracle_combine_row.restype = None
-            lib.oracle_combine_row.argtypes = [i, i, P, P, P, P, P]
+            lib.oracle_combine_row.argtypes = [i, i, P, P, P, P, P, P]
             lib.oracle_combine.restype = None
-            lib.oracle_combine.argtypes = [i, i, i, P, P, P, P, P]
+            lib.oracle_combine.argtypes = [i, i, i, P, P, P, P, P, P]
             lib.oracle_layer.restype = i
-            lib.oracle_layer.argtypes = [i] * 9 + [P] * 19
+            lib.oracle_layer.argtypes = [i] * 9 + [P] * 20
             _lib = lib
     return _lib
 
@@ -219,7 +219,7 @@ def shared_row(x_row, ws13, ws2, act):
     return h, y
 
 
-def combine(y_perm, dest, w, y_shared=None):
+def combine(y_perm, dest, w, y_shared=None, residual=None):
     y_perm = _c(y_perm, np.uint16)
     dest = _c(dest, np.int32).reshape(-1)
     w = _c(w, np.float32)
@@ -227,23 +227,25 @@ def combine(y_perm, dest, w, y_shared=None):
     H = y_perm.shape[1]
     out = np.zeros((T, H), np.uint16)
     ys = None if y_shared is None else _c(y_shared, np.uint16)
-    _load().oracle_combine(T, k, H, _p(y_perm), _p(dest), _p(w), _p(ys), _p(out))
+    res = None if residual is None else _c(residual, np.uint16)
+    _load().oracle_combine(T, k, H, _p(y_perm), _p(dest), _p(w), _p(ys), _p(res), _p(out))
     return out
 
 
-def combine_row(y_perm, dest_t, w_t, y_shared_t=None):
+def combine_row(y_perm, dest_t, w_t, y_shared_t=None, residual_t=None):
     y_perm = _c(y_perm, np.uint16)
     dest_t = _c(dest_t, np.int32)
     w_t = _c(w_t, np.float32)
     H = y_perm.shape[1]
     out = np.zeros(H, np.uint16)
     ys = None if y_shared_t is None else _c(y_shared_t, np.uint16)
-    _load().oracle_combine_row(len(w_t), H, _p(y_perm), _p(dest_t), _p(w_t), _p(ys), _p(out))
+    res = None if residual_t is None else _c(residual_t, np.uint16)
+    _load().oracle_combine_row(len(w_t), H, _p(y_perm), _p(dest_t), _p(w_t), _p(ys), _p(res), _p(out))
     return out
 
 
 def layer(x, w13, w2, act, k, capacity, logits=None, ids_in=None, w_in=None,
-          ws13=None, ws2=None):
+          ws13=None, ws2=None, residual=None):
     """The whole layer; returns a dict with every intermediate and 'status'."""
     x = _c(x, np.uint16)
     w13 = _c(w13, np.uint16)
@@ -266,8 +268,9 @@ def layer(x, w13, w2, act, k, capacity, logits=None, ids_in=None, w_in=None,
     lg = None if logits is None else _c(logits, np.float32)
     ii = None if ids_in is None else _c(ids_in, np.int32)
     wi = None if w_in is None else _c(w_in, np.float32)
+    res = None if residual is None else _c(residual, np.uint16)
     st = _load().oracle_layer(T, H, E, k, I, act, S, Is, capacity, _p(lg), _p(ii), _p(wi), _p(x),
-                              _p(w13), _p(w2), _p(ws13), _p(ws2), _p(o["ids"]), _p(o["w"]),
+                              _p(w13), _p(w2), _p(ws13), _p(ws2), _p(res), _p(o["ids"]), _p(o["w"]),
                               _p(o["counts"]), _p(o["offsets"]), _p(o["dest"]), _p(o["sorted_pair"]),
                               _p(o["x_perm"]), _p(o["h"]), _p(o["y_perm"]), _p(o["h_shared"]),
                               _p(o["y_shared"]), _p(o["out"]))

@@ -317,13 +317,14 @@ void oracle_expert_ffn(int T, int H, int E, int I, int act, int S, int Is,
 }
 
 // ---- combine ------------------------------------------------------------
-// [MI300] MOE_COMBINE_RESIDUAL (the weighted combine; the residual add is not
-// part of this layer) and [ORT] "FP32 final routing/reduction": for token t,
-// out[t] = bf16( sum_{j<k} w[t,j] * y_perm[dest[t,j]] + y_shared[t] ), summed
-// in j order, then the shared term.  Pairs with dest < 0 (invalid routes)
-// contribute nothing.
+// [MI300] MOE_COMBINE_RESIDUAL (the weighted combine with the block's residual
+// add) and [ORT] "FP32 final routing/reduction": for token t,
+// out[t] = bf16( sum_{j<k} w[t,j] * y_perm[dest[t,j]] + y_shared[t] + residual[t] ),
+// summed in j order, then the shared term, then the residual (both optional).
+// Pairs with dest < 0 (invalid routes) contribute nothing.
 void oracle_combine_row(int k, int H, const uint16_t* y_perm, const int32_t* dest_t,
-                        const float* w_t, const uint16_t* y_shared_t, uint16_t* out_t) {
+                        const float* w_t, const uint16_t* y_shared_t, const uint16_t* residual_t,
+                        uint16_t* out_t) {
     for (int c = 0; c < H; ++c) {
         double s = 0.0;
         for (int j = 0; j < k; ++j) {
@@ -331,15 +332,17 @@ void oracle_combine_row(int k, int H, const uint16_t* y_perm, const int32_t* des
             s += (double)w_t[j] * bf16_to_double(y_perm[(size_t)dest_t[j] * H + c]);
         }
         if (y_shared_t) s += bf16_to_double(y_shared_t[c]);
+        if (residual_t) s += bf16_to_double(residual_t[c]);
         out_t[c] = double_to_bf16(s);
     }
 }
 
 void oracle_combine(int T, int k, int H, const uint16_t* y_perm, const int32_t* dest,
-                    const float* w, const uint16_t* y_shared, uint16_t* out) {
+                    const float* w, const uint16_t* y_shared, const uint16_t* residual, uint16_t* out) {
     for (int t = 0; t < T; ++t)
         oracle_combine_row(k, H, y_perm, dest + (size_t)t * k, w + (size_t)t * k,
                            y_shared ? y_shared + (size_t)t * H : nullptr,
+                           residual ? residual + (size_t)t * H : nullptr,
                            out + (size_t)t * H);
 }
 
@@ -350,7 +353,7 @@ void oracle_combine(int T, int k, int H, const uint16_t* y_perm, const int32_t* 
 int oracle_layer(int T, int H, int E, int k, int I, int act, int S, int Is, int capacity,
                  const float* logits, const int32_t* ids_in, const float* w_in,
                  const uint16_t* x, const uint16_t* w13, const uint16_t* w2,
-                 const uint16_t* ws13, const uint16_t* ws2,
+                 const uint16_t* ws13, const uint16_t* ws2, const uint16_t* residual,
                  int32_t* ids, float* w, int32_t* counts, int32_t* offsets,
                  int32_t* dest, int32_t* sorted_pair, uint16_t* x_perm,
                  uint16_t* h, uint16_t* y_perm, uint16_t* h_shared, uint16_t* y_shared,
@@ -368,7 +371,7 @@ int oracle_layer(int T, int H, int E, int k, int I, int act, int S, int Is, int 
     if (st == ST_CAPACITY) return st;
     oracle_expert_ffn(T, H, E, I, act, S, Is, x_perm, offsets, w13, w2, x, ws13, ws2,
                       h, y_perm, h_shared, y_shared);
-    oracle_combine(T, k, H, y_perm, dest, w, S > 0 ? y_shared : nullptr, out);
+    oracle_combine(T, k, H, y_perm, dest, w, S > 0 ? y_shared : nullptr, residual, out);
     return st;
 }
 

@@ -34,6 +34,7 @@ MUTANTS = {
     "sigmoid_weights_from_biased_key": ("(double)route_scale * (double)score[order[j]] / z",
                                         "(double)route_scale * (double)key[order[j]] / z"),
     "gate_transposed": ("bf16_to_double(wg[(size_t)e * H + h])", "bf16_to_double(wg[(size_t)h * E + e])"),
+    "residual_dropped": ("if (residual_t) s += bf16_to_double(residual_t[c]);", "if (residual_t) s += 0.0;"),
     "first_slot_dropped_in_combine": ("for (int j = 0; j < k; ++j) {\n            if (dest_t[j] < 0) continue;",
                                       "for (int j = 1; j < k; ++j) {\n            if (dest_t[j] < 0) continue;"),
 }
@@ -57,6 +58,7 @@ PINS = [
     (P.test_shared_experts_sum_before_rounding, {}),
     (P.test_combine_identity_experts_return_x, dict(k=4)),
     (P.test_combine_weights_are_applied_per_slot, {}),
+    (P.test_combine_residual_is_added_once, {}),
     (P.test_layer_internal_routing_equals_preselected, {}),
     (P.test_route_sigmoid_without_bias_selects_like_softmax, {}),
     (P.test_route_sigmoid_dominant_bias_selects_its_set_and_weights_ignore_it, {}),

@@ -366,6 +366,23 @@ def test_combine_identity_experts_return_x(oracle_mod, k):
     assert np.array_equal(bits_to_f64(out2), 2 * bits_to_f64(x))
 
 
+def test_combine_residual_is_added_once(oracle_mod):
+    # identity experts with power-of-two weights give x; a residual r adds r
+    # exactly when x + r is exact in BF16 (here r = x, so the result is 2x),
+    # and it is added after the shared term (x + x + x = 3x for small integers)
+    rng = np.random.default_rng(31)
+    T, E, H, k = 12, 6, 16, 2
+    x = bf16_of_exact(rng.integers(-8, 9, size=(T, H)))
+    ids = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    _, _, _, dest, _, xp = oracle_mod.dispatch(ids, x, E, T)
+    w = np.full((T, k), 0.5, np.float32)
+    assert np.array_equal(bits_to_f64(oracle_mod.combine(xp, dest, w, residual=x)), 2 * bits_to_f64(x))
+    assert np.array_equal(bits_to_f64(oracle_mod.combine(xp, dest, w, y_shared=x, residual=x)),
+                          3 * bits_to_f64(x))
+    out = oracle_mod.combine_row(xp, dest.reshape(T, k)[0], w[0], None, x[0])
+    assert np.array_equal(bits_to_f64(out), 2 * bits_to_f64(x[0]))
+
+
 def test_combine_weights_are_applied_per_slot(oracle_mod):
     # y rows 1.0 and 2.0 with weights 0.75 / 0.25 -> 1.25 exactly; swapped -> 1.75
     y = bf16_of_exact([[1.0] * 4, [2.0] * 4])
