@@ -182,26 +182,31 @@ MOE_API moe_status moe_expert_ffn(const moe_shape* shape, const uint16_t* x_perm
                           void* ws, size_t ws_bytes, void* stream);
 
 /* Weighted combine back to token order (DeepSeek fleet REPORT.md,
- * MOE_COMBINE_RESIDUAL without the residual; ONNX Runtime PR #33963, "FP32
- * final routing/reduction"):
- *   out[t] = bf16( sum_{j<k} topk_w[t,j] * y_perm[dest[t*k+j]]  +  y_shared[t] )
- * summed in FP32 in j order, then the shared term; pairs with dest < 0 are skipped.
+ * MOE_COMBINE_RESIDUAL: the combine with the block's residual add fused;
+ * ONNX Runtime PR #33963, "FP32 final routing/reduction"):
+ *   out[t] = bf16( sum_{j<k} topk_w[t,j] * y_perm[dest[t*k+j]] + y_shared[t] + residual[t] )
+ * summed in FP32 in j order, then the shared term, then the residual; pairs
+ * with dest < 0 are skipped.
  *   y_perm device bf16 [T*k, H]; dest device i32 [T*k]; topk_w device f32 [T, k];
- *   y_shared device bf16 [T, H] or NULL; out device bf16 [T, H]. */
+ *   y_shared device bf16 [T, H] or NULL; residual device bf16 [T, H] or NULL
+ *   (out may alias residual: each element is read before it is written);
+ *   out device bf16 [T, H]. */
 MOE_API moe_status moe_combine(const moe_shape* shape, const uint16_t* y_perm, const int32_t* dest,
-                       const float* topk_w, const uint16_t* y_shared, uint16_t* out,
-                       void* ws, size_t ws_bytes, void* stream);
+                               const float* topk_w, const uint16_t* y_shared, const uint16_t* residual,
+                               uint16_t* out, void* ws, size_t ws_bytes, void* stream);
 
 /* The whole layer: route (when logits != NULL) or take preselected ids_in /
  * w_in (device i32 [T,k] / f32 [T,k], used when logits == NULL), then dispatch,
- * expert FFN and combine, with every intermediate in the workspace.  Given the
- * ids and weights moe_route returns, the output is bitwise the same either way
- * (ONNX Runtime PR #33963: internal and preselected routing give bitwise-equal
- * outputs).  out: device bf16 [T, H]. */
+ * expert FFN and combine (adding residual [T, H] when it is not NULL), with
+ * every intermediate in the workspace.  Given the ids and weights moe_route
+ * returns, the output is bitwise the same either way (ONNX Runtime PR #33963:
+ * internal and preselected routing give bitwise-equal outputs).
+ * out: device bf16 [T, H] (may alias residual). */
 MOE_API moe_status moe_layer(const moe_shape* shape, const float* logits, const int32_t* ids_in,
-                     const float* w_in, const uint16_t* x, const uint16_t* w13,
-                     const uint16_t* w2, const uint16_t* ws13, const uint16_t* ws2,
-                     uint16_t* out, void* ws, size_t ws_bytes, void* stream);
+                             const float* w_in, const uint16_t* x, const uint16_t* w13,
+                             const uint16_t* w2, const uint16_t* ws13, const uint16_t* ws2,
+                             const uint16_t* residual, uint16_t* out, void* ws, size_t ws_bytes,
+                             void* stream);
 
 /* moe_dispatch for callers that cannot allocate device memory, and so cannot
  * provide the workspace the other calls take: code that runs where cudaMalloc

@@ -154,8 +154,8 @@ moe_status do_down(const moe_shape& s, const uint16_t* h, const int32_t* offsets
 }
 
 moe_status do_combine(const moe_shape& s, const uint16_t* y_perm, const int32_t* dest, const float* w,
-                      const uint16_t* y_shared, uint16_t* out, cudaStream_t st) {
-    return from_cuda(launch_combine(s, y_perm, dest, w, y_shared, out, st));
+                      const uint16_t* y_shared, const uint16_t* residual, uint16_t* out, cudaStream_t st) {
+    return from_cuda(launch_combine(s, y_perm, dest, w, y_shared, residual, out, st));
 }
 
 }  // namespace
@@ -275,26 +275,30 @@ moe_status moe_expert_ffn(const moe_shape* shape, const uint16_t* x_perm, const 
 }
 
 moe_status moe_combine(const moe_shape* shape, const uint16_t* y_perm, const int32_t* dest, const float* topk_w,
-                       const uint16_t* y_shared, uint16_t* out, void* ws, size_t ws_bytes, void* stream) {
+                       const uint16_t* y_shared, const uint16_t* residual, uint16_t* out, void* ws,
+                       size_t ws_bytes, void* stream) {
     clear_error();
     moe_status r = check_shape(shape);
     if (r != MOE_OK) return r;
     if ((r = check_ws(shape, ws, ws_bytes, false)) != MOE_OK) return r;
     if (!aligned(y_perm, 16) || !aligned(dest, 16) || !aligned(topk_w, 16) || !aligned(out, 16) ||
-        !aligned_or_null(y_shared, 16))
+        !aligned_or_null(y_shared, 16) || !aligned_or_null(residual, 16))
         return MOE_ERR_INVALID_ARG;
-    return do_combine(*shape, y_perm, dest, topk_w, y_shared, out, static_cast<cudaStream_t>(stream));
+    return do_combine(*shape, y_perm, dest, topk_w, y_shared, residual, out, static_cast<cudaStream_t>(stream));
 }
 
 moe_status moe_layer(const moe_shape* shape, const float* logits, const int32_t* ids_in, const float* w_in,
                      const uint16_t* x, const uint16_t* w13, const uint16_t* w2, const uint16_t* ws13,
-                     const uint16_t* ws2, uint16_t* out, void* ws, size_t ws_bytes, void* stream) {
+                     const uint16_t* ws2, const uint16_t* residual, uint16_t* out, void* ws, size_t ws_bytes,
+                     void* stream) {
     clear_error();
     moe_status r = check_shape(shape);
     if (r != MOE_OK) return r;
     if ((r = check_ws(shape, ws, ws_bytes, true)) != MOE_OK) return r;
     if (logits ? !aligned(logits, 16) : (!aligned(ids_in, 16) || !aligned(w_in, 16))) return MOE_ERR_INVALID_ARG;
-    if (!aligned(x, 16) || !aligned(w13, 16) || !aligned(w2, 16) || !aligned(out, 16)) return MOE_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(w13, 16) || !aligned(w2, 16) || !aligned(out, 16) ||
+        !aligned_or_null(residual, 16))
+        return MOE_ERR_INVALID_ARG;
     if (shape->shared > 0 && (!aligned(ws13, 16) || !aligned(ws2, 16))) return MOE_ERR_INVALID_ARG;
     const moe_shape& s = *shape;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -319,7 +323,7 @@ moe_status moe_layer(const moe_shape* shape, const float* logits, const int32_t*
         return r;
     if ((r = do_up(s, x_perm, offsets, w13, x, ws13, h, ws, st)) != MOE_OK) return r;
     if ((r = do_down(s, h, offsets, w2, ws2, y_perm, y_shared, ws, st)) != MOE_OK) return r;
-    return do_combine(s, y_perm, dest, w, y_shared, out, st);
+    return do_combine(s, y_perm, dest, w, y_shared, residual, out, st);
 }
 
 moe_status moe_status_read(void* ws, void* stream, moe_status* device_status) {

@@ -1,9 +1,11 @@
 // combine.cu -- K6, the weighted unpermute-combine back to token order.
 //
-// DeepSeek fleet REPORT.md (MOE_COMBINE_RESIDUAL row; the residual add is not
-// part of this layer) and ONNX Runtime PR #33963 ("FP32 final routing/reduction"):
-//   out[t] = bf16( sum_{j<k} w[t,j] * y_perm[dest[t*k+j]] + y_shared[t] )
-// accumulated in FP32, j = 0..k-1 in order, then the shared-expert term.
+// DeepSeek fleet REPORT.md (MOE_COMBINE_RESIDUAL row: the combine with the
+// block's residual add fused) and ONNX Runtime PR #33963 ("FP32 final
+// routing/reduction"):
+//   out[t] = bf16( sum_{j<k} w[t,j] * y_perm[dest[t*k+j]] + y_shared[t] + residual[t] )
+// accumulated in FP32, j = 0..k-1 in order, then the shared-expert term, then
+// the residual (both optional).
 // One block per token row; 16-byte vectors (8 BF16) per thread; the k source
 // rows of a chunk are loaded together before they are summed in order.
 #include "common.cuh"
@@ -27,7 +29,8 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 __global__ void __launch_bounds__(256)
 combine_kernel(int T, int HV, int k, const uint4* __restrict__ y_perm, const int32_t* __restrict__ dest,
-               const float* __restrict__ w, const uint4* __restrict__ y_shared, uint4* __restrict__ out) {
+               const float* __restrict__ w, const uint4* __restrict__ y_shared, const uint4* residual,
+               uint4* out) {   // out may alias residual: each 16-byte group is read, then written, by one thread
     __shared__ int dsh[32];
     __shared__ float wsh[32];
     const long long R = (long long)T * k;
@@ -56,6 +59,7 @@ combine_kernel(int T, int HV, int k, const uint4* __restrict__ y_perm, const int
                 }
             }
             if (y_shared) acc_bf16x8(a, __ldcs(y_shared + (size_t)t * HV + c), 1.0f);
+            if (residual) acc_bf16x8(a, residual[(size_t)t * HV + c], 1.0f);
             uint4 o;
             o.x = pack_bf16x2(a[0], a[1]);
             o.y = pack_bf16x2(a[2], a[3]);
@@ -70,7 +74,7 @@ combine_kernel(int T, int HV, int k, const uint4* __restrict__ y_perm, const int
 }  // namespace
 
 cudaError_t launch_combine(const moe_shape& s, const uint16_t* y_perm, const int32_t* dest, const float* w,
-                           const uint16_t* y_shared, uint16_t* out, cudaStream_t st) {
+                           const uint16_t* y_shared, const uint16_t* residual, uint16_t* out, cudaStream_t st) {
     const int HV = s.hidden / 8;
     int threads = 32;
     while (threads < 256 && threads < HV) threads *= 2;
@@ -79,6 +83,7 @@ cudaError_t launch_combine(const moe_shape& s, const uint16_t* y_perm, const int
     if (blocks > cap) blocks = cap;
     combine_kernel<<<(unsigned)blocks, threads, 0, st>>>(s.tokens, HV, s.top_k, reinterpret_cast<const uint4*>(y_perm),
                                                          dest, w, reinterpret_cast<const uint4*>(y_shared),
+                                                         reinterpret_cast<const uint4*>(residual),
                                                          reinterpret_cast<uint4*>(out));
     return cudaGetLastError();
 }

@@ -291,7 +291,8 @@ cudaError_t launch_scatter(const moe_shape& s, const uint16_t* x, const int32_t*
                            const int32_t* offsets, const int32_t* rank, int32_t* dest,
                            int32_t* sorted_pair, uint16_t* x_perm, WsHeader* hdr, cudaStream_t st);
 cudaError_t launch_combine(const moe_shape& s, const uint16_t* y_perm, const int32_t* dest,
-                           const float* w, const uint16_t* y_shared, uint16_t* out, cudaStream_t st);
+                           const float* w, const uint16_t* y_shared, const uint16_t* residual, uint16_t* out,
+                           cudaStream_t st);
 
 // Grouped GEMM problem (one launch): for every group g and row r of the group,
 // out[row0(g) + r, g*out_group_col + n] = epilogue( sum_seg sum_k A[row0(g)+r, seg*a_seg_col + k]

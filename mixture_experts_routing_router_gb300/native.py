@@ -83,8 +83,8 @@ def lib():
                 "moe_expert_up": [SP, P, P, P, P, P, P, P, S, P],
                 "moe_expert_down": [SP, P, P, P, P, P, P, P, S, P],
                 "moe_expert_ffn": [SP, P, P, P, P, P, P, P, P, P, P, P, S, P],
-                "moe_combine": [SP, P, P, P, P, P, P, S, P],
-                "moe_layer": [SP, P, P, P, P, P, P, P, P, P, P, S, P],
+                "moe_combine": [SP, P, P, P, P, P, P, P, S, P],
+                "moe_layer": [SP, P, P, P, P, P, P, P, P, P, P, P, S, P],
                 "moe_status_read": [P, P, ctypes.POINTER(ctypes.c_int)],
                 "moe_dispatch_noalloc": [SP, P, P, P, P, P, P, P, P, P],
                 "moe_gate": [SP, P, P, P, P, S, P],
@@ -199,15 +199,15 @@ def moe_expert_ffn(shape, x_perm, offsets, w13, w2, x, ws13, ws2, h, y_perm, y_s
                                 _stream(stream)), "moe_expert_ffn")
 
 
-def moe_combine(shape, y_perm, dest, topk_w, y_shared, out, ws, stream=None):
-    _check(lib().moe_combine(ctypes.byref(shape), _ptr(y_perm), _ptr(dest), _ptr(topk_w), _ptr(y_shared), _ptr(out),
-                             _ptr(ws), _wsb(ws), _stream(stream)), "moe_combine")
+def moe_combine(shape, y_perm, dest, topk_w, y_shared, out, ws, stream=None, residual=None):
+    _check(lib().moe_combine(ctypes.byref(shape), _ptr(y_perm), _ptr(dest), _ptr(topk_w), _ptr(y_shared),
+                             _ptr(residual), _ptr(out), _ptr(ws), _wsb(ws), _stream(stream)), "moe_combine")
 
 
-def moe_layer(shape, logits, ids_in, w_in, x, w13, w2, ws13, ws2, out, ws, stream=None):
+def moe_layer(shape, logits, ids_in, w_in, x, w13, w2, ws13, ws2, out, ws, stream=None, residual=None):
     _check(lib().moe_layer(ctypes.byref(shape), _ptr(logits), _ptr(ids_in), _ptr(w_in), _ptr(x), _ptr(w13),
-                           _ptr(w2), _ptr(ws13), _ptr(ws2), _ptr(out), _ptr(ws), _wsb(ws), _stream(stream)),
-           "moe_layer")
+                           _ptr(w2), _ptr(ws13), _ptr(ws2), _ptr(residual), _ptr(out), _ptr(ws), _wsb(ws),
+                           _stream(stream)), "moe_layer")
 
 
 def moe_dispatch_noalloc(shape, x, topk_ids, counts, offsets, dest, sorted_pair, x_perm, device_status=None,

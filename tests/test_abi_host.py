@@ -81,15 +81,19 @@ def test_null_and_misaligned_pointers_are_rejected_before_launch(L):
                        fake_ws, n, None) == N.MOE_ERR_INVALID_ARG
     # workspace too small
     assert L.moe_layer(ctypes.byref(s), ctypes.c_void_p(4096), None, None, ctypes.c_void_p(4096),
-                       ctypes.c_void_p(4096), ctypes.c_void_p(4096), None, None, ctypes.c_void_p(4096),
+                       ctypes.c_void_p(4096), ctypes.c_void_p(4096), None, None, None, ctypes.c_void_p(4096),
                        fake_ws, n - 1, None) == N.MOE_ERR_INVALID_ARG
+    # misaligned residual
+    assert L.moe_combine(ctypes.byref(s), ctypes.c_void_p(4096), ctypes.c_void_p(4096), ctypes.c_void_p(4096),
+                         None, ctypes.c_void_p(4100), ctypes.c_void_p(4096), fake_ws, n, None) \
+        == N.MOE_ERR_INVALID_ARG
     # misaligned workspace
     assert L.moe_combine(ctypes.byref(s), ctypes.c_void_p(4096), ctypes.c_void_p(4096), ctypes.c_void_p(4096),
-                         None, ctypes.c_void_p(4096), ctypes.c_void_p((1 << 20) + 16), n, None) \
+                         None, None, ctypes.c_void_p(4096), ctypes.c_void_p((1 << 20) + 16), n, None) \
         == N.MOE_ERR_INVALID_ARG
     # preselected path without weights
     assert L.moe_layer(ctypes.byref(s), None, ctypes.c_void_p(4096), None, ctypes.c_void_p(4096),
-                       ctypes.c_void_p(4096), ctypes.c_void_p(4096), None, None, ctypes.c_void_p(4096),
+                       ctypes.c_void_p(4096), ctypes.c_void_p(4096), None, None, None, ctypes.c_void_p(4096),
                        fake_ws, n, None) == N.MOE_ERR_INVALID_ARG
     # shared experts without their weights
     s2 = shape(shared=2, shared_inter=64)

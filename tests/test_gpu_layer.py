@@ -141,3 +141,19 @@ def test_layer_error_statuses():
     shape.capacity = wl.tokens
     N.moe_layer(shape, g["logits"], None, None, g["x"], g["w13"], g["w2"], None, None, out, ws)
     assert N.moe_status_read(ws) == N.MOE_OK
+
+
+def test_layer_with_residual():
+    wl = SMALL["deepseek_t96"]
+    g = inputs(wl, unit_scale=True, seed=31)
+    res = synth.normal((wl.tokens, wl.hidden), 1.0, 31, "residual", dev())
+    ref = oracle.layer(bits(g["x"]), bits(g["w13"]), bits(g["w2"]), wl.act, wl.top_k, wl.cap,
+                       logits=g["logits"].cpu().numpy(), ws13=bits(g["ws13"]), ws2=bits(g["ws2"]),
+                       residual=bits(res))
+    shape = N.shape_of(wl)
+    ws = N.workspace(shape, dev())
+    out = torch.empty(wl.tokens, wl.hidden, dtype=torch.bfloat16, device=dev())
+    N.moe_layer(shape, g["logits"], None, None, g["x"], g["w13"], g["w2"], g["ws13"], g["ws2"], out, ws,
+                residual=res)
+    assert N.moe_status_read(ws) == N.MOE_OK
+    assert_close(bits(out), ref["out"], "layer + residual")

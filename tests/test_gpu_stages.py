@@ -302,3 +302,23 @@ def test_combine_skips_invalid_pairs():
     out = torch.empty(64, 128, dtype=torch.bfloat16, device=dev())
     N.moe_combine(shape, y_dev, i32_dev(dest), f32_dev(w), None, out, ws)
     assert_close(bits(out), want, "combine invalid")
+
+
+@pytest.mark.parametrize("in_place", [False, True])
+def test_combine_with_residual(in_place):
+    """The MOE_COMBINE_RESIDUAL form: out = sum_j w y + y_shared + residual,
+    also with out written over the residual buffer."""
+    wl = W["deepseek"].with_(tokens=200)
+    lg = synth.make_logits(wl, seed=12).numpy()
+    _, ids, w = oracle.route(lg, wl.top_k)
+    st, counts, offsets, dest, sp, _ = oracle.dispatch(ids, np.zeros((wl.tokens, 8), np.uint16), wl.experts, wl.cap)
+    y_dev = synth.normal((wl.pairs, wl.hidden), 1.0, 12, "y_perm", dev())
+    ys_dev = synth.normal((wl.tokens, wl.hidden), 1.0, 12, "y_shared", dev())
+    res_dev = synth.normal((wl.tokens, wl.hidden), 1.0, 12, "residual", dev())
+    want = oracle.combine(bits(y_dev), dest, w, bits(ys_dev), bits(res_dev))
+    shape = N.shape_of(wl)
+    ws = N.workspace(shape, dev())
+    out = res_dev if in_place else torch.empty(wl.tokens, wl.hidden, dtype=torch.bfloat16, device=dev())
+    N.moe_combine(shape, y_dev, i32_dev(dest), f32_dev(w), ys_dev, out, ws, residual=res_dev)
+    assert N.moe_status_read(ws) == N.MOE_OK
+    assert_close(bits(out), want, "combine + residual")
