@@ -31,6 +31,7 @@ SMALL = {
     "one_expert": synth.Workload("one_expert", 300, 64, 1, 1, 128),
     "k_eq_e": synth.Workload("k_eq_e", 40, 128, 8, 8, 64),
     "wide_e": synth.Workload("wide_e", 70, 64, 1000, 32, 32),
+    "max_e": synth.Workload("max_e", 300, 64, 1024, 32, 32),                 # the ABI's largest E and k
     "t1": synth.Workload("t1", 1, 256, 16, 4, 128),
     "shared3": synth.Workload("shared3", 50, 128, 12, 2, 64, shared=3, shared_inter=72),
     # reductions of 4096 and more take the 256-row two-accumulator tile: full
@@ -62,7 +63,8 @@ def oracle_stages(wl, g):
 # ---------------------------------------------------------------------------
 # route
 # ---------------------------------------------------------------------------
-ROUTE_CASES = {**{k: v for k, v in W.items()}, **{k: SMALL[k] for k in ("ragged", "wide_e", "t1", "k_eq_e")}}
+ROUTE_CASES = {**{k: v for k, v in W.items()},
+               **{k: SMALL[k] for k in ("ragged", "wide_e", "max_e", "t1", "k_eq_e")}}
 
 
 @pytest.mark.parametrize("name", sorted(ROUTE_CASES))
@@ -132,7 +134,8 @@ def gpu_dispatch(wl, x_dev, ids_np, cap=None):
     return o, N.moe_status_read(ws)
 
 
-DISPATCH_CASES = ["tiny", "count_first", "deepseek", "large", "ragged", "one_expert", "k_eq_e", "wide_e", "t1"] + DECODE
+DISPATCH_CASES = ["tiny", "count_first", "deepseek", "large", "ragged", "one_expert", "k_eq_e", "wide_e", "max_e",
+                  "t1"] + DECODE
 
 
 @pytest.mark.parametrize("name", DISPATCH_CASES)
