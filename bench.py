@@ -71,6 +71,18 @@ def load_peaks():
     return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
 
 
+def up_kernel_name(wl, sms):
+    """Which kernel the library runs for the up projection (the library's own
+    host rule: the small-row kernel when a group holds at most 64 rows and its
+    items fit in two waves, the CTA-pair kernel when groups average 256 rows)."""
+    R = wl.tokens * wl.top_k
+    if wl.tokens <= 64 and min(wl.experts, R) * ((wl.inter + 127) // 128) <= 2 * sms:
+        return "decode_gemm_kernel (expert up projection)"
+    if R // wl.experts >= 256:
+        return "grouped_gemm_pair_kernel (expert up projection)"
+    return "grouped_gemm_kernel (expert up projection)"
+
+
 def kernel_source_sha():
     h = hashlib.sha256()
     for f in ("common.cuh", "gemm.cu"):
@@ -521,7 +533,8 @@ def run_native(args, wl, world, rank, local):
                               f"events)" if flush else
                               f"inputs larger than L2 (x {g['x'].numel() * 2 >> 20} MiB, touched weights "
                               f"{touched >> 20} MiB): no flush")},
-            "roofline": {"kernel": "grouped_gemm_kernel (expert up projection)", **roof,
+            "roofline": {"kernel": up_kernel_name(wl, torch.cuda.get_device_properties(dev).multi_processor_count),
+                         **roof,
                          "traffic": ncu_traffic() if wl.name == WORKLOAD else None},
             "expert_up_tflops": achieved,
             "dispatch_combine_gbs": dc_gbs, "dispatch_combine_hbm_frac": dc_gbs / peaks["hbm_gbs"],

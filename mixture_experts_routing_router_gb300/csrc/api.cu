@@ -110,6 +110,7 @@ moe_status do_up(const moe_shape& s, const uint16_t* x_perm, const int32_t* offs
     g.K = s.hidden; g.nseg = 1; g.a_seg_col = 0; g.b_seg_row = 0;
     g.N = s.inter; g.b_group_rows = up_rows(s, s.inter); g.up_off = s.inter;
     g.out = h; g.ldo = s.inter; g.out_group_col = 0;
+    g.max_group_rows = s.tokens;   // a token's k experts are distinct
     moe_status r = launch_grouped_gemm(g, hdr, st);
     if (r != MOE_OK || s.shared == 0) return r;
     GemmProblem q{};
@@ -137,6 +138,7 @@ moe_status do_down(const moe_shape& s, const uint16_t* h, const int32_t* offsets
     g.K = s.inter; g.nseg = 1; g.a_seg_col = 0; g.b_seg_row = 0;
     g.N = s.hidden; g.b_group_rows = s.hidden; g.up_off = 0;
     g.out = y_perm; g.ldo = s.hidden; g.out_group_col = 0;
+    g.max_group_rows = s.tokens;
     moe_status r = launch_grouped_gemm(g, hdr, st);
     if (r != MOE_OK || s.shared == 0) return r;
     // all shared experts in one accumulation: K runs over (s, n), so their sum

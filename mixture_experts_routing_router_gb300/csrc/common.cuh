@@ -5,6 +5,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 
@@ -74,6 +75,7 @@ constexpr unsigned long long kWaitLimitNs = 2000000000ull;   // 2 s
 // Where a bounded wait gave up (WsHeader::timeout_site).
 enum TimeoutSite : int {
     kSiteNone = 0, kSiteLookback = 1, kSiteGemmProducer = 2, kSiteGemmMma = 3, kSiteGemmEpilogue = 4,
+    kSiteGemmDecode = 5,
 };
 
 // ---------------------------------------------------------------------------
@@ -191,6 +193,15 @@ __device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, uint32_t (&r)[32]
           "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
           "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
           "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+// 16 consecutive FP32 columns of this warp's 32 TMEM lanes.
+__device__ __forceinline__ void tmem_ld_16cols(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
@@ -311,9 +322,22 @@ struct GemmProblem {
     int b_group_rows;
     int up_off;                                           // SwiGLU: rows from gate to up half
     void* out; long long ldo; int out_group_col;
+    int max_group_rows;                                   // host bound on rows per group (0: a_rows)
 };
 // Returns MOE_OK, MOE_ERR_CUDA (tensor map / launch) or MOE_ERR_UNSUPPORTED.
+// Problems whose groups hold at most kDecodeRows rows and whose work fits in
+// about two waves run the small-row kernel (launch_decode_gemm); the rest the
+// tile kernels.
 moe_status launch_grouped_gemm(const GemmProblem& p, WsHeader* hdr, cudaStream_t st);
+
+// Small-row form: weights on the MMA's M side, nb (16..kDecodeRows, a
+// multiple of 16) activation rows per chunk on its N side.
+constexpr int kDecodeRows = 64;
+moe_status launch_decode_gemm(const GemmProblem& p, int nb, WsHeader* hdr, cudaStream_t st);
+
+// Tensor map of a row-major [rows, cols] BF16 matrix, 128-byte swizzle, boxes
+// of 64 columns x box_rows rows (records the failure for moe_last_error_message).
+bool make_tensor_map_bf16(CUtensorMap* m, const void* base, long long rows, long long cols, unsigned box_rows);
 
 int device_sm_count();
 

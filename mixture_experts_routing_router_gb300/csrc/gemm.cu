@@ -22,7 +22,10 @@
 // Three tile shapes, chosen per launch:
 //   * CTA pair (groups averaging >= 256 rows, e.g. the large layer's experts):
 //     two SMs share a 256-row tile through tcgen05.mma.cta_group::2, each
-//     loading its own A rows and half of B -- see grouped_gemm_pair_kernel.
+//     loading its own A rows and half of B; a group's partial last tile runs
+//     with the operands swapped -- see grouped_gemm_pair_kernel.
+// Groups of at most a few dozen rows (decode) run the small-row kernel in
+// gemm_decode.cu when its work fits in about two waves.
 //   * single CTA, HALVES = 1 (fewer rows per group, K < 4096): 128-row tiles,
 //     two 256-column accumulators in TMEM so the epilogue of one tile overlaps
 //     the main loop of the next; 4 stages of 48 KiB; 4 epilogue warps.
@@ -63,7 +66,7 @@ constexpr int kTailRows = 64;
 // Dynamic shared memory ceiling set on the kernels: the stage ring plus the
 // control block and the per-group tables of up to 1024 groups.  It stays below
 // the 227 KiB opt-in limit minus the kernel's small static shared memory.
-constexpr int MAX_DYN_SMEM = 212 * 1024;
+constexpr int MAX_DYN_SMEM = 216 * 1024;
 // Reductions at least this long use the 256-row tile (HALVES = 2).
 constexpr long long kLongK = 4096;
 // Groups averaging at least this many rows use the CTA-pair kernel (compute
@@ -109,6 +112,9 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<const uint32_t*>(&b);
 }
+
+// The four epilogue warps of a CTA (named barrier 1; __syncthreads uses 0).
+__device__ __forceinline__ void epi_bar_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 struct Tile { int g, mt, nt, row0, mrows; };
 
@@ -459,12 +465,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 // ---------------------------------------------------------------------------
 // The CTA-pair shape.  A cluster of two CTAs (two SMs) owns a 256-row tile:
 // each CTA TMA-loads its own 128 A rows and its half of the 256-row B tile
-// (gate rows in CTA 0 and up rows in CTA 1 for SwiGLU), so a CTA moves 32 KiB
-// per 64-wide K step instead of 48, and six stages fit.  The leader CTA's MMA
-// thread issues tcgen05.mma.cta_group::2 (M 256, N 256; M 128 -- 64 rows per
-// CTA -- for a tile of 128 rows or fewer) reading both CTAs' shared memory and
-// writing both CTAs' TMEM; its commits arrive on the same barrier offsets in
-// both CTAs.  Each CTA keeps two 256-column accumulators, so the epilogue of
+// (for SwiGLU, 64 gate rows and the matching 64 up rows per CTA), so a CTA
+// moves 32 KiB per 64-wide K step instead of 48, and six stages fit.  The
+// leader CTA's MMA thread issues tcgen05.mma.cta_group::2 (M 256, N 256)
+// reading both CTAs' shared memory and writing both CTAs' TMEM; its commits
+// arrive on the same barrier offsets in both CTAs.  A group's partial last
+// tile swaps the operands (weights M 256, rows N = rows padded to 16).  Each CTA keeps two 256-column accumulators, so the epilogue of
 // one tile overlaps the next tile's main loop.  Both CTAs' TMA loads count on
 // the leader's stage barrier; both CTAs' epilogues release the leader's
 // accumulator barrier.  No multicast load: each CTA reads only its own part.
@@ -474,7 +480,12 @@ constexpr int P_STAGE_BYTES = A_BYTES + B_HALF_BYTES;   // 32 KiB per CTA
 constexpr int P_THREADS = 192;
 constexpr int P_BMT = 256;
 constexpr uint32_t P_IDESC_FULL = idesc_bf16_f32(256, BN_MMA);
-constexpr uint32_t P_IDESC_TAIL = idesc_bf16_f32(128, BN_MMA);
+// A group's last row tile with fewer than 256 rows is computed with the
+// operands swapped (D^T = W * X^T): the pair's 256 weight rows (each CTA's B
+// half) on the MMA's M side and the tile's rows, padded to 16, on its N side.
+// A 5-row tile then costs 16 rows of tensor work instead of 128; under the
+// power cap the saved tensor work is saved time.
+constexpr int P_XG_FLOATS = 64 * 17;                    // SwiGLU gate exchange (64 rows x 16, padded)
 
 struct PairCtl {
     unsigned long long full[P_STAGES];
@@ -499,6 +510,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
     int* prefix = reinterpret_cast<int*>(ctl + 1);
     int* rstart = prefix + (p.groups + 1);
     int* rcount = rstart + p.groups;
+    float* xg = reinterpret_cast<float*>(rcount + p.groups);        // [P_XG_FLOATS]
     const uint32_t smem_base = smem_u32(smem);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -584,8 +596,12 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
             bool ok = true;
             for (int tile = pair; tile < total && ok; tile += npairs) {
                 const Tile t = decode_tile<MODE == kGemmSwiGLU || MODE == kGemmReLU2>(tile, prefix, rstart, rcount, p, ntn, P_BMT);
-                const bool tail = t.mrows - t.mt * P_BMT <= BM;
-                const int a_row = t.row0 + t.mt * P_BMT + (int)rank * (tail ? 64 : BM);
+                const int rows_t = t.mrows - t.mt * P_BMT;             // rows of this tile
+                const bool swap = rows_t < P_BMT;
+                const int npad = (rows_t + 15) & ~15;
+                // this CTA's rows of the tile: all 256 rows split 128/128 (full), or the
+                // padded rows split npad/2 each (swapped)
+                const int a_row = t.row0 + t.mt * P_BMT + (int)rank * (swap ? npad / 2 : BM);
                 const int n0 = t.nt * BN_OUT;
                 // B half of this CTA: SwiGLU -- 64 gate rows and the matching 64 up
                 // rows of output columns n0 + 64*rank ..; otherwise 128 rows
@@ -597,13 +613,16 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
                     const uint32_t full_leader = mapa_shared(full_local, 0);
                     if (rank == 0) mbar_arrive_expect_tx(full_local, 2 * P_STAGE_BYTES);
                     const uint32_t sa = smem_base + stage * P_STAGE_BYTES;
-                    tma_load_2d_pair(sa, &tmA, full_leader, seg * p.a_seg_col + kb * BK, a_row);
+                    // swapped: weights in the MMA's A slot, rows in its B slot (16 KiB each)
+                    const uint32_t s_rows = swap ? sa + A_BYTES : sa;
+                    const uint32_t s_w = swap ? sa : sa + A_BYTES;
+                    tma_load_2d_pair(s_rows, &tmA, full_leader, seg * p.a_seg_col + kb * BK, a_row);
                     if (MODE == kGemmSwiGLU) {   // two 64-row boxes: gate, then up
-                        tma_load_2d_pair(sa + A_BYTES, &tmB, full_leader, kb * BK, b_row + seg * p.b_seg_row);
-                        tma_load_2d_pair(sa + A_BYTES + B_HALF_BYTES / 2, &tmB, full_leader, kb * BK,
+                        tma_load_2d_pair(s_w, &tmB, full_leader, kb * BK, b_row + seg * p.b_seg_row);
+                        tma_load_2d_pair(s_w + B_HALF_BYTES / 2, &tmB, full_leader, kb * BK,
                                          b_row + p.up_off + seg * p.b_seg_row);
                     } else {
-                        tma_load_2d_pair(sa + A_BYTES, &tmB, full_leader, kb * BK, b_row + seg * p.b_seg_row);
+                        tma_load_2d_pair(s_w, &tmB, full_leader, kb * BK, b_row + seg * p.b_seg_row);
                     }
                     if (++stage == P_STAGES) { stage = 0; ph ^= 1u; }
                 }
@@ -625,8 +644,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
             bool ok = true;
             for (int tile = pair; tile < total && ok; tile += npairs) {
                 const Tile t = decode_tile<MODE == kGemmSwiGLU || MODE == kGemmReLU2>(tile, prefix, rstart, rcount, p, ntn, P_BMT);
-                const bool tail = t.mrows - t.mt * P_BMT <= BM;
-                const uint32_t idesc = tail ? P_IDESC_TAIL : P_IDESC_FULL;
+                const int rows_t = t.mrows - t.mt * P_BMT;
+                const uint32_t idesc = rows_t < P_BMT ? idesc_bf16_f32(256, (rows_t + 15) & ~15) : P_IDESC_FULL;
                 if (!mbar_wait_bounded(smem_u32(&ctl->tempty[acc]), aph ^ 1u, abort)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d = tmem_base + (uint32_t)(acc * BN_MMA);
@@ -664,7 +683,6 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
         uint32_t aph = 0;
         for (int tile = pair; tile < total; tile += npairs) {
             const Tile t = decode_tile<MODE == kGemmSwiGLU || MODE == kGemmReLU2>(tile, prefix, rstart, rcount, p, ntn, P_BMT);
-            const bool tail = t.mrows - t.mt * P_BMT <= BM;
             if (!mbar_wait_bounded(smem_u32(&ctl->tfull[acc]), aph, abort)) {
                 if (lane == 0) {
                     raise_status(p.hdr, MOE_ERR_TIMEOUT);
@@ -673,33 +691,80 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
                 break;
             }
             tc_fence_after();
-            // D columns 0..127 come from CTA 0's B half, 128..255 from CTA 1's.
-            // Full tile (M 256): this CTA's 128 rows, lane = row, all 256 columns.
-            // Tail (M 128): this CTA's 64 rows; lanes 0..63 hold columns 0..127 and
-            // lanes 64..127 the same rows' columns 128..255.
-            const int bb = tail ? (q >> 1) : 0;                            // column block of the lanes
-            const int rin = tail ? (int)rank * 64 + (q & 1) * 32 + lane : (int)rank * BM + q * 32 + lane;
-            const int r = t.mt * P_BMT + rin;
-            const bool live = t.mt * P_BMT + (tail ? (int)rank * 64 + (q & 1) * 32 : (int)rank * BM + q * 32) < t.mrows;
-            if (live) {
-                const bool row_ok = r < t.mrows;
-                auto* orow = out_row<MODE>(p, t.row0 + (row_ok ? r : 0), t.g);
+            const int rows_t = t.mrows - t.mt * P_BMT;
+            if (rows_t < P_BMT) {
+                // Swapped: TMEM lane = this CTA's weight row i (its B half), column j =
+                // row j of the tile.  SwiGLU: lanes 0..63 gate, 64..127 up of output
+                // columns n0 + 64*rank + (i mod 64); the gate values cross to the up
+                // warps through shared memory, 16 rows at a time.
+                const int i = q * 32 + lane;
+                const int n0 = t.nt * BN_OUT;
+                const bool gate = MODE == kGemmSwiGLU && q < 2;
+                const int col = (MODE == kGemmSwiGLU) ? n0 + 64 * (int)rank + (i & 63) : n0 + 128 * (int)rank + i;
+                const bool col_ok = col < p.N;
+                const uint32_t tl = tmem_base + (uint32_t)(acc * BN_MMA) + ((uint32_t)(q * 32) << 16);
+                const int npad = (rows_t + 15) & ~15;
+                for (int c = 0; c < npad; c += 16) {
+                    uint32_t v[16];
+                    tmem_ld_16cols(tl + (uint32_t)c, v);
+                    tmem_ld_wait();
+                    if (MODE == kGemmSwiGLU) {
+                        if (gate) {
+#pragma unroll
+                            for (int u = 0; u < 16; ++u) xg[i * 17 + u] = __uint_as_float(v[u]);
+                        }
+                        epi_bar_sync();
+                        if (!gate && col_ok) {
+#pragma unroll
+                            for (int u = 0; u < 16; ++u) {
+                                const int row = c + u;
+                                if (row < rows_t) {
+                                    const float g = xg[(i - 64) * 17 + u];
+                                    out_row<MODE>(p, t.row0 + t.mt * P_BMT + row, t.g)[col] =
+                                        __float2bfloat16_rn(g / (1.0f + __expf(-g)) * __uint_as_float(v[u]));
+                                }
+                            }
+                        }
+                        epi_bar_sync();
+                    } else if (col_ok) {
+#pragma unroll
+                        for (int u = 0; u < 16; ++u) {
+                            const int row = c + u;
+                            if (row < rows_t) {
+                                const float x = __uint_as_float(v[u]);
+                                auto* o = out_row<MODE>(p, t.row0 + t.mt * P_BMT + row, t.g) + col;
+                                if constexpr (MODE == kGemmF32) *o = x;
+                                else *o = __float2bfloat16_rn(MODE == kGemmReLU2 ? (x > 0.f ? x * x : 0.f) : x);
+                            }
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&ctl->tempty[acc]), 0));
+                acc ^= 1;
+                if (acc == 0) aph ^= 1u;
+                continue;
+            }
+            {
+                // Full tile (M 256): lane = this CTA's row 128*rank + 32q + lane, all
+                // 256 columns; D columns 0..127 come from CTA 0's B half, 128..255
+                // from CTA 1's.
+                const int r = t.mt * P_BMT + (int)rank * BM + q * 32 + lane;
+                auto* orow = out_row<MODE>(p, t.row0 + r, t.g);
                 const uint32_t tl = tmem_base + (uint32_t)(acc * BN_MMA) + ((uint32_t)(q * 32) << 16);
                 const int n0 = t.nt * BN_OUT;
                 if (MODE == kGemmSwiGLU) {
                     // each 128-column block is [64 gate | 64 up] of output columns 64 * block ..
-                    const int nblk = tail ? 1 : 2;
 #pragma unroll 1
-                    for (int b = 0; b < nblk; ++b)
+                    for (int b = 0; b < 2; ++b)
 #pragma unroll 1
                         for (int i0 = 0; i0 < 64; i0 += 32)
-                            epilogue_chunk<MODE>(tl + b * 128 + i0, tl + b * 128 + 64 + i0, row_ok, orow,
-                                                 n0 + 64 * (b + bb) + i0, p.N);
+                            epilogue_chunk<MODE>(tl + b * 128 + i0, tl + b * 128 + 64 + i0, true, orow,
+                                                 n0 + 64 * b + i0, p.N);
                 } else {
-                    const int nch = tail ? 4 : 8;
 #pragma unroll 1
-                    for (int c = 0; c < nch; ++c)
-                        epilogue_chunk<MODE>(tl + c * 32, 0, row_ok, orow, n0 + 128 * bb + c * 32, p.N);
+                    for (int c = 0; c < 8; ++c) epilogue_chunk<MODE>(tl + c * 32, 0, true, orow, n0 + c * 32, p.N);
                 }
             }
             tc_fence_before();
@@ -808,7 +873,8 @@ cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const KPar
 }
 
 size_t pair_smem_bytes(int groups) {
-    return 1024 + (size_t)P_STAGES * P_STAGE_BYTES + sizeof(PairCtl) + 3 * (size_t)(groups + 1) * 4;
+    return 1024 + (size_t)P_STAGES * P_STAGE_BYTES + sizeof(PairCtl) + 3 * (size_t)(groups + 1) * 4 +
+           (size_t)P_XG_FLOATS * 4;
 }
 
 template <int HALVES>
@@ -819,10 +885,25 @@ size_t smem_bytes(int groups) {
 
 }  // namespace
 
+bool make_tensor_map_bf16(CUtensorMap* m, const void* base, long long rows, long long cols, unsigned box_rows) {
+    return make_map(m, base, rows, cols, box_rows);
+}
+
 moe_status launch_grouped_gemm(const GemmProblem& g, WsHeader* hdr, cudaStream_t st) {
     if (g.groups < 1 || g.groups > 1024 || g.K < 1 || g.N < 1) {
         set_error("grouped GEMM: unsupported problem (groups %d, K %d, N %d)", g.groups, g.K, g.N);
         return MOE_ERR_UNSUPPORTED;
+    }
+    // A bound on the rows of any group: a few dozen rows make the GEMM a weight
+    // stream.  When its work items (non-empty groups x 128-row weight blocks)
+    // fit in about two waves the small-row kernel spreads them over more SMs and
+    // starts sooner; with many more items the tile kernels' larger tiles
+    // stream a few percent better (measured at 1 to 16 tokens over 240 experts).
+    const long long row_bound = g.offsets ? (g.max_group_rows > 0 ? g.max_group_rows : g.a_rows) : g.rows_all;
+    if (row_bound <= kDecodeRows) {
+        const long long slots = g.offsets ? (g.a_rows < g.groups ? g.a_rows : g.groups) : g.groups;
+        if (slots * ((g.N + 127) / 128) <= 2LL * device_sm_count())
+            return launch_decode_gemm(g, row_bound < 16 ? 16 : (int)((row_bound + 15) / 16 * 16), hdr, st);
     }
     const long long avg_rows = g.offsets ? g.a_rows / g.groups : g.rows_all;
     const bool pairs = avg_rows >= kPairRows && device_sm_count() >= 2;

@@ -1,0 +1,391 @@
+// gemm_decode.cu -- K8, the small-row ("decode") form of the grouped GEMM.
+//
+// At decode a routed expert sees a handful of tokens (ONNX Runtime PR #33963,
+// "Measured CUDA kernel latency": 1, 8 and 16 rows over 9 experts of 240), so
+// every weight element serves a few rows and the layer streams weights.  This
+// kernel swaps the operands of the grouped GEMM: D^T = W * X^T, with 128 weight
+// rows on the MMA's M side and NB of the group's rows (16..64, a multiple of
+// 16) on its N side, FP32 in TMEM.  A work item is one 128-row block of one
+// non-empty group's weights, so a single token already spreads its experts'
+// weights over ~100 SMs.  A group with more than NB rows is taken in NB-row
+// chunks, re-streaming its weights per chunk (correct for any bucket; the host
+// picks NB from a bound on the rows per group).
+//
+// Persistent CTAs (at most one per SM) take items round-robin.  Roles: warp 0
+// lane 0 issues the TMA loads of a ring of stages (weights: one 128-row box,
+// SwiGLU two -- the gate rows and the matching up rows; activations: one
+// NB-row box); warp 1 lane 0 issues tcgen05.mma into one of two accumulators;
+// warps 2..5 run the epilogue (warp w owns TMEM lanes 32(w%4)..+31, i.e. the
+// output columns n0 + 32(w%4) + lane) while the next item streams.  The list
+// of non-empty groups is built once per CTA from the offsets.
+//
+// The epilogue arithmetic is the tile kernels': SwiGLU silu(g)*u, ReLU^2,
+// plain, or the FP32 accumulator.  Every wait is bounded (MOE_ERR_TIMEOUT,
+// TMEM freed, no trap).
+#include "common.cuh"
+
+#include <mutex>
+
+namespace moe {
+namespace {
+
+constexpr int DBM = 128;                   // weight rows per item (MMA M)
+constexpr int DBK = 64;                    // 64 BF16 = one 128-byte swizzle row
+constexpr int W_BYTES = DBM * DBK * 2;     // 16 KiB weight box
+constexpr int DTHREADS = 192;              // producer, MMA, 4 epilogue warps
+constexpr int MAX_DSTAGES = 16;
+constexpr int MAX_DSMEM = 212 * 1024;
+
+struct DParams {
+    const int32_t* offsets;
+    int groups, rows_all;
+    int a_rows;                 // rows of the activation matrix (bucket bounds are clamped to it)
+    int K, nseg, a_seg_col, b_seg_row;
+    int N, b_group_rows, up_off;
+    void* out;
+    long long ldo;
+    int out_group_col;
+    WsHeader* hdr;
+    int nb;                     // activation rows per chunk (MMA N): 16, 32, 48 or 64
+    int stages, stage_bytes;
+    uint32_t tmem_cols;         // two accumulators of (SwiGLU ? 2 : 1) * nb columns, power of two
+};
+
+template <int MODE> struct OutOfD { using T = __nv_bfloat16; };
+template <> struct OutOfD<kGemmF32> { using T = float; };
+
+struct DCtl {
+    unsigned long long full[MAX_DSTAGES];
+    unsigned long long empty[MAX_DSTAGES];
+    unsigned long long tfull[2];
+    unsigned long long tempty[2];
+    unsigned long long drain;
+    uint32_t tmem_base;
+    int abort;
+    int ng;                     // non-empty groups
+    int wsum[DTHREADS / 32];
+};
+
+__device__ __forceinline__ void clamped_bounds(const DParams& p, int g, int& lo, int& hi) {
+    lo = p.offsets[g];
+    hi = p.offsets[g + 1];
+    lo = lo < 0 ? 0 : (lo > p.a_rows ? p.a_rows : lo);
+    hi = hi < lo ? lo : (hi > p.a_rows ? p.a_rows : hi);
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(DTHREADS, 1)
+decode_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                   const DParams p) {
+    constexpr int NW = (MODE == kGemmSwiGLU) ? 2 : 1;      // weight boxes per stage
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_u32 = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + ((1024u - (raw_u32 & 1023u)) & 1023u);
+    DCtl* ctl = reinterpret_cast<DCtl*>(smem + p.stages * p.stage_bytes);
+    int* gid = reinterpret_cast<int*>(ctl + 1);            // [groups] non-empty groups, in order
+    int* gst = gid + p.groups;                              // first row
+    int* gcnt = gst + p.groups;                             // rows
+    const uint32_t smem_base = smem_u32(smem);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    // ---- the non-empty groups (block-wide compaction of the offsets) --------
+    if (p.offsets) {
+        const int per = (p.groups + DTHREADS - 1) / DTHREADS;
+        const int g0 = tid * per;
+        int cnt = 0;
+        for (int i = 0; i < per; ++i) {
+            const int g = g0 + i;
+            if (g < p.groups) {
+                int lo, hi;
+                clamped_bounds(p, g, lo, hi);
+                cnt += hi > lo;
+            }
+        }
+        int inc = cnt;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, inc, off);
+            if (lane >= off) inc += v;
+        }
+        if (lane == 31) ctl->wsum[warp] = inc;
+        __syncthreads();
+        int k = inc - cnt;
+        for (int w = 0; w < warp; ++w) k += ctl->wsum[w];
+        if (tid == DTHREADS - 1) ctl->ng = k + cnt;
+        for (int i = 0; i < per; ++i) {
+            const int g = g0 + i;
+            if (g < p.groups) {
+                int lo, hi;
+                clamped_bounds(p, g, lo, hi);
+                if (hi > lo) { gid[k] = g; gst[k] = lo; gcnt[k] = hi - lo; ++k; }
+            }
+        }
+    } else {
+        for (int g = tid; g < p.groups; g += DTHREADS) {
+            gid[g] = g;
+            gst[g] = 0;
+            gcnt[g] = p.rows_all < p.a_rows ? p.rows_all : p.a_rows;
+        }
+        if (tid == 0) ctl->ng = p.groups;
+    }
+
+    // ---- set-up: barriers, TMEM ----------------------------------------------
+    if (tid == 0) {
+        for (int s = 0; s < p.stages; ++s) {
+            mbar_init(smem_u32(&ctl->full[s]), 1);
+            mbar_init(smem_u32(&ctl->empty[s]), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(smem_u32(&ctl->tfull[a]), 1);
+            mbar_init(smem_u32(&ctl->tempty[a]), 4);        // the 4 epilogue warps
+        }
+        mbar_init(smem_u32(&ctl->drain), 1);
+        ctl->abort = 0;
+        fence_mbar_init();
+        fence_proxy_async_smem();
+        tma_prefetch_desc(&tmX);
+        tma_prefetch_desc(&tmW);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&ctl->tmem_base), p.tmem_cols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ctl->tmem_base;
+    volatile int* abort = &ctl->abort;
+    const int ntn = (p.N + DBM - 1) / DBM;
+    const int items = ctl->ng * ntn;
+    const int nkb = (p.K + DBK - 1) / DBK;
+    const int nk = nkb * p.nseg;
+    const int nb = p.nb;
+    const uint32_t acc_cols = (uint32_t)(NW * nb);
+    const uint32_t x_off = (uint32_t)(NW * W_BYTES);
+
+    if (warp == 0) {
+        // ---------------- TMA producer ----------------
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
+                const int slot = it / ntn, nt = it - slot * ntn;
+                const int g = gid[slot], row0 = gst[slot], rows = gcnt[slot];
+                const int w_row = g * p.b_group_rows + nt * DBM;
+                for (int xr = row0; xr < row0 + rows && ok; xr += nb) {
+                    for (int i = 0; i < nk; ++i) {
+                        const int seg = i / nkb, kb = i - seg * nkb;
+                        if (!mbar_wait_bounded(smem_u32(&ctl->empty[stage]), ph ^ 1u, abort)) { ok = false; break; }
+                        const uint32_t full = smem_u32(&ctl->full[stage]);
+                        mbar_arrive_expect_tx(full, (uint32_t)p.stage_bytes);
+                        const uint32_t sa = smem_base + (uint32_t)(stage * p.stage_bytes);
+                        tma_load_2d(sa, &tmW, full, kb * DBK, w_row + seg * p.b_seg_row);
+                        if (MODE == kGemmSwiGLU)
+                            tma_load_2d(sa + W_BYTES, &tmW, full, kb * DBK, w_row + p.up_off + seg * p.b_seg_row);
+                        tma_load_2d(sa + x_off, &tmX, full, seg * p.a_seg_col + kb * DBK, xr);
+                        if (++stage == p.stages) { stage = 0; ph ^= 1u; }
+                    }
+                }
+            }
+            if (!ok) {
+                // let copies already issued land before the CTA exits
+                const unsigned long long t0 = globaltimer_ns();
+                while (globaltimer_ns() - t0 < 1000000ull) { }
+                raise_status(p.hdr, MOE_ERR_TIMEOUT);
+                p.hdr->timeout_site = kSiteGemmDecode;
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16_f32(DBM, nb);
+            int stage = 0, acc = 0;
+            uint32_t ph = 0, aph = 0;
+            bool ok = true;
+            for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
+                const int rows = gcnt[it / ntn];
+                for (int c0 = 0; c0 < rows && ok; c0 += nb) {
+                    if (!mbar_wait_bounded(smem_u32(&ctl->tempty[acc]), aph ^ 1u, abort)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t d = tmem + (uint32_t)acc * acc_cols;
+                    for (int i = 0; i < nk; ++i) {
+                        if (!mbar_wait_bounded(smem_u32(&ctl->full[stage]), ph, abort)) { ok = false; break; }
+                        tc_fence_after();
+                        const uint32_t sa = smem_base + (uint32_t)(stage * p.stage_bytes);
+                        const uint64_t wd = sdesc_k_sw128(sa);
+                        const uint64_t xd = sdesc_k_sw128(sa + x_off);
+#pragma unroll
+                        for (int kk = 0; kk < DBK / 16; ++kk) {
+                            const uint32_t accum = (i > 0 || kk > 0) ? 1u : 0u;
+                            tc_mma_bf16(d, wd + (uint64_t)(kk * 2), xd + (uint64_t)(kk * 2), idesc, accum);
+                            if (MODE == kGemmSwiGLU)
+                                tc_mma_bf16(d + (uint32_t)nb, sdesc_k_sw128(sa + W_BYTES) + (uint64_t)(kk * 2),
+                                            xd + (uint64_t)(kk * 2), idesc, accum);
+                        }
+                        tc_commit(smem_u32(&ctl->empty[stage]));
+                        if (++stage == p.stages) { stage = 0; ph ^= 1u; }
+                    }
+                    if (!ok) break;
+                    tc_commit(smem_u32(&ctl->tfull[acc]));
+                    if (++acc == 2) { acc = 0; aph ^= 1u; }
+                }
+            }
+            // drain: wait until every MMA this thread issued has completed
+            tc_commit(smem_u32(&ctl->drain));
+            volatile int never = 0;
+            const bool drained = mbar_wait_bounded(smem_u32(&ctl->drain), 0, &never);
+            if (!ok || !drained) {
+                raise_status(p.hdr, MOE_ERR_TIMEOUT);
+                p.hdr->timeout_site = kSiteGemmDecode;
+                *abort = 1;
+            }
+        }
+    } else {
+        // ---------------- epilogue (warps 2..5) ----------------
+        const int q = warp & 3;                                 // TMEM lane quarter
+        int acc = 0;
+        uint32_t aph = 0;
+        bool ok = true;
+        for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
+            const int slot = it / ntn, nt = it - slot * ntn;
+            const int g = gid[slot], row0 = gst[slot], rows = gcnt[slot];
+            const int n = nt * DBM + 32 * q + lane;             // weight row = output column
+            typename OutOfD<MODE>::T* ocol = reinterpret_cast<typename OutOfD<MODE>::T*>(p.out) +
+                                             (size_t)g * p.out_group_col + (n < p.N ? n : 0);
+            for (int c0 = 0; c0 < rows; c0 += nb) {
+                if (!mbar_wait_bounded(smem_u32(&ctl->tfull[acc]), aph, abort)) {
+                    if (lane == 0) {
+                        raise_status(p.hdr, MOE_ERR_TIMEOUT);
+                        p.hdr->timeout_site = kSiteGemmDecode;
+                    }
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t taddr = tmem + (uint32_t)acc * acc_cols + ((uint32_t)(32 * q) << 16);
+                for (int c = 0; c < nb; c += 16) {
+                    uint32_t gv[16], uv[16];
+                    tmem_ld_16cols(taddr + (uint32_t)c, gv);
+                    if (MODE == kGemmSwiGLU) tmem_ld_16cols(taddr + (uint32_t)(nb + c), uv);
+                    tmem_ld_wait();
+                    if (n < p.N) {
+#pragma unroll
+                        for (int r = 0; r < 16; ++r) {
+                            const int row = c0 + c + r;
+                            if (row < rows) {
+                                const float x = __uint_as_float(gv[r]);
+                                auto* o = ocol + (size_t)(row0 + row) * p.ldo;
+                                if constexpr (MODE == kGemmF32) {
+                                    *o = x;
+                                } else {
+                                    float a;
+                                    if (MODE == kGemmSwiGLU) a = x / (1.0f + __expf(-x)) * __uint_as_float(uv[r]);
+                                    else if (MODE == kGemmReLU2) a = x > 0.f ? x * x : 0.f;
+                                    else a = x;
+                                    *o = __float2bfloat16_rn(a);
+                                }
+                            }
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[acc]));
+                if (++acc == 2) { acc = 0; aph ^= 1u; }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, p.tmem_cols);
+    }
+}
+
+template <int MODE>
+cudaError_t launch_d(const CUtensorMap& mx, const CUtensorMap& mw, const DParams& dp, unsigned grid, size_t smem,
+                     cudaStream_t st) {
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [] {
+        attr_err = cudaFuncSetAttribute(decode_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        MAX_DSMEM);
+    });
+    if (attr_err != cudaSuccess) {
+        set_error("cudaFuncSetAttribute(decode GEMM, %d bytes): %s", MAX_DSMEM, cudaGetErrorString(attr_err));
+        return attr_err;
+    }
+    decode_gemm_kernel<MODE><<<grid, DTHREADS, smem, st>>>(mx, mw, dp);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) set_error("decode GEMM launch: %s", cudaGetErrorString(e));
+    return e;
+}
+
+}  // namespace
+
+moe_status launch_decode_gemm(const GemmProblem& g, int nb, WsHeader* hdr, cudaStream_t st) {
+    if (nb < 16 || nb > kDecodeRows || nb % 16 != 0) {
+        set_error("decode GEMM: %d rows per chunk is not a multiple of 16 in [16, %d]", nb, kDecodeRows);
+        return MOE_ERR_INTERNAL;
+    }
+    const int nw = g.mode == kGemmSwiGLU ? 2 : 1;
+    DParams dp;
+    dp.offsets = g.offsets;
+    dp.groups = g.groups;
+    dp.rows_all = g.rows_all;
+    dp.a_rows = (int)g.a_rows;
+    dp.K = g.K;
+    dp.nseg = g.nseg;
+    dp.a_seg_col = g.a_seg_col;
+    dp.b_seg_row = g.b_seg_row;
+    dp.N = g.N;
+    dp.b_group_rows = g.b_group_rows;
+    dp.up_off = g.up_off;
+    dp.out = g.out;
+    dp.ldo = g.ldo;
+    dp.out_group_col = g.out_group_col;
+    dp.hdr = hdr;
+    dp.nb = nb;
+    dp.stage_bytes = nw * W_BYTES + nb * DBK * 2;
+    uint32_t cols = 32;
+    while (cols < (uint32_t)(2 * nw * nb)) cols <<= 1;
+    dp.tmem_cols = cols;
+
+    // items: (non-empty group) x (128-row weight block); at most one CTA per SM
+    const long long ntn = (g.N + DBM - 1) / DBM;
+    const long long slots = g.offsets ? (g.a_rows < g.groups ? g.a_rows : g.groups) : g.groups;
+    long long grid = slots * ntn;
+    const int sms = device_sm_count();
+    if (grid > sms) grid = sms;
+    if (grid < 1) grid = 1;
+    const size_t fixed = 1024 + sizeof(DCtl) + (size_t)3 * g.groups * sizeof(int);
+    const int nk = ((g.K + DBK - 1) / DBK) * g.nseg;
+    long long stages = ((long long)MAX_DSMEM - (long long)fixed) / dp.stage_bytes;
+    if (stages > MAX_DSTAGES) stages = MAX_DSTAGES;
+    if (stages > 2 * nk) stages = 2 * nk;              // two items' worth is plenty
+    if (stages < 2) stages = 2;
+    dp.stages = (int)stages;
+    const size_t smem = fixed + (size_t)stages * dp.stage_bytes;
+    if (smem > (size_t)MAX_DSMEM) {
+        set_error("decode GEMM needs %zu bytes of shared memory", smem);
+        return MOE_ERR_UNSUPPORTED;
+    }
+    CUtensorMap mx, mw;
+    if (!make_tensor_map_bf16(&mx, g.a, g.a_rows, g.a_cols, (unsigned)nb)) return MOE_ERR_CUDA;
+    if (!make_tensor_map_bf16(&mw, g.b, g.b_rows, g.b_cols, (unsigned)DBM)) return MOE_ERR_CUDA;
+    cudaError_t e;
+    switch (g.mode) {
+        case kGemmSwiGLU: e = launch_d<kGemmSwiGLU>(mx, mw, dp, (unsigned)grid, smem, st); break;
+        case kGemmReLU2: e = launch_d<kGemmReLU2>(mx, mw, dp, (unsigned)grid, smem, st); break;
+        case kGemmF32: e = launch_d<kGemmF32>(mx, mw, dp, (unsigned)grid, smem, st); break;
+        default: e = launch_d<kGemmPlain>(mx, mw, dp, (unsigned)grid, smem, st); break;
+    }
+    return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // namespace moe

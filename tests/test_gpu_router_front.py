@@ -60,7 +60,8 @@ def test_route_sigmoid_ties_and_nonfinite():
 
 
 GATE_CASES = {
-    "tiny": W["tiny"],                                        # single-CTA tile
+    "tiny": W["tiny"],                                        # 64 rows: small-row kernel
+    "decode_16": W["decode_16_distinct"],                     # 16 rows, 240 experts: small-row kernel
     "count_first": W["count_first"],                          # 2048 rows: CTA pair
     "ragged": synth.Workload("ragged", 300, 136, 33, 2, 64),  # E = 33: element stores, K tail
     "large": W["large"],                                      # the large layer, sampled rows

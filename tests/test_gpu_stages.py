@@ -240,6 +240,28 @@ def test_expert_ffn_full(name, unit):
         assert_close(bits(o["y_shared"]), ref["y_shared"], f"{name} y_shared")
 
 
+@pytest.mark.parametrize("act", [synth.ACT_SWIGLU, synth.ACT_RELU2])
+def test_expert_ffn_buckets_above_the_row_bound(act):
+    """Caller-made offsets may hold more rows in a group than the token count
+    (here 100 and 28 rows at 16 tokens): the small-row kernel, picked from the
+    token count, then takes such a group in 16-row chunks."""
+    wl = synth.Workload("chunked", 16, 192, 8, 8, 96, act=act)
+    g = inputs(wl, unit_scale=True, seed=12)
+    R = wl.pairs
+    x_perm = synth.normal((R, wl.hidden), 1.0, 12, "x_perm", dev())
+    offsets = np.array([0, 100, 100, 100, 128, 128, 128, 128, 128], np.int32)
+    h_ref, y_ref, _, _ = oracle.expert_ffn(bits(x_perm), offsets, bits(g["w13"]), bits(g["w2"]), wl.act)
+    shape = N.shape_of(wl)
+    ws = N.workspace(shape, dev())
+    o = alloc_stage_outputs(wl)
+    N.moe_expert_up(shape, x_perm, i32_dev(offsets), g["w13"], g["x"], None, o["h"], ws)
+    assert N.moe_status_read(ws) == N.MOE_OK
+    assert_close(bits(o["h"]), h_ref, "chunked h")
+    N.moe_expert_down(shape, to_bf16_dev(h_ref), i32_dev(offsets), g["w2"], None, o["y_perm"], None, ws)
+    assert N.moe_status_read(ws) == N.MOE_OK
+    assert_close(bits(o["y_perm"]), y_ref, "chunked y_perm")
+
+
 @pytest.mark.parametrize("name", ["count_first", "deepseek", "large"])
 def test_expert_up_sampled_rows_full_size(name):
     """Full-size up projection (the bench's launch configuration) checked on
