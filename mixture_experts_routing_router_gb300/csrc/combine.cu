@@ -31,6 +31,8 @@ __global__ void __launch_bounds__(256)
 combine_kernel(int T, int HV, int k, const uint4* __restrict__ y_perm, const int32_t* __restrict__ dest,
                const float* __restrict__ w, const uint4* __restrict__ y_shared, const uint4* residual,
                uint4* out) {   // out may alias residual: each 16-byte group is read, then written, by one thread
+    pdl_wait();
+    pdl_trigger();
     __shared__ int dsh[32];
     __shared__ float wsh[32];
     const long long R = (long long)T * k;
@@ -81,11 +83,13 @@ cudaError_t launch_combine(const moe_shape& s, const uint16_t* y_perm, const int
     long long blocks = s.tokens;
     const long long cap = (long long)device_sm_count() * (2048 / threads);
     if (blocks > cap) blocks = cap;
-    combine_kernel<<<(unsigned)blocks, threads, 0, st>>>(s.tokens, HV, s.top_k, reinterpret_cast<const uint4*>(y_perm),
-                                                         dest, w, reinterpret_cast<const uint4*>(y_shared),
-                                                         reinterpret_cast<const uint4*>(residual),
-                                                         reinterpret_cast<uint4*>(out));
-    return cudaGetLastError();
+    // Launched early (programmatic dependency) only for small layers: there it
+    // hides the launch behind the down projection's tail; behind a long GEMM
+    // its waiting blocks measured ~1 % slower on the 16384-token layer.
+    const bool pdl = kUsePdl && s.tokens <= kDecodeRows;
+    return launch_kernel(combine_kernel, dim3((unsigned)blocks), dim3(threads), 0, st, 1, pdl, s.tokens, HV,
+                         s.top_k, reinterpret_cast<const uint4*>(y_perm), dest, w, reinterpret_cast<const uint4*>(y_shared),
+                         reinterpret_cast<const uint4*>(residual), reinterpret_cast<uint4*>(out));
 }
 
 }  // namespace moe

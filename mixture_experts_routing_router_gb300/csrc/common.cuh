@@ -5,6 +5,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
@@ -142,6 +143,18 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
         }
     }
 }
+
+// ---- programmatic dependent launch ----------------------------------------------
+// Every kernel of the library runs: a prologue that touches no memory another
+// kernel writes (barrier init, TMEM allocation, descriptor prefetch), then
+// pdl_wait() -- which returns once the preceding kernel in the stream has
+// completed and its writes are visible -- then pdl_trigger(), which lets the
+// next kernel's CTAs start their own prologue as SMs free up.  No kernel
+// triggers before its wait returns, so when a kernel passes its wait every
+// earlier kernel of the stream has completed.  Without a programmatic
+// dependency (or launched plainly) both are no-ops.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // ---- TMA --------------------------------------------------------------------
 // 2-D tiled bulk tensor load global -> shared, completion counted on `bar`.
@@ -304,6 +317,37 @@ cudaError_t launch_scatter(const moe_shape& s, const uint16_t* x, const int32_t*
 cudaError_t launch_combine(const moe_shape& s, const uint16_t* y_perm, const int32_t* dest,
                            const float* w, const uint16_t* y_shared, const uint16_t* residual, uint16_t* out,
                            cudaStream_t st);
+
+// Launch with programmatic stream serialization (the kernel may start while
+// the preceding kernel of the stream finishes; it waits in pdl_wait), and an
+// optional cluster of `cluster_x` CTAs.
+constexpr bool kUsePdl = true;
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                          unsigned cluster_x, bool pdl, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    unsigned n = 0;
+    if (pdl) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    if (cluster_x > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = cluster_x;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Grouped GEMM problem (one launch): for every group g and row r of the group,
 // out[row0(g) + r, g*out_group_col + n] = epilogue( sum_seg sum_k A[row0(g)+r, seg*a_seg_col + k]

@@ -37,6 +37,17 @@ __device__ __forceinline__ unsigned lanemask_lt() {
     return m;
 }
 
+// Fresh look-back state for a dispatch: flags "not ready", tile counter 0 (a
+// kernel rather than memsets, so the layer stays one chain of kernels).
+__global__ void __launch_bounds__(256)
+clear_lookback_kernel(unsigned long long* flags, long long n, WsHeader* hdr) {
+    pdl_wait();
+    pdl_trigger();
+    const long long i0 = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    for (long long i = i0; i < n; i += (long long)gridDim.x * blockDim.x) flags[i] = 0ull;
+    if (i0 == 0) hdr->tile_counter = 0u;
+}
+
 __global__ void __launch_bounds__(kCountThreads)
 count_kernel(long long R, int k, int E, int capacity, const int32_t* __restrict__ ids,
              int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ rank,
@@ -49,7 +60,10 @@ count_kernel(long long R, int k, int E, int capacity, const int32_t* __restrict_
     constexpr int kItems = kCountChunk / kCountThreads;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
-    if (tid == 0) tile_s = atomicAdd(&hdr->tile_counter, 1u);
+    pdl_wait();
+    pdl_trigger();
+    // one tile: no look-back, so neither the counter nor the flags are read
+    if (tid == 0) tile_s = ntiles == 1 ? 0u : atomicAdd(&hdr->tile_counter, 1u);
     for (int e = tid; e < E; e += kCountThreads) hist[e] = 0;
     __syncthreads();
     const unsigned tile = tile_s;
@@ -173,6 +187,8 @@ scatter_kernel(int T, int HV, int k, int E, const uint4* __restrict__ x, const i
                const int32_t* __restrict__ offsets, const int32_t* __restrict__ rank,
                int32_t* __restrict__ dest, int32_t* __restrict__ sorted_pair, uint4* __restrict__ x_perm,
                const WsHeader* hdr) {
+    pdl_wait();
+    pdl_trigger();
     if (hdr->cap_exceeded) return;                 // over capacity: no payload moves
     __shared__ int dsh[32];
     const long long R = (long long)T * k;
@@ -227,15 +243,19 @@ cudaError_t launch_count(const moe_shape& s, const int32_t* ids, int32_t* counts
                          int32_t* rank, unsigned long long* flags, int count_tiles, WsHeader* hdr,
                          cudaStream_t st) {
     const long long R = (long long)s.tokens * s.top_k;
-    // fresh look-back state: flags "not ready", tile counter 0
-    cudaError_t err = cudaMemsetAsync(flags, 0, (size_t)count_tiles * s.experts * 8, st);
-    if (err != cudaSuccess) return err;
-    err = cudaMemsetAsync(&hdr->tile_counter, 0, sizeof(unsigned), st);
-    if (err != cudaSuccess) return err;
+    // fresh look-back state: flags "not ready", tile counter 0 (a single tile
+    // reads neither)
+    if (count_tiles > 1) {
+        const long long nflags = (long long)count_tiles * s.experts;
+        long long cblocks = (nflags + 255) / 256;
+        if (cblocks > device_sm_count()) cblocks = device_sm_count();
+        const cudaError_t err = launch_kernel(clear_lookback_kernel, dim3((unsigned)cblocks), dim3(256), 0, st, 1,
+                                              kUsePdl, flags, nflags, hdr);
+        if (err != cudaSuccess) return err;
+    }
     const size_t smem = (size_t)2 * s.experts * sizeof(int);
-    count_kernel<<<count_tiles, kCountThreads, smem, st>>>(R, s.top_k, s.experts, s.capacity, ids, counts,
-                                                           offsets, rank, flags, count_tiles, hdr);
-    return cudaGetLastError();
+    return launch_kernel(count_kernel, dim3((unsigned)count_tiles), dim3(kCountThreads), smem, st, 1, kUsePdl, R,
+                         s.top_k, s.experts, s.capacity, ids, counts, offsets, rank, flags, count_tiles, hdr);
 }
 
 cudaError_t launch_scatter(const moe_shape& s, const uint16_t* x, const int32_t* ids, const int32_t* offsets,
@@ -246,10 +266,9 @@ cudaError_t launch_scatter(const moe_shape& s, const uint16_t* x, const int32_t*
     long long blocks = s.tokens;
     const long long cap = (long long)device_sm_count() * (2048 / threads);
     if (blocks > cap) blocks = cap;
-    scatter_kernel<<<(unsigned)blocks, threads, 0, st>>>(s.tokens, HV, s.top_k, s.experts,
-                                                         reinterpret_cast<const uint4*>(x), ids, offsets, rank,
-                                                         dest, sorted_pair, reinterpret_cast<uint4*>(x_perm), hdr);
-    return cudaGetLastError();
+    return launch_kernel(scatter_kernel, dim3((unsigned)blocks), dim3(threads), 0, st, 1, kUsePdl, s.tokens, HV,
+                         s.top_k, s.experts, reinterpret_cast<const uint4*>(x), ids, offsets, rank, dest, sorted_pair,
+                         reinterpret_cast<uint4*>(x_perm), static_cast<const WsHeader*>(hdr));
 }
 
 }  // namespace moe

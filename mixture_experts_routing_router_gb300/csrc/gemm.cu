@@ -279,6 +279,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         tmem_alloc(smem_u32(&ctl->tmem_base), TMEM_COLS);
         tmem_relinquish();
     }
+    pdl_wait();
+    pdl_trigger();
     // Group rows.  Each bucket is clamped to [0, a_rows] on its own, so even
     // malformed offsets keep every row access inside A and the output.
     for (int g = tid; g < p.groups; g += C::THREADS) {
@@ -538,6 +540,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
         tmem_alloc_pair(smem_u32(&ctl->tmem_base), TMEM_COLS);
         tmem_relinquish_pair();
     }
+    pdl_wait();
+    pdl_trigger();
     for (int g = tid; g < p.groups; g += P_THREADS) {
         if (p.offsets) {
             int lo = p.offsets[g], hi = p.offsets[g + 1];
@@ -836,8 +840,8 @@ cudaError_t launch_mode(const CUtensorMap& ma, const CUtensorMap& mb, const KPar
         set_error("cudaFuncSetAttribute(max dynamic smem %d): %s", MAX_DYN_SMEM, cudaGetErrorString(attr_err));
         return attr_err;
     }
-    grouped_gemm_kernel<MODE, HALVES><<<device_sm_count(), Cfg<HALVES>::THREADS, smem, st>>>(ma, mb, kp);
-    const cudaError_t e = cudaGetLastError();
+    const cudaError_t e = launch_kernel(grouped_gemm_kernel<MODE, HALVES>, dim3((unsigned)device_sm_count()),
+                                        dim3(Cfg<HALVES>::THREADS), smem, st, 1, kUsePdl, ma, mb, kp);
     if (e != cudaSuccess) set_error("grouped GEMM launch (smem %zu): %s", smem, cudaGetErrorString(e));
     return e;
 }
@@ -855,19 +859,8 @@ cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const KPar
         set_error("cudaFuncSetAttribute(max dynamic smem %d): %s", MAX_DYN_SMEM, cudaGetErrorString(attr_err));
         return attr_err;
     }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(device_sm_count() & ~1), 1, 1);
-    cfg.blockDim = dim3(P_THREADS, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel<MODE>, ma, mb, kp);
+    const cudaError_t e = launch_kernel(grouped_gemm_pair_kernel<MODE>, dim3((unsigned)(device_sm_count() & ~1)),
+                                        dim3(P_THREADS), smem, st, 2, kUsePdl, ma, mb, kp);
     if (e != cudaSuccess) set_error("grouped GEMM pair launch (smem %zu): %s", smem, cudaGetErrorString(e));
     return e;
 }

@@ -89,6 +89,30 @@ decode_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
+    // ---- set-up: barriers, TMEM ----------------------------------------------
+    if (tid == 0) {
+        for (int s = 0; s < p.stages; ++s) {
+            mbar_init(smem_u32(&ctl->full[s]), 1);
+            mbar_init(smem_u32(&ctl->empty[s]), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(smem_u32(&ctl->tfull[a]), 1);
+            mbar_init(smem_u32(&ctl->tempty[a]), 4);        // the 4 epilogue warps
+        }
+        mbar_init(smem_u32(&ctl->drain), 1);
+        ctl->abort = 0;
+        fence_mbar_init();
+        fence_proxy_async_smem();
+        tma_prefetch_desc(&tmX);
+        tma_prefetch_desc(&tmW);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&ctl->tmem_base), p.tmem_cols);
+        tmem_relinquish();
+    }
+    pdl_wait();
+    pdl_trigger();
+
     // ---- the non-empty groups (block-wide compaction of the offsets) --------
     if (p.offsets) {
         const int per = (p.groups + DTHREADS - 1) / DTHREADS;
@@ -130,27 +154,6 @@ decode_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
         if (tid == 0) ctl->ng = p.groups;
     }
 
-    // ---- set-up: barriers, TMEM ----------------------------------------------
-    if (tid == 0) {
-        for (int s = 0; s < p.stages; ++s) {
-            mbar_init(smem_u32(&ctl->full[s]), 1);
-            mbar_init(smem_u32(&ctl->empty[s]), 1);
-        }
-        for (int a = 0; a < 2; ++a) {
-            mbar_init(smem_u32(&ctl->tfull[a]), 1);
-            mbar_init(smem_u32(&ctl->tempty[a]), 4);        // the 4 epilogue warps
-        }
-        mbar_init(smem_u32(&ctl->drain), 1);
-        ctl->abort = 0;
-        fence_mbar_init();
-        fence_proxy_async_smem();
-        tma_prefetch_desc(&tmX);
-        tma_prefetch_desc(&tmW);
-    }
-    if (warp == 1) {
-        tmem_alloc(smem_u32(&ctl->tmem_base), p.tmem_cols);
-        tmem_relinquish();
-    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -320,8 +323,8 @@ cudaError_t launch_d(const CUtensorMap& mx, const CUtensorMap& mw, const DParams
         set_error("cudaFuncSetAttribute(decode GEMM, %d bytes): %s", MAX_DSMEM, cudaGetErrorString(attr_err));
         return attr_err;
     }
-    decode_gemm_kernel<MODE><<<grid, DTHREADS, smem, st>>>(mx, mw, dp);
-    const cudaError_t e = cudaGetLastError();
+    const cudaError_t e =
+        launch_kernel(decode_gemm_kernel<MODE>, dim3(grid), dim3(DTHREADS), smem, st, 1, kUsePdl, mx, mw, dp);
     if (e != cudaSuccess) set_error("decode GEMM launch: %s", cudaGetErrorString(e));
     return e;
 }

@@ -28,6 +28,8 @@ template <int EPL>
 __global__ void __launch_bounds__(256)
 route_kernel(int T, int E, int k, const float* __restrict__ logits, int32_t* __restrict__ ids,
              float* __restrict__ w, WsHeader* hdr) {
+    pdl_wait();
+    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int gwarp = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
     const int nwarps = (int)((gridDim.x * blockDim.x) >> 5);
@@ -90,6 +92,8 @@ template <int EPL>
 __global__ void __launch_bounds__(256)
 route_sigmoid_kernel(int T, int E, int k, const float* __restrict__ logits, const float* __restrict__ bias,
                      float route_scale, int32_t* __restrict__ ids, float* __restrict__ w, WsHeader* hdr) {
+    pdl_wait();
+    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int gwarp = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
     const int nwarps = (int)((gridDim.x * blockDim.x) >> 5);
@@ -155,9 +159,8 @@ cudaError_t launch_sigmoid_epl(const moe_shape& s, const float* logits, const fl
     long long blocks = ((long long)s.tokens + warps_per_block - 1) / warps_per_block;
     const long long cap = (long long)device_sm_count() * 8;
     if (blocks > cap) blocks = cap;
-    route_sigmoid_kernel<EPL><<<(unsigned)blocks, 32 * warps_per_block, 0, st>>>(s.tokens, s.experts, s.top_k,
-                                                                                  logits, bias, scale, ids, w, hdr);
-    return cudaGetLastError();
+    return launch_kernel(route_sigmoid_kernel<EPL>, dim3((unsigned)blocks), dim3(32 * warps_per_block), 0, st, 1,
+                         kUsePdl, s.tokens, s.experts, s.top_k, logits, bias, scale, ids, w, hdr);
 }
 
 template <int EPL>
@@ -167,9 +170,8 @@ cudaError_t launch_epl(const moe_shape& s, const float* logits, int32_t* ids, fl
     long long blocks = ((long long)s.tokens + warps_per_block - 1) / warps_per_block;
     const long long cap = (long long)device_sm_count() * 8;
     if (blocks > cap) blocks = cap;
-    route_kernel<EPL><<<(unsigned)blocks, 32 * warps_per_block, 0, st>>>(s.tokens, s.experts, s.top_k,
-                                                                          logits, ids, w, hdr);
-    return cudaGetLastError();
+    return launch_kernel(route_kernel<EPL>, dim3((unsigned)blocks), dim3(32 * warps_per_block), 0, st, 1,
+                         kUsePdl, s.tokens, s.experts, s.top_k, logits, ids, w, hdr);
 }
 
 }  // namespace
