@@ -92,6 +92,12 @@ def _load():
             lib.oracle_combine.argtypes = [i, i, i, P, P, P, P, P, P]
             lib.oracle_layer.restype = i
             lib.oracle_layer.argtypes = [i] * 9 + [P] * 20
+            lib.oracle_fp8_e4m3_decode.restype = None
+            lib.oracle_fp8_e4m3_decode.argtypes = [i, P, P]
+            lib.oracle_expert_ffn_fp8.restype = None
+            lib.oracle_expert_ffn_fp8.argtypes = [i, i, i, i] + [P] * 8
+            lib.oracle_layer_fp8.restype = i
+            lib.oracle_layer_fp8.argtypes = [i] * 7 + [P] * 19
             _lib = lib
     return _lib
 
@@ -274,5 +280,60 @@ def layer(x, w13, w2, act, k, capacity, logits=None, ids_in=None, w_in=None,
                               _p(o["counts"]), _p(o["offsets"]), _p(o["dest"]), _p(o["sorted_pair"]),
                               _p(o["x_perm"]), _p(o["h"]), _p(o["y_perm"]), _p(o["h_shared"]),
                               _p(o["y_shared"]), _p(o["out"]))
+    o["status"] = st
+    return o
+
+
+# ---- FP8 E4M3 expert weights ----------------------------------------------
+def fp8_e4m3_decode(codes):
+    """E4M3 codes (uint8) -> float64 values (NaN for the two NaN codes)."""
+    c = _c(codes, np.uint8)
+    out = np.zeros(c.shape, np.float64)
+    _load().oracle_fp8_e4m3_decode(int(c.size), _p(c), _p(out))
+    return out
+
+
+def expert_ffn_fp8(x_perm, offsets, w13, s13, w2, s2, act):
+    """Routed experts with FP8 E4M3 weights and one FP32 scale per weight row:
+    w13 uint8 [E, up, H], s13 float32 [E, up], w2 uint8 [E, H, I], s2 float32 [E, H].
+    -> (h [R, I], y_perm [R, H]) as BF16 bits."""
+    x_perm = _c(x_perm, np.uint16)
+    offsets = _c(offsets, np.int32)
+    w13 = _c(w13, np.uint8)
+    w2 = _c(w2, np.uint8)
+    s13 = _c(s13, np.float32)
+    s2 = _c(s2, np.float32)
+    E, H, I = w2.shape
+    R = x_perm.shape[0]
+    h = np.zeros((R, I), np.uint16)
+    y = np.zeros((R, H), np.uint16)
+    _load().oracle_expert_ffn_fp8(H, E, I, act, _p(x_perm), _p(offsets), _p(w13), _p(s13), _p(w2), _p(s2),
+                                  _p(h), _p(y))
+    return h, y
+
+
+def layer_fp8(x, w13, s13, w2, s2, act, k, capacity, logits=None, ids_in=None, w_in=None, residual=None):
+    """The whole layer with FP8 E4M3 expert weights (no shared experts)."""
+    x = _c(x, np.uint16)
+    w13 = _c(w13, np.uint8)
+    w2 = _c(w2, np.uint8)
+    s13 = _c(s13, np.float32)
+    s2 = _c(s2, np.float32)
+    T, H = x.shape
+    E, _, I = w2.shape
+    R = T * k
+    o = dict(ids=np.zeros((T, k), np.int32), w=np.zeros((T, k), np.float32),
+             counts=np.zeros(E, np.int32), offsets=np.zeros(E + 1, np.int32),
+             dest=np.full(R, -7, np.int32), sorted_pair=np.full(R, -7, np.int32),
+             x_perm=np.zeros((R, H), np.uint16), h=np.zeros((R, I), np.uint16),
+             y_perm=np.zeros((R, H), np.uint16), out=np.zeros((T, H), np.uint16))
+    lg = None if logits is None else _c(logits, np.float32)
+    ii = None if ids_in is None else _c(ids_in, np.int32)
+    wi = None if w_in is None else _c(w_in, np.float32)
+    res = None if residual is None else _c(residual, np.uint16)
+    st = _load().oracle_layer_fp8(T, H, E, k, I, act, capacity, _p(lg), _p(ii), _p(wi), _p(x), _p(w13), _p(s13),
+                                  _p(w2), _p(s2), _p(res), _p(o["ids"]), _p(o["w"]), _p(o["counts"]),
+                                  _p(o["offsets"]), _p(o["dest"]), _p(o["sorted_pair"]), _p(o["x_perm"]),
+                                  _p(o["h"]), _p(o["y_perm"]), _p(o["out"]))
     o["status"] = st
     return o

@@ -35,6 +35,13 @@ MUTANTS = {
                                         "(double)route_scale * (double)key[order[j]] / z"),
     "gate_transposed": ("bf16_to_double(wg[(size_t)e * H + h])", "bf16_to_double(wg[(size_t)h * E + e])"),
     "residual_dropped": ("if (residual_t) s += bf16_to_double(residual_t[c]);", "if (residual_t) s += 0.0;"),
+    "fp8_gate_and_up_swapped": ("h_row[n] = double_to_bf16(silu(gate) * upv);",
+                                "h_row[n] = double_to_bf16(silu(upv) * gate);"),
+    "fp8_exponent_bias_8": ("std::ldexp(1.0 + m / 8.0, e - 7)", "std::ldexp(1.0 + m / 8.0, e - 8)"),
+    "fp8_subnormals_read_as_normals": ("(e == 0) ? std::ldexp((double)m, -9)", "(e == 0) ? std::ldexp(1.0 + m / 8.0, -7)"),
+    "fp8_nan_code_finite": ("if (e == 15 && m == 7) return std::nan(\"\");", "if (false) return std::nan(\"\");"),
+    "fp8_up_scale_from_first_row": ("return acc * (double)s13_e[wr];", "return acc * (double)s13_e[0];"),
+    "fp8_down_scale_from_first_row": ("double_to_bf16(acc * (double)s2_e[c])", "double_to_bf16(acc * (double)s2_e[0])"),
     "first_slot_dropped_in_combine": ("for (int j = 0; j < k; ++j) {\n            if (dest_t[j] < 0) continue;",
                                       "for (int j = 1; j < k; ++j) {\n            if (dest_t[j] < 0) continue;"),
 }
@@ -65,6 +72,11 @@ PINS = [
     (P.test_route_sigmoid_negative_bias_excludes_the_top_experts, {}),
     (P.test_route_sigmoid_closed_form_weights, {}),
     (P.test_gate_projection_matches_float64_matmul, {}),
+    (P.test_fp8_decode_closed_forms, {}),
+    (P.test_fp8_decode_matches_torch, {}),
+    (P.test_fp8_ffn_equals_bf16_path_on_exact_weights, dict(act=0)),
+    (P.test_fp8_ffn_equals_bf16_path_on_exact_weights, dict(act=1)),
+    (P.test_fp8_layer_equals_bf16_layer_on_exact_weights, {}),
 ]
 
 

@@ -485,3 +485,75 @@ def test_gate_projection_matches_float64_matmul(oracle_mod):
     # transposing the weight matrix is caught
     assert not np.allclose(oracle_mod.gate(x[:, :E], rand_bf16(rng, (E, E))),
                            oracle_mod.gate(x[:, :E], rand_bf16(rng, (E, E))))
+
+
+# --------------------------------------------------------------------------
+# FP8 E4M3 expert weights (one FP32 scale per weight row)
+# --------------------------------------------------------------------------
+def test_fp8_decode_closed_forms(oracle_mod):
+    """OCP E4M3: bias 7, 3 mantissa bits, subnormals at exponent 0, no
+    infinities, NaN only at S.1111.111."""
+    v = oracle_mod.fp8_e4m3_decode(np.arange(256, dtype=np.uint8))
+    assert v[0x00] == 0.0 and math.copysign(1.0, v[0x00]) > 0
+    assert v[0x80] == 0.0 and math.copysign(1.0, v[0x80]) < 0
+    assert v[0x01] == 2.0 ** -9 and v[0x07] == 7 * 2.0 ** -9        # subnormals
+    assert v[0x08] == 2.0 ** -6                                      # smallest normal
+    assert v[0x38] == 1.0 and v[0x3C] == 1.5 and v[0x40] == 2.0 and v[0x41] == 2.25
+    assert v[0x7E] == 448.0                                          # largest finite
+    nan = np.isnan(v)
+    assert nan.sum() == 2 and nan[0x7F] and nan[0xFF]
+    assert np.all(np.diff(v[:0x7F]) > 0)                             # monotone over the positive codes
+    assert np.array_equal(v[0x80:0xFF], -v[:0x7F])
+
+
+def test_fp8_decode_matches_torch(oracle_mod):
+    """torch's float8_e4m3fn conversion is an independent implementation."""
+    t = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    v = oracle_mod.fp8_e4m3_decode(np.arange(256, dtype=np.uint8))
+    assert np.array_equal(np.isnan(t), np.isnan(v))
+    ok = ~np.isnan(v)
+    assert np.array_equal(t[ok], v[ok])
+
+
+def fp8_exact_case(rng, E, up, H, I):
+    """FP8 codes and power-of-two row scales: every dequantized weight
+    decode(code) * scale is exact in BF16, so the BF16 path of the oracle on
+    those values is an independent statement of the same sums."""
+    c13 = (torch.from_numpy(rng.standard_normal((E, up, H)).astype(np.float32)) * 0.6).to(
+        torch.float8_e4m3fn).view(torch.uint8).numpy()
+    c2 = (torch.from_numpy(rng.standard_normal((E, H, I)).astype(np.float32)) * 0.6).to(
+        torch.float8_e4m3fn).view(torch.uint8).numpy()
+    s13 = (2.0 ** rng.integers(-3, 4, (E, up))).astype(np.float32)
+    s2 = (2.0 ** rng.integers(-3, 4, (E, H))).astype(np.float32)
+    w13 = bf16_of_exact(torch.tensor(c13).view(torch.float8_e4m3fn).to(torch.float64).numpy() * s13[:, :, None])
+    w2 = bf16_of_exact(torch.tensor(c2).view(torch.float8_e4m3fn).to(torch.float64).numpy() * s2[:, :, None])
+    return c13, s13, c2, s2, w13, w2
+
+
+@pytest.mark.parametrize("act", [0, 1])
+def test_fp8_ffn_equals_bf16_path_on_exact_weights(oracle_mod, act):
+    rng = np.random.default_rng(31 + act)
+    E, H, I, R = 3, 48, 40, 30
+    up = 2 * I if act == 0 else I
+    c13, s13, c2, s2, w13, w2 = fp8_exact_case(rng, E, up, H, I)
+    x_perm = rand_bf16(rng, (R, H))
+    offsets = np.array([0, 7, 7, R], np.int32)
+    h8, y8 = oracle_mod.expert_ffn_fp8(x_perm, offsets, c13, s13, c2, s2, act)
+    hb, yb, _, _ = oracle_mod.expert_ffn(x_perm, offsets, w13, w2, act)
+    assert np.array_equal(h8, hb)
+    assert np.array_equal(y8, yb)
+    assert np.mean(h8 != 0) > 0.3                                    # not trivially zero
+
+
+def test_fp8_layer_equals_bf16_layer_on_exact_weights(oracle_mod):
+    rng = np.random.default_rng(41)
+    T, E, k, H, I = 24, 6, 2, 32, 48
+    c13, s13, c2, s2, w13, w2 = fp8_exact_case(rng, E, 2 * I, H, I)
+    x = rand_bf16(rng, (T, H))
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    res = rand_bf16(rng, (T, H))
+    o8 = oracle_mod.layer_fp8(x, c13, s13, c2, s2, 0, k, T, logits=logits, residual=res)
+    ob = oracle_mod.layer(x, w13, w2, 0, k, T, logits=logits, residual=res)
+    assert o8["status"] == ob["status"] == 0
+    for key in ("ids", "offsets", "dest", "x_perm", "h", "y_perm", "out"):
+        assert np.array_equal(o8[key], ob[key]), key
