@@ -208,6 +208,38 @@ MOE_API moe_status moe_layer(const moe_shape* shape, const float* logits, const 
                              const uint16_t* residual, uint16_t* out, void* ws, size_t ws_bytes,
                              void* stream);
 
+/* Quantized expert weights: FP8 E4M3 (ONNX Runtime PR #33963: weight-only
+ * quantized FC1/FC2 experts with BF16 activations, BF16 store boundaries and
+ * FP32 accumulation; the codec here is FP8 E4M3 -- the afdEP-comm record's
+ * fp8 payload type -- in place of the page's IQ2_XXS).
+ *   w13       device u8  [E, up, H]  E4M3 codes (OCP: bias 7, no infinities,
+ *                                    S.1111.111 is NaN); row layout as moe_expert_up
+ *   w13_scale device f32 [E, up]     one scale per weight row
+ *   w2        device u8  [E, H, I]   E4M3 codes; w2_scale device f32 [E, H]
+ * A weight is decode(code) * scale of its row; the kernels decode the codes to
+ * BF16 in shared memory (exactly), multiply in BF16 with FP32 accumulation and
+ * apply the row scale to the accumulator:
+ *   SwiGLU: h[r][n] = bf16( silu(g) * u ), g = (x_r . dec(W13[e][n])) * s13[e][n],
+ *           u = (x_r . dec(W13[e][I+n])) * s13[e][I+n];  ReLU^2 likewise with one row;
+ *   y_perm[r][c] = bf16( (h_r . dec(W2[e][c])) * s2[e][c] ).
+ * Host errors: MOE_ERR_UNSUPPORTED when shape->shared > 0 (no shared experts
+ * here); MOE_ERR_INVALID_ARG when hidden or inter is not a multiple of 16 or a
+ * pointer is not 16-byte aligned.  The other arguments, the workspace and the
+ * device errors are those of moe_expert_up / moe_expert_down / moe_layer.
+ * These run on the small-row kernel at any size: efficient when groups hold
+ * up to 64 rows (decode); larger groups are taken in 64-row chunks. */
+MOE_API moe_status moe_expert_up_fp8(const moe_shape* shape, const uint16_t* x_perm, const int32_t* offsets,
+                                     const uint8_t* w13, const float* w13_scale, uint16_t* h, void* ws,
+                                     size_t ws_bytes, void* stream);
+MOE_API moe_status moe_expert_down_fp8(const moe_shape* shape, const uint16_t* h, const int32_t* offsets,
+                                       const uint8_t* w2, const float* w2_scale, uint16_t* y_perm, void* ws,
+                                       size_t ws_bytes, void* stream);
+MOE_API moe_status moe_layer_fp8(const moe_shape* shape, const float* logits, const int32_t* ids_in,
+                                 const float* w_in, const uint16_t* x, const uint8_t* w13,
+                                 const float* w13_scale, const uint8_t* w2, const float* w2_scale,
+                                 const uint16_t* residual, uint16_t* out, void* ws, size_t ws_bytes,
+                                 void* stream);
+
 /* moe_dispatch for callers that cannot allocate device memory, and so cannot
  * provide the workspace the other calls take: code that runs where cudaMalloc
  * is not allowed or not safe (while a CUDA graph is being captured, inside a

@@ -155,6 +155,53 @@ moe_status do_down(const moe_shape& s, const uint16_t* h, const int32_t* offsets
     return launch_grouped_gemm(q, hdr, st);
 }
 
+// FP8 E4M3 expert weights (no shared experts): one FP32 scale per weight row.
+moe_status do_up_fp8(const moe_shape& s, const uint16_t* x_perm, const int32_t* offsets, const uint8_t* w13,
+                     const float* s13, uint16_t* h, void* ws, cudaStream_t st) {
+    const long long R = (long long)s.tokens * s.top_k;
+    GemmProblem g{};
+    g.mode = s.act == MOE_ACT_SWIGLU ? kGemmSwiGLU : kGemmReLU2;
+    g.a = x_perm; g.a_rows = R; g.a_cols = s.hidden;
+    g.b = w13; g.b_rows = (long long)s.experts * up_rows(s, s.inter); g.b_cols = s.hidden;
+    g.offsets = offsets; g.groups = s.experts; g.rows_all = 0;
+    g.K = s.hidden; g.nseg = 1; g.a_seg_col = 0; g.b_seg_row = 0;
+    g.N = s.inter; g.b_group_rows = up_rows(s, s.inter); g.up_off = s.inter;
+    g.out = h; g.ldo = s.inter; g.out_group_col = 0;
+    g.max_group_rows = s.tokens;
+    g.wfmt = kWeightFp8E4M3; g.wscale = s13;
+    return launch_grouped_gemm(g, at<WsHeader>(ws, 0), st);
+}
+
+moe_status do_down_fp8(const moe_shape& s, const uint16_t* h, const int32_t* offsets, const uint8_t* w2,
+                       const float* s2, uint16_t* y_perm, void* ws, cudaStream_t st) {
+    const long long R = (long long)s.tokens * s.top_k;
+    GemmProblem g{};
+    g.mode = kGemmPlain;
+    g.a = h; g.a_rows = R; g.a_cols = s.inter;
+    g.b = w2; g.b_rows = (long long)s.experts * s.hidden; g.b_cols = s.inter;
+    g.offsets = offsets; g.groups = s.experts; g.rows_all = 0;
+    g.K = s.inter; g.nseg = 1; g.a_seg_col = 0; g.b_seg_row = 0;
+    g.N = s.hidden; g.b_group_rows = s.hidden; g.up_off = 0;
+    g.out = y_perm; g.ldo = s.hidden; g.out_group_col = 0;
+    g.max_group_rows = s.tokens;
+    g.wfmt = kWeightFp8E4M3; g.wscale = s2;
+    return launch_grouped_gemm(g, at<WsHeader>(ws, 0), st);
+}
+
+// FP8 weight rows are TMA-loaded: their byte stride (H or I) must be a
+// multiple of 16; shared experts are not part of the FP8 entry points.
+moe_status check_fp8_shape(const moe_shape* s) {
+    if (s->shared > 0) {
+        set_error("FP8 expert weights: shared experts are not supported (shape.shared must be 0)");
+        return MOE_ERR_UNSUPPORTED;
+    }
+    if (s->hidden % 16 != 0 || s->inter % 16 != 0) {
+        set_error("FP8 expert weights: hidden and inter must be multiples of 16 (got %d, %d)", s->hidden, s->inter);
+        return MOE_ERR_INVALID_ARG;
+    }
+    return MOE_OK;
+}
+
 moe_status do_combine(const moe_shape& s, const uint16_t* y_perm, const int32_t* dest, const float* w,
                       const uint16_t* y_shared, const uint16_t* residual, uint16_t* out, cudaStream_t st) {
     return from_cuda(launch_combine(s, y_perm, dest, w, y_shared, residual, out, st));
@@ -326,6 +373,70 @@ moe_status moe_layer(const moe_shape* shape, const float* logits, const int32_t*
     if ((r = do_up(s, x_perm, offsets, w13, x, ws13, h, ws, st)) != MOE_OK) return r;
     if ((r = do_down(s, h, offsets, w2, ws2, y_perm, y_shared, ws, st)) != MOE_OK) return r;
     return do_combine(s, y_perm, dest, w, y_shared, residual, out, st);
+}
+
+moe_status moe_expert_up_fp8(const moe_shape* shape, const uint16_t* x_perm, const int32_t* offsets,
+                             const uint8_t* w13, const float* w13_scale, uint16_t* h, void* ws, size_t ws_bytes,
+                             void* stream) {
+    clear_error();
+    moe_status r = check_shape(shape);
+    if (r != MOE_OK) return r;
+    if ((r = check_fp8_shape(shape)) != MOE_OK) return r;
+    if ((r = check_ws(shape, ws, ws_bytes, false)) != MOE_OK) return r;
+    if (!aligned(x_perm, 16) || !aligned(offsets, 16) || !aligned(w13, 16) || !aligned(w13_scale, 16) ||
+        !aligned(h, 16))
+        return MOE_ERR_INVALID_ARG;
+    return do_up_fp8(*shape, x_perm, offsets, w13, w13_scale, h, ws, static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_expert_down_fp8(const moe_shape* shape, const uint16_t* h, const int32_t* offsets, const uint8_t* w2,
+                               const float* w2_scale, uint16_t* y_perm, void* ws, size_t ws_bytes, void* stream) {
+    clear_error();
+    moe_status r = check_shape(shape);
+    if (r != MOE_OK) return r;
+    if ((r = check_fp8_shape(shape)) != MOE_OK) return r;
+    if ((r = check_ws(shape, ws, ws_bytes, false)) != MOE_OK) return r;
+    if (!aligned(h, 16) || !aligned(offsets, 16) || !aligned(w2, 16) || !aligned(w2_scale, 16) || !aligned(y_perm, 16))
+        return MOE_ERR_INVALID_ARG;
+    return do_down_fp8(*shape, h, offsets, w2, w2_scale, y_perm, ws, static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_layer_fp8(const moe_shape* shape, const float* logits, const int32_t* ids_in, const float* w_in,
+                         const uint16_t* x, const uint8_t* w13, const float* w13_scale, const uint8_t* w2,
+                         const float* w2_scale, const uint16_t* residual, uint16_t* out, void* ws, size_t ws_bytes,
+                         void* stream) {
+    clear_error();
+    moe_status r = check_shape(shape);
+    if (r != MOE_OK) return r;
+    if ((r = check_fp8_shape(shape)) != MOE_OK) return r;
+    if ((r = check_ws(shape, ws, ws_bytes, true)) != MOE_OK) return r;
+    if (logits ? !aligned(logits, 16) : (!aligned(ids_in, 16) || !aligned(w_in, 16))) return MOE_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(w13, 16) || !aligned(w13_scale, 16) || !aligned(w2, 16) ||
+        !aligned(w2_scale, 16) || !aligned(out, 16) || !aligned_or_null(residual, 16))
+        return MOE_ERR_INVALID_ARG;
+    const moe_shape& s = *shape;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const WsLayout L = ws_layout(s);
+    const int32_t* ids = ids_in;
+    const float* w = w_in;
+    if (logits) {
+        int32_t* ids_ws = at<int32_t>(ws, L.ids);
+        float* w_ws = at<float>(ws, L.w);
+        if ((r = do_route(s, logits, ids_ws, w_ws, ws, st)) != MOE_OK) return r;
+        ids = ids_ws;
+        w = w_ws;
+    }
+    int32_t* offsets = at<int32_t>(ws, L.offsets);
+    int32_t* dest = at<int32_t>(ws, L.dest);
+    uint16_t* x_perm = at<uint16_t>(ws, L.x_perm);
+    uint16_t* h = at<uint16_t>(ws, L.h);
+    uint16_t* y_perm = at<uint16_t>(ws, L.y_perm);
+    if ((r = do_dispatch(s, x, ids, at<int32_t>(ws, L.counts), offsets, dest, at<int32_t>(ws, L.sorted_pair), x_perm,
+                         ws, st)) != MOE_OK)
+        return r;
+    if ((r = do_up_fp8(s, x_perm, offsets, w13, w13_scale, h, ws, st)) != MOE_OK) return r;
+    if ((r = do_down_fp8(s, h, offsets, w2, w2_scale, y_perm, ws, st)) != MOE_OK) return r;
+    return do_combine(s, y_perm, dest, w, nullptr, residual, out, st);
 }
 
 moe_status moe_status_read(void* ws, void* stream, moe_status* device_status) {

@@ -367,7 +367,11 @@ struct GemmProblem {
     int up_off;                                           // SwiGLU: rows from gate to up half
     void* out; long long ldo; int out_group_col;
     int max_group_rows;                                   // host bound on rows per group (0: a_rows)
+    int wfmt;                                             // kWeightBf16 or kWeightFp8E4M3 (B's format)
+    const float* wscale;                                  // FP8: FP32 scale per B row
 };
+constexpr int kWeightBf16 = 0;
+constexpr int kWeightFp8E4M3 = 1;
 // Returns MOE_OK, MOE_ERR_CUDA (tensor map / launch) or MOE_ERR_UNSUPPORTED.
 // Problems whose groups hold at most kDecodeRows rows and whose work fits in
 // about two waves run the small-row kernel (launch_decode_gemm); the rest the
@@ -382,6 +386,10 @@ moe_status launch_decode_gemm(const GemmProblem& p, int nb, WsHeader* hdr, cudaS
 // Tensor map of a row-major [rows, cols] BF16 matrix, 128-byte swizzle, boxes
 // of 64 columns x box_rows rows (records the failure for moe_last_error_message).
 bool make_tensor_map_bf16(CUtensorMap* m, const void* base, long long rows, long long cols, unsigned box_rows);
+// Tensor map of a row-major [rows, cols] byte matrix (FP8 codes), no swizzle,
+// boxes of box_cols bytes x box_rows rows.
+bool make_tensor_map_u8_rows(CUtensorMap* m, const void* base, long long rows, long long cols, unsigned box_cols,
+                             unsigned box_rows);
 
 int device_sm_count();
 

@@ -882,6 +882,28 @@ bool make_tensor_map_bf16(CUtensorMap* m, const void* base, long long rows, long
     return make_map(m, base, rows, cols, box_rows);
 }
 
+bool make_tensor_map_u8_rows(CUtensorMap* m, const void* base, long long rows, long long cols, unsigned box_cols,
+                             unsigned box_rows) {
+    auto enc = encode_fn();
+    if (!enc) {
+        set_error("cuTensorMapEncodeTiled is not available from the driver");
+        return false;
+    }
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols};
+    cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1u, 1u};
+    const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        set_error("cuTensorMapEncodeTiled failed (CUresult %d) for a [%lld, %lld] byte tensor at %p", (int)r, rows,
+                  cols, base);
+        return false;
+    }
+    return true;
+}
+
 moe_status launch_grouped_gemm(const GemmProblem& g, WsHeader* hdr, cudaStream_t st) {
     if (g.groups < 1 || g.groups > 1024 || g.K < 1 || g.N < 1) {
         set_error("grouped GEMM: unsupported problem (groups %d, K %d, N %d)", g.groups, g.K, g.N);
@@ -893,6 +915,16 @@ moe_status launch_grouped_gemm(const GemmProblem& g, WsHeader* hdr, cudaStream_t
     // starts sooner; with many more items the tile kernels' larger tiles
     // stream a few percent better (measured at 1 to 16 tokens over 240 experts).
     const long long row_bound = g.offsets ? (g.max_group_rows > 0 ? g.max_group_rows : g.a_rows) : g.rows_all;
+    if (g.wfmt == kWeightFp8E4M3) {
+        // FP8 weights are decoded by the small-row kernel at any size (groups of
+        // more than 64 rows are taken in 64-row chunks)
+        if (g.nseg != 1) {
+            set_error("grouped GEMM: FP8 weights take one K segment");
+            return MOE_ERR_UNSUPPORTED;
+        }
+        const int nb = row_bound >= kDecodeRows ? kDecodeRows : (row_bound < 16 ? 16 : (int)((row_bound + 15) / 16 * 16));
+        return launch_decode_gemm(g, nb, hdr, st);
+    }
     if (row_bound <= kDecodeRows) {
         const long long slots = g.offsets ? (g.a_rows < g.groups ? g.a_rows : g.groups) : g.groups;
         if (slots * ((g.N + 127) / 128) <= 2LL * device_sm_count())

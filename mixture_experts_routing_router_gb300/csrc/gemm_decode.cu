@@ -22,6 +22,15 @@
 // The epilogue arithmetic is the tile kernels': SwiGLU silu(g)*u, ReLU^2,
 // plain, or the FP32 accumulator.  Every wait is bounded (MOE_ERR_TIMEOUT,
 // TMEM freed, no trap).
+//
+// FP8 weights (FP8W): the weights arrive as OCP E4M3 codes with one FP32 scale
+// per weight row -- the ONNX Runtime operator's weight-only quantized experts
+// (BF16 activations), with E4M3 as the codec.  Every E4M3 value is exact in
+// BF16, so four more warps (6..9) convert each TMA-loaded FP8 box (128 rows x
+// 64 bytes, no swizzle) into the BF16 128-byte-swizzled K-major layout of a
+// separate ring of conversion slots, and the MMA stays BF16 with FP32
+// accumulation; the row scale multiplies the accumulator in the epilogue.
+// The FP8 stage holds the activation box first, then the FP8 weight box(es).
 #include "common.cuh"
 
 #include <mutex>
@@ -33,6 +42,9 @@ constexpr int DBM = 128;                   // weight rows per item (MMA M)
 constexpr int DBK = 64;                    // 64 BF16 = one 128-byte swizzle row
 constexpr int W_BYTES = DBM * DBK * 2;     // 16 KiB weight box
 constexpr int DTHREADS = 192;              // producer, MMA, 4 epilogue warps
+constexpr int DTHREADS_FP8 = 320;          // + 4 converter warps
+constexpr int W8_BYTES = DBM * DBK;        // 8 KiB FP8 weight box (128 rows x 64 codes)
+constexpr int MAX_CSLOTS = 4;
 constexpr int MAX_DSTAGES = 16;
 constexpr int MAX_DSMEM = 212 * 1024;
 
@@ -49,6 +61,13 @@ struct DParams {
     int nb;                     // activation rows per chunk (MMA N): 16, 32, 48 or 64
     int stages, stage_bytes;
     uint32_t tmem_cols;         // two accumulators of (SwiGLU ? 2 : 1) * nb columns, power of two
+    uint32_t x_off;             // activation box within a stage
+    uint32_t w_off;             // first weight box within a stage
+    // FP8 weights
+    const float* wscale;        // [weight rows] FP32 scale per weight row
+    uint32_t conv_off;          // conversion ring, from the aligned shared-memory base
+    uint32_t conv_slot_bytes;
+    int conv_slots;
 };
 
 template <int MODE> struct OutOfD { using T = __nv_bfloat16; };
@@ -59,12 +78,26 @@ struct DCtl {
     unsigned long long empty[MAX_DSTAGES];
     unsigned long long tfull[2];
     unsigned long long tempty[2];
+    unsigned long long cfull[MAX_CSLOTS];      // FP8: slot converted (4 converter warps)
+    unsigned long long cempty[MAX_CSLOTS];     // FP8: slot consumed by the MMA
     unsigned long long drain;
     uint32_t tmem_base;
     int abort;
     int ng;                     // non-empty groups
-    int wsum[DTHREADS / 32];
+    int wsum[DTHREADS_FP8 / 32];
 };
+
+// Two E4M3 codes (low byte first) -> two BF16 values (low half first), exact:
+// E4M3 -> FP16 in hardware, FP16 -> FP32 -> BF16 without rounding.
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two) {
+    uint32_t h2, b;
+    float lo, hi;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((unsigned short)two));
+    asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+        : "=f"(lo), "=f"(hi) : "r"(h2));
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(b) : "f"(hi), "f"(lo));
+    return b;
+}
 
 __device__ __forceinline__ void clamped_bounds(const DParams& p, int g, int& lo, int& hi) {
     lo = p.offsets[g];
@@ -73,15 +106,18 @@ __device__ __forceinline__ void clamped_bounds(const DParams& p, int g, int& lo,
     hi = hi < lo ? lo : (hi > p.a_rows ? p.a_rows : hi);
 }
 
-template <int MODE>
-__global__ void __launch_bounds__(DTHREADS, 1)
+template <int MODE, bool FP8W>
+__global__ void __launch_bounds__(FP8W ? DTHREADS_FP8 : DTHREADS, 1)
 decode_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                    const DParams p) {
     constexpr int NW = (MODE == kGemmSwiGLU) ? 2 : 1;      // weight boxes per stage
+    constexpr int NTH = FP8W ? DTHREADS_FP8 : DTHREADS;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + ((1024u - (raw_u32 & 1023u)) & 1023u);
-    DCtl* ctl = reinterpret_cast<DCtl*>(smem + p.stages * p.stage_bytes);
+    // [TMA stage ring][FP8 conversion ring][control block][group lists]
+    DCtl* ctl = reinterpret_cast<DCtl*>(smem + (size_t)p.stages * p.stage_bytes +
+                                        (size_t)p.conv_slots * p.conv_slot_bytes);
     int* gid = reinterpret_cast<int*>(ctl + 1);            // [groups] non-empty groups, in order
     int* gst = gid + p.groups;                              // first row
     int* gcnt = gst + p.groups;                             // rows
@@ -99,6 +135,11 @@ decode_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
             mbar_init(smem_u32(&ctl->tfull[a]), 1);
             mbar_init(smem_u32(&ctl->tempty[a]), 4);        // the 4 epilogue warps
         }
+        if (FP8W)
+            for (int c = 0; c < p.conv_slots; ++c) {
+                mbar_init(smem_u32(&ctl->cfull[c]), 4);     // the 4 converter warps
+                mbar_init(smem_u32(&ctl->cempty[c]), 1);
+            }
         mbar_init(smem_u32(&ctl->drain), 1);
         ctl->abort = 0;
         fence_mbar_init();
@@ -115,7 +156,7 @@ decode_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
 
     // ---- the non-empty groups (block-wide compaction of the offsets) --------
     if (p.offsets) {
-        const int per = (p.groups + DTHREADS - 1) / DTHREADS;
+        const int per = (p.groups + NTH - 1) / NTH;
         const int g0 = tid * per;
         int cnt = 0;
         for (int i = 0; i < per; ++i) {
@@ -136,7 +177,7 @@ decode_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
         __syncthreads();
         int k = inc - cnt;
         for (int w = 0; w < warp; ++w) k += ctl->wsum[w];
-        if (tid == DTHREADS - 1) ctl->ng = k + cnt;
+        if (tid == NTH - 1) ctl->ng = k + cnt;
         for (int i = 0; i < per; ++i) {
             const int g = g0 + i;
             if (g < p.groups) {
@@ -146,7 +187,7 @@ decode_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
             }
         }
     } else {
-        for (int g = tid; g < p.groups; g += DTHREADS) {
+        for (int g = tid; g < p.groups; g += NTH) {
             gid[g] = g;
             gst[g] = 0;
             gcnt[g] = p.rows_all < p.a_rows ? p.rows_all : p.a_rows;
@@ -165,7 +206,8 @@ decode_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
     const int nk = nkb * p.nseg;
     const int nb = p.nb;
     const uint32_t acc_cols = (uint32_t)(NW * nb);
-    const uint32_t x_off = (uint32_t)(NW * W_BYTES);
+    const uint32_t x_off = p.x_off, w_off = p.w_off;
+    const uint32_t w_box = FP8W ? (uint32_t)W8_BYTES : (uint32_t)W_BYTES;
 
     if (warp == 0) {
         // ---------------- TMA producer ----------------
@@ -184,9 +226,9 @@ decode_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
                         const uint32_t full = smem_u32(&ctl->full[stage]);
                         mbar_arrive_expect_tx(full, (uint32_t)p.stage_bytes);
                         const uint32_t sa = smem_base + (uint32_t)(stage * p.stage_bytes);
-                        tma_load_2d(sa, &tmW, full, kb * DBK, w_row + seg * p.b_seg_row);
+                        tma_load_2d(sa + w_off, &tmW, full, kb * DBK, w_row + seg * p.b_seg_row);
                         if (MODE == kGemmSwiGLU)
-                            tma_load_2d(sa + W_BYTES, &tmW, full, kb * DBK, w_row + p.up_off + seg * p.b_seg_row);
+                            tma_load_2d(sa + w_off + w_box, &tmW, full, kb * DBK, w_row + p.up_off + seg * p.b_seg_row);
                         tma_load_2d(sa + x_off, &tmX, full, seg * p.a_seg_col + kb * DBK, xr);
                         if (++stage == p.stages) { stage = 0; ph ^= 1u; }
                     }
@@ -204,8 +246,8 @@ decode_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
             const uint32_t idesc = idesc_bf16_f32(DBM, nb);
-            int stage = 0, acc = 0;
-            uint32_t ph = 0, aph = 0;
+            int stage = 0, acc = 0, cs = 0;
+            uint32_t ph = 0, aph = 0, cph = 0;
             bool ok = true;
             for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
                 const int rows = gcnt[it / ntn];
@@ -215,20 +257,28 @@ decode_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
                     const uint32_t d = tmem + (uint32_t)acc * acc_cols;
                     for (int i = 0; i < nk; ++i) {
                         if (!mbar_wait_bounded(smem_u32(&ctl->full[stage]), ph, abort)) { ok = false; break; }
+                        // FP8: the BF16 weights are in conversion slot cs (written by the
+                        // converter warps after this stage landed)
+                        if (FP8W && !mbar_wait_bounded(smem_u32(&ctl->cfull[cs]), cph, abort)) { ok = false; break; }
                         tc_fence_after();
                         const uint32_t sa = smem_base + (uint32_t)(stage * p.stage_bytes);
-                        const uint64_t wd = sdesc_k_sw128(sa);
+                        const uint32_t wa = FP8W ? smem_base + p.conv_off + (uint32_t)cs * p.conv_slot_bytes : sa + w_off;
+                        const uint64_t wd = sdesc_k_sw128(wa);
                         const uint64_t xd = sdesc_k_sw128(sa + x_off);
 #pragma unroll
                         for (int kk = 0; kk < DBK / 16; ++kk) {
                             const uint32_t accum = (i > 0 || kk > 0) ? 1u : 0u;
                             tc_mma_bf16(d, wd + (uint64_t)(kk * 2), xd + (uint64_t)(kk * 2), idesc, accum);
                             if (MODE == kGemmSwiGLU)
-                                tc_mma_bf16(d + (uint32_t)nb, sdesc_k_sw128(sa + W_BYTES) + (uint64_t)(kk * 2),
+                                tc_mma_bf16(d + (uint32_t)nb, sdesc_k_sw128(wa + W_BYTES) + (uint64_t)(kk * 2),
                                             xd + (uint64_t)(kk * 2), idesc, accum);
                         }
                         tc_commit(smem_u32(&ctl->empty[stage]));
                         if (++stage == p.stages) { stage = 0; ph ^= 1u; }
+                        if (FP8W) {
+                            tc_commit(smem_u32(&ctl->cempty[cs]));
+                            if (++cs == p.conv_slots) { cs = 0; cph ^= 1u; }
+                        }
                     }
                     if (!ok) break;
                     tc_commit(smem_u32(&ctl->tfull[acc]));
@@ -245,6 +295,56 @@ decode_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
                 *abort = 1;
             }
         }
+    } else if (FP8W && warp >= 6) {
+        // ---------------- FP8 -> BF16 converter (warps 6..9) ----------------
+        // Thread ct takes FP8 chunks ct + 128*j (j < 4) of each weight box: chunk
+        // (row r, 16 codes at K 16*c16) becomes BF16 chunks 2*c16 and 2*c16 + 1 of
+        // row r, stored at their 128-byte-swizzle positions.
+        const int ct = tid - 192;
+        int stage = 0, cs = 0;
+        uint32_t ph = 0, cph = 0;
+        bool ok = true;
+        for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
+            const int rows = gcnt[it / ntn];
+            for (int c0 = 0; c0 < rows && ok; c0 += nb) {
+                for (int i = 0; i < nk; ++i) {
+                    if (!mbar_wait_bounded(smem_u32(&ctl->full[stage]), ph, abort) ||
+                        !mbar_wait_bounded(smem_u32(&ctl->cempty[cs]), cph ^ 1u, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint8_t* src = smem + (size_t)stage * p.stage_bytes + w_off;
+                    uint8_t* dst = smem + p.conv_off + (size_t)cs * p.conv_slot_bytes;
+#pragma unroll
+                    for (int wb = 0; wb < NW; ++wb) {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const int idx = ct + 128 * j;
+                            const int r = idx >> 2, c16 = idx & 3;
+                            const uint4 v = *reinterpret_cast<const uint4*>(src + wb * W8_BYTES + r * 64 + c16 * 16);
+                            uint4 lo, hi;
+                            lo.x = e4m3x2_to_bf16x2(v.x & 0xffffu);
+                            lo.y = e4m3x2_to_bf16x2(v.x >> 16);
+                            lo.z = e4m3x2_to_bf16x2(v.y & 0xffffu);
+                            lo.w = e4m3x2_to_bf16x2(v.y >> 16);
+                            hi.x = e4m3x2_to_bf16x2(v.z & 0xffffu);
+                            hi.y = e4m3x2_to_bf16x2(v.z >> 16);
+                            hi.z = e4m3x2_to_bf16x2(v.w & 0xffffu);
+                            hi.w = e4m3x2_to_bf16x2(v.w >> 16);
+                            uint8_t* row = dst + wb * W_BYTES + r * 128;
+                            const int sw = r & 7;
+                            *reinterpret_cast<uint4*>(row + (((2 * c16) ^ sw) << 4)) = lo;
+                            *reinterpret_cast<uint4*>(row + (((2 * c16 + 1) ^ sw) << 4)) = hi;
+                        }
+                    }
+                    fence_proxy_async_smem();                   // generic writes -> tensor-core reads
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&ctl->cfull[cs]));
+                    if (++stage == p.stages) { stage = 0; ph ^= 1u; }
+                    if (++cs == p.conv_slots) { cs = 0; cph ^= 1u; }
+                }
+            }
+        }
     } else {
         // ---------------- epilogue (warps 2..5) ----------------
         const int q = warp & 3;                                 // TMEM lane quarter
@@ -257,6 +357,12 @@ decode_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
             const int n = nt * DBM + 32 * q + lane;             // weight row = output column
             typename OutOfD<MODE>::T* ocol = reinterpret_cast<typename OutOfD<MODE>::T*>(p.out) +
                                              (size_t)g * p.out_group_col + (n < p.N ? n : 0);
+            // FP8: the weight rows' FP32 scales (gate and up rows for SwiGLU)
+            float sg = 1.f, su = 1.f;
+            if (FP8W && n < p.N) {
+                sg = p.wscale[(size_t)g * p.b_group_rows + n];
+                if (MODE == kGemmSwiGLU) su = p.wscale[(size_t)g * p.b_group_rows + p.up_off + n];
+            }
             for (int c0 = 0; c0 < rows; c0 += nb) {
                 if (!mbar_wait_bounded(smem_u32(&ctl->tfull[acc]), aph, abort)) {
                     if (lane == 0) {
@@ -278,13 +384,15 @@ decode_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
                         for (int r = 0; r < 16; ++r) {
                             const int row = c0 + c + r;
                             if (row < rows) {
-                                const float x = __uint_as_float(gv[r]);
+                                const float x = FP8W ? __uint_as_float(gv[r]) * sg : __uint_as_float(gv[r]);
                                 auto* o = ocol + (size_t)(row0 + row) * p.ldo;
                                 if constexpr (MODE == kGemmF32) {
                                     *o = x;
                                 } else {
                                     float a;
-                                    if (MODE == kGemmSwiGLU) a = x / (1.0f + __expf(-x)) * __uint_as_float(uv[r]);
+                                    if (MODE == kGemmSwiGLU)
+                                        a = x / (1.0f + __expf(-x)) *
+                                            (FP8W ? __uint_as_float(uv[r]) * su : __uint_as_float(uv[r]));
                                     else if (MODE == kGemmReLU2) a = x > 0.f ? x * x : 0.f;
                                     else a = x;
                                     *o = __float2bfloat16_rn(a);
@@ -310,13 +418,13 @@ decode_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
     }
 }
 
-template <int MODE>
+template <int MODE, bool FP8W>
 cudaError_t launch_d(const CUtensorMap& mx, const CUtensorMap& mw, const DParams& dp, unsigned grid, size_t smem,
                      cudaStream_t st) {
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(decode_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        attr_err = cudaFuncSetAttribute(decode_gemm_kernel<MODE, FP8W>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         MAX_DSMEM);
     });
     if (attr_err != cudaSuccess) {
@@ -324,7 +432,8 @@ cudaError_t launch_d(const CUtensorMap& mx, const CUtensorMap& mw, const DParams
         return attr_err;
     }
     const cudaError_t e =
-        launch_kernel(decode_gemm_kernel<MODE>, dim3(grid), dim3(DTHREADS), smem, st, 1, kUsePdl, mx, mw, dp);
+        launch_kernel(decode_gemm_kernel<MODE, FP8W>, dim3(grid), dim3(FP8W ? DTHREADS_FP8 : DTHREADS), smem, st, 1,
+                      kUsePdl, mx, mw, dp);
     if (e != cudaSuccess) set_error("decode GEMM launch: %s", cudaGetErrorString(e));
     return e;
 }
@@ -337,6 +446,11 @@ moe_status launch_decode_gemm(const GemmProblem& g, int nb, WsHeader* hdr, cudaS
         return MOE_ERR_INTERNAL;
     }
     const int nw = g.mode == kGemmSwiGLU ? 2 : 1;
+    const bool fp8 = g.wfmt == kWeightFp8E4M3;
+    if (fp8 && (g.mode == kGemmF32 || !g.wscale)) {
+        set_error("decode GEMM: FP8 weights need a scale per weight row and a BF16 output");
+        return MOE_ERR_UNSUPPORTED;
+    }
     DParams dp;
     dp.offsets = g.offsets;
     dp.groups = g.groups;
@@ -354,7 +468,22 @@ moe_status launch_decode_gemm(const GemmProblem& g, int nb, WsHeader* hdr, cudaS
     dp.out_group_col = g.out_group_col;
     dp.hdr = hdr;
     dp.nb = nb;
-    dp.stage_bytes = nw * W_BYTES + nb * DBK * 2;
+    dp.wscale = g.wscale;
+    if (fp8) {
+        // stage: [activation box: nb rows x 128 B][FP8 weight box(es): 8 KiB each]
+        dp.x_off = 0;
+        dp.w_off = (uint32_t)(nb * DBK * 2);
+        dp.stage_bytes = nb * DBK * 2 + nw * W8_BYTES;
+        dp.conv_slots = nw == 2 ? 2 : 3;
+        dp.conv_slot_bytes = (uint32_t)(nw * W_BYTES);
+    } else {
+        // stage: [BF16 weight box(es): 16 KiB each][activation box]
+        dp.x_off = (uint32_t)(nw * W_BYTES);
+        dp.w_off = 0;
+        dp.stage_bytes = nw * W_BYTES + nb * DBK * 2;
+        dp.conv_slots = 0;
+        dp.conv_slot_bytes = 0;
+    }
     uint32_t cols = 32;
     while (cols < (uint32_t)(2 * nw * nb)) cols <<= 1;
     dp.tmem_cols = cols;
@@ -366,13 +495,15 @@ moe_status launch_decode_gemm(const GemmProblem& g, int nb, WsHeader* hdr, cudaS
     const int sms = device_sm_count();
     if (grid > sms) grid = sms;
     if (grid < 1) grid = 1;
-    const size_t fixed = 1024 + sizeof(DCtl) + (size_t)3 * g.groups * sizeof(int);
+    const size_t conv = (size_t)dp.conv_slots * dp.conv_slot_bytes;
+    const size_t fixed = 1024 + conv + sizeof(DCtl) + (size_t)3 * g.groups * sizeof(int);
     const int nk = ((g.K + DBK - 1) / DBK) * g.nseg;
     long long stages = ((long long)MAX_DSMEM - (long long)fixed) / dp.stage_bytes;
     if (stages > MAX_DSTAGES) stages = MAX_DSTAGES;
     if (stages > 2 * nk) stages = 2 * nk;              // two items' worth is plenty
     if (stages < 2) stages = 2;
     dp.stages = (int)stages;
+    dp.conv_off = (uint32_t)((size_t)stages * dp.stage_bytes);           // a multiple of 1 KiB
     const size_t smem = fixed + (size_t)stages * dp.stage_bytes;
     if (smem > (size_t)MAX_DSMEM) {
         set_error("decode GEMM needs %zu bytes of shared memory", smem);
@@ -380,13 +511,23 @@ moe_status launch_decode_gemm(const GemmProblem& g, int nb, WsHeader* hdr, cudaS
     }
     CUtensorMap mx, mw;
     if (!make_tensor_map_bf16(&mx, g.a, g.a_rows, g.a_cols, (unsigned)nb)) return MOE_ERR_CUDA;
-    if (!make_tensor_map_bf16(&mw, g.b, g.b_rows, g.b_cols, (unsigned)DBM)) return MOE_ERR_CUDA;
+    if (fp8 ? !make_tensor_map_u8_rows(&mw, g.b, g.b_rows, g.b_cols, (unsigned)DBK, (unsigned)DBM)
+            : !make_tensor_map_bf16(&mw, g.b, g.b_rows, g.b_cols, (unsigned)DBM))
+        return MOE_ERR_CUDA;
     cudaError_t e;
-    switch (g.mode) {
-        case kGemmSwiGLU: e = launch_d<kGemmSwiGLU>(mx, mw, dp, (unsigned)grid, smem, st); break;
-        case kGemmReLU2: e = launch_d<kGemmReLU2>(mx, mw, dp, (unsigned)grid, smem, st); break;
-        case kGemmF32: e = launch_d<kGemmF32>(mx, mw, dp, (unsigned)grid, smem, st); break;
-        default: e = launch_d<kGemmPlain>(mx, mw, dp, (unsigned)grid, smem, st); break;
+    if (fp8) {
+        switch (g.mode) {
+            case kGemmSwiGLU: e = launch_d<kGemmSwiGLU, true>(mx, mw, dp, (unsigned)grid, smem, st); break;
+            case kGemmReLU2: e = launch_d<kGemmReLU2, true>(mx, mw, dp, (unsigned)grid, smem, st); break;
+            default: e = launch_d<kGemmPlain, true>(mx, mw, dp, (unsigned)grid, smem, st); break;
+        }
+    } else {
+        switch (g.mode) {
+            case kGemmSwiGLU: e = launch_d<kGemmSwiGLU, false>(mx, mw, dp, (unsigned)grid, smem, st); break;
+            case kGemmReLU2: e = launch_d<kGemmReLU2, false>(mx, mw, dp, (unsigned)grid, smem, st); break;
+            case kGemmF32: e = launch_d<kGemmF32, false>(mx, mw, dp, (unsigned)grid, smem, st); break;
+            default: e = launch_d<kGemmPlain, false>(mx, mw, dp, (unsigned)grid, smem, st); break;
+        }
     }
     return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

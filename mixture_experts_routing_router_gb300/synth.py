@@ -182,6 +182,34 @@ def shared_expert_weights(wl: Workload, s: int, seed: int = 0, device="cpu", uni
             normal((H, Is), s2, seed, f"ws2/{s}", device))
 
 
+def quantize_rows_fp8(w: torch.Tensor):
+    """Input preparation for FP8 expert weights: each row of ``w`` [..., rows, K]
+    becomes E4M3 codes (torch's round-to-nearest float8_e4m3fn conversion) of
+    w / scale with scale = max|row| / 448 (1 for an all-zero row).
+    -> (codes uint8 [..., rows, K], scale float32 [..., rows])."""
+    wf = w.float()
+    amax = wf.abs().amax(dim=-1, keepdim=True)
+    scale = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
+    codes = (wf / scale).to(torch.float8_e4m3fn).view(torch.uint8)
+    return codes.contiguous(), scale.squeeze(-1).contiguous()
+
+
+def make_fp8_weights(wl: Workload, seed: int = 0, device="cpu", unit_scale: bool = False) -> dict:
+    """FP8 E4M3 expert weights with one FP32 scale per weight row, quantized
+    from the same per-expert BF16 draws as make_inputs:
+    w13 uint8 [E, up, H], s13 float32 [E, up], w2 uint8 [E, H, I], s2 float32 [E, H]."""
+    E, H, I = wl.experts, wl.hidden, wl.inter
+    d = {"w13": torch.empty((E, wl.up, H), dtype=torch.uint8, device=device),
+         "s13": torch.empty((E, wl.up), dtype=torch.float32, device=device),
+         "w2": torch.empty((E, H, I), dtype=torch.uint8, device=device),
+         "s2": torch.empty((E, H), dtype=torch.float32, device=device)}
+    for e in range(E):
+        a, b = expert_weights(wl, e, seed, device, unit_scale)
+        d["w13"][e], d["s13"][e] = quantize_rows_fp8(a)
+        d["w2"][e], d["s2"][e] = quantize_rows_fp8(b)
+    return d
+
+
 def gate_weights(wl: Workload, seed: int = 0, device="cpu") -> torch.Tensor:
     """Router projection W_gate [E, H] ~ N(0, 1/H): x ~ N(0,1) gives logits of
     about unit scale."""

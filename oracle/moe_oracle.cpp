@@ -349,6 +349,8 @@ void oracle_expert_ffn_fp8(int H, int E, int I, int act, const uint16_t* x_perm,
                            const uint8_t* w13, const float* s13, const uint8_t* w2, const float* s2,
                            uint16_t* h, uint16_t* y_perm) {
     const size_t up = (act == ACT_SWIGLU) ? 2 * (size_t)I : (size_t)I;
+    double dec[256];                          // the 256 code values, from the decode above
+    for (int c = 0; c < 256; ++c) dec[c] = fp8_e4m3_to_double((uint8_t)c);
     for (int e = 0; e < E; ++e) {
         const uint8_t* w13_e = w13 + (size_t)e * up * H;
         const float* s13_e = s13 + (size_t)e * up;
@@ -360,7 +362,7 @@ void oracle_expert_ffn_fp8(int H, int E, int I, int act, const uint16_t* x_perm,
             auto dot = [&](size_t wr) {
                 double acc = 0.0;
                 for (int c = 0; c < H; ++c)
-                    acc += bf16_to_double(x_row[c]) * fp8_e4m3_to_double(w13_e[wr * H + c]);
+                    acc += bf16_to_double(x_row[c]) * dec[w13_e[wr * H + c]];
                 return acc * (double)s13_e[wr];
             };
             for (int n = 0; n < I; ++n) {
@@ -376,7 +378,7 @@ void oracle_expert_ffn_fp8(int H, int E, int I, int act, const uint16_t* x_perm,
             for (int c = 0; c < H; ++c) {
                 double acc = 0.0;
                 for (int n = 0; n < I; ++n)
-                    acc += bf16_to_double(h_row[n]) * fp8_e4m3_to_double(w2_e[(size_t)c * I + n]);
+                    acc += bf16_to_double(h_row[n]) * dec[w2_e[(size_t)c * I + n]];
                 y_perm[(size_t)r * H + c] = double_to_bf16(acc * (double)s2_e[c]);
             }
         }

@@ -106,3 +106,25 @@ def test_status_strings(L):
     for code in range(9):
         assert len(N.status_string(code)) > 0
     assert N.status_string(3).startswith("an expert")
+
+
+def test_fp8_entry_points_validate_on_the_host(L):
+    fake = ctypes.c_void_p(4096)
+    # shared experts are not part of the FP8 entry points
+    s = shape(shared=1, shared_inter=64)
+    n = N.moe_workspace_size(s)
+    ws = ctypes.c_void_p(1 << 20)
+    assert L.moe_expert_up_fp8(ctypes.byref(s), fake, fake, fake, fake, fake, ws, n, None) == N.MOE_ERR_UNSUPPORTED
+    # TMA-loaded FP8 rows need hidden and inter to be multiples of 16
+    s = shape(hidden=264)
+    n = N.moe_workspace_size(s)
+    assert L.moe_layer_fp8(ctypes.byref(s), fake, None, None, fake, fake, fake, fake, fake, None, fake, ws, n,
+                           None) == N.MOE_ERR_INVALID_ARG
+    s = shape(inter=520)
+    n = N.moe_workspace_size(s)
+    assert L.moe_expert_down_fp8(ctypes.byref(s), fake, fake, fake, fake, fake, ws, n, None) == N.MOE_ERR_INVALID_ARG
+    # misaligned scale pointer
+    s = shape()
+    n = N.moe_workspace_size(s)
+    assert L.moe_expert_up_fp8(ctypes.byref(s), fake, fake, fake, ctypes.c_void_p(4100), fake, ws, n,
+                               None) == N.MOE_ERR_INVALID_ARG
