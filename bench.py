@@ -43,8 +43,9 @@ def describe(wl):
             + ", W ~ N(0,0.02), x ~ N(0,1), seed 0")
 
 
-def algorithmic(wl, counts=None):
-    """Bytes / FLOPs the method itself must move or compute (no padding)."""
+def algorithmic(wl, counts=None, weight_bytes=2):
+    """Bytes / FLOPs the method itself must move or compute (no padding).
+    weight_bytes: 2 for BF16 weights, 1 for FP8 (plus a 4-byte scale per row)."""
     T, H, E, k, I = wl.tokens, wl.hidden, wl.experts, wl.top_k, wl.inter
     R = T * k
     up = wl.up
@@ -57,8 +58,9 @@ def algorithmic(wl, counts=None):
     if counts is not None:
         nz = int((counts > 0).sum())
         d["nonempty_experts"] = nz
-        d["up_bytes"] = nz * up * H * 2 + R * H * 2 + R * I * 2
-        d["down_bytes"] = nz * H * I * 2 + R * I * 2 + R * H * 2
+        scales = 4 if weight_bytes == 1 else 0
+        d["up_bytes"] = nz * up * (H * weight_bytes + scales) + R * H * 2 + R * I * 2
+        d["down_bytes"] = nz * H * (I * weight_bytes + scales) + R * I * 2 + R * H * 2
     return d
 
 
@@ -71,12 +73,13 @@ def load_peaks():
     return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
 
 
-def up_kernel_name(wl, sms):
+def up_kernel_name(wl, sms, fp8=False):
     """Which kernel the library runs for the up projection (the library's own
-    host rule: the small-row kernel when a group holds at most 64 rows and its
-    items fit in two waves, the CTA-pair kernel when groups average 256 rows)."""
+    host rule: the small-row kernel for FP8 weights, or when a group holds at
+    most 64 rows and its items fit in two waves; the CTA-pair kernel when groups
+    average 256 rows)."""
     R = wl.tokens * wl.top_k
-    if wl.tokens <= 64 and min(wl.experts, R) * ((wl.inter + 127) // 128) <= 2 * sms:
+    if fp8 or (wl.tokens <= 64 and min(wl.experts, R) * ((wl.inter + 127) // 128) <= 2 * sms):
         return "decode_gemm_kernel (expert up projection)"
     if R // wl.experts >= 256:
         return "grouped_gemm_pair_kernel (expert up projection)"
@@ -276,17 +279,29 @@ def run_native(args, wl, world, rank, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     stream = torch.cuda.Stream(device=dev)
-    g = synth.make_inputs(wl, seed=rank, device=dev)
+    fp8 = args.weights == "fp8"
+    if fp8 and wl.shared:
+        raise SystemExit("FP8 expert weights: the workload has shared experts, which the FP8 entry points omit")
+    g = synth.make_inputs(wl, seed=rank, device=dev, weights=not fp8)
+    q = synth.make_fp8_weights(wl, seed=rank, device=dev) if fp8 else None
     shape = N.shape_of(wl)
     ws = N.workspace(shape, dev)
     T, H, E, k, I = wl.tokens, wl.hidden, wl.experts, wl.top_k, wl.inter
     R = T * k
     out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
-    kernels_per_layer = 6 + (2 if wl.shared else 0)
+    # route, count (+ clearing its look-back state when R > 1024 pairs), scatter,
+    # up, down, combine (+ the shared experts' up and down)
+    kernels_per_layer = 6 + (1 if R > 1024 else 0) + (2 if wl.shared else 0)
+
+    def layer_on(lg_d, x_d, out_d):
+        if fp8:
+            N.moe_layer_fp8(shape, lg_d, None, None, x_d, q["w13"], q["s13"], q["w2"], q["s2"], out_d, ws, stream)
+        else:
+            N.moe_layer(shape, lg_d, None, None, x_d, g["w13"], g["w2"], g.get("ws13"), g.get("ws2"), out_d, ws,
+                        stream)
 
     def layer():
-        N.moe_layer(shape, g["logits"], None, None, g["x"], g["w13"], g["w2"], g.get("ws13"), g.get("ws2"),
-                    out, ws, stream)
+        layer_on(g["logits"], g["x"], out)
 
     # L2: the large layer's inputs (x 235 MB, 22.5 GB of weights) exceed it;
     # smaller workloads get a write of 4x L2 before every timed step instead,
@@ -296,7 +311,8 @@ def run_native(args, wl, world, rank, local):
     stream.synchronize()
     l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 * 2**20) or 126 * 2**20
     cnt0 = ws_counts(N, shape, g, ws, stream, dev)
-    touched = int((cnt0 > 0).sum()) * (wl.up * H + H * I) * 2 + wl.shared * (wl.shared_up * H + H * wl.shared_inter) * 2
+    touched = int((cnt0 > 0).sum()) * (wl.up * H + H * I) * (1 if fp8 else 2) + \
+        wl.shared * (wl.shared_up * H + H * wl.shared_inter) * 2
     flush = not (g["x"].numel() * 2 > l2 and touched > 4 * l2)
     flush_buf = torch.empty(4 * l2, dtype=torch.uint8, device=dev) if flush else None
 
@@ -360,8 +376,10 @@ def run_native(args, wl, world, rank, local):
     stage_fns = [
         lambda: N.moe_route(shape, g["logits"], ids, w, ws, stream),
         lambda: N.moe_dispatch(shape, g["x"], ids, counts, offsets, dest, sp, x_perm, ws, stream),
-        lambda: N.moe_expert_up(shape, x_perm, offsets, g["w13"], g["x"], g.get("ws13"), h, ws, stream),
-        lambda: N.moe_expert_down(shape, h, offsets, g["w2"], g.get("ws2"), y_perm, y_sh, ws, stream),
+        (lambda: N.moe_expert_up_fp8(shape, x_perm, offsets, q["w13"], q["s13"], h, ws, stream)) if fp8 else
+        (lambda: N.moe_expert_up(shape, x_perm, offsets, g["w13"], g["x"], g.get("ws13"), h, ws, stream)),
+        (lambda: N.moe_expert_down_fp8(shape, h, offsets, q["w2"], q["s2"], y_perm, ws, stream)) if fp8 else
+        (lambda: N.moe_expert_down(shape, h, offsets, g["w2"], g.get("ws2"), y_perm, y_sh, ws, stream)),
         lambda: N.moe_combine(shape, y_perm, dest, w, y_sh, out, ws, stream),
     ]
     with torch.cuda.stream(stream):
@@ -413,7 +431,7 @@ def run_native(args, wl, world, rank, local):
     if st != N.MOE_OK:
         raise RuntimeError(f"device status {st} after stage timing")
     cnt = counts.cpu().numpy()
-    alg = algorithmic(wl, cnt)
+    alg = algorithmic(wl, cnt, 1 if fp8 else 2)
 
     # ---- end to end through the C-ABI with host buffers -----------------------
     # Every step copies its inputs (x, logits) from pinned host memory, runs
@@ -429,8 +447,7 @@ def run_native(args, wl, world, rank, local):
     e2e_steps = max(3, args.steps)
 
     def run_layer_on(lg_d, x_d, out_d):
-        N.moe_layer(shape, lg_d, None, None, x_d, g["w13"], g["w2"], g.get("ws13"), g.get("ws2"), out_d, ws,
-                    stream)
+        layer_on(lg_d, x_d, out_d)
 
     if not flush:
         s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
@@ -512,7 +529,7 @@ def run_native(args, wl, world, rank, local):
     gemm_tflops = (alg["up_flops"] + alg["down_flops"]) / ((stage_ms["expert_up"] + stage_ms["expert_down"]) / 1e3) / 1e12
 
     cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and not args.no_cpu_baseline and not fp8:     # the oracle sample is the BF16 layer
         import oracle
         oracle.build()
         rng = np.random.default_rng(0)
@@ -532,10 +549,13 @@ def run_native(args, wl, world, rank, local):
                        "l2": (f"L2 flushed before every timed step (write of {4 * l2 >> 20} MiB, outside the step's "
                               f"events)" if flush else
                               f"inputs larger than L2 (x {g['x'].numel() * 2 >> 20} MiB, touched weights "
-                              f"{touched >> 20} MiB): no flush")},
-            "roofline": {"kernel": up_kernel_name(wl, torch.cuda.get_device_properties(dev).multi_processor_count),
+                              f"{touched >> 20} MiB): no flush"),
+                       "expert_weights": ("FP8 E4M3 codes + one FP32 scale per weight row (quantized from the BF16 "
+                                          "draws); BF16 activations and MMA" if fp8 else "BF16")},
+            "roofline": {"kernel": up_kernel_name(wl, torch.cuda.get_device_properties(dev).multi_processor_count,
+                                                  fp8),
                          **roof,
-                         "traffic": ncu_traffic() if wl.name == WORKLOAD else None},
+                         "traffic": ncu_traffic() if wl.name == WORKLOAD and not fp8 else None},
             "expert_up_tflops": achieved,
             "dispatch_combine_gbs": dc_gbs, "dispatch_combine_hbm_frac": dc_gbs / peaks["hbm_gbs"],
             "gemm_tflops": gemm_tflops, "gemm_frac": gemm_tflops / peak,
@@ -557,6 +577,8 @@ def main():
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--cpu-tokens", type=int, default=24)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--weights", default="bf16", choices=["bf16", "fp8"],
+                    help="expert weight format (fp8: E4M3 codes with a scale per row, moe_layer_fp8)")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be at least 3")

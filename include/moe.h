@@ -212,8 +212,10 @@ MOE_API moe_status moe_layer(const moe_shape* shape, const float* logits, const 
  * quantized FC1/FC2 experts with BF16 activations, BF16 store boundaries and
  * FP32 accumulation; the codec here is FP8 E4M3 -- the afdEP-comm record's
  * fp8 payload type -- in place of the page's IQ2_XXS).
- *   w13       device u8  [E, up, H]  E4M3 codes (OCP: bias 7, no infinities,
- *                                    S.1111.111 is NaN); row layout as moe_expert_up
+ *   w13       device u8  [E, up, H]  E4M3 codes (OCP: bias 7, subnormals, no
+ *                                    infinities); row layout as moe_expert_up.  The
+ *                                    NaN codes S.1111.111 are not valid weights
+ *                                    (the kernels decode them as +-480)
  *   w13_scale device f32 [E, up]     one scale per weight row
  *   w2        device u8  [E, H, I]   E4M3 codes; w2_scale device f32 [E, H]
  * A weight is decode(code) * scale of its row; the kernels decode the codes to

@@ -386,8 +386,9 @@ moe_status launch_decode_gemm(const GemmProblem& p, int nb, WsHeader* hdr, cudaS
 // Tensor map of a row-major [rows, cols] BF16 matrix, 128-byte swizzle, boxes
 // of 64 columns x box_rows rows (records the failure for moe_last_error_message).
 bool make_tensor_map_bf16(CUtensorMap* m, const void* base, long long rows, long long cols, unsigned box_rows);
-// Tensor map of a row-major [rows, cols] byte matrix (FP8 codes), no swizzle,
-// boxes of box_cols bytes x box_rows rows.
+// Tensor map of a row-major [rows, cols] byte matrix (FP8 codes), boxes of
+// box_cols bytes x box_rows rows; 128-byte boxes are 128-byte swizzled, others
+// not swizzled.
 bool make_tensor_map_u8_rows(CUtensorMap* m, const void* base, long long rows, long long cols, unsigned box_cols,
                              unsigned box_rows);
 

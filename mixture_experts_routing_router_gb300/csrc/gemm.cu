@@ -884,6 +884,7 @@ bool make_tensor_map_bf16(CUtensorMap* m, const void* base, long long rows, long
 
 bool make_tensor_map_u8_rows(CUtensorMap* m, const void* base, long long rows, long long cols, unsigned box_cols,
                              unsigned box_rows) {
+    // 128-byte rows are 128-byte swizzled (the converter reads them conflict-free)
     auto enc = encode_fn();
     if (!enc) {
         set_error("cuTensorMapEncodeTiled is not available from the driver");
@@ -894,7 +895,8 @@ bool make_tensor_map_u8_rows(CUtensorMap* m, const void* base, long long rows, l
     cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1u, 1u};
     const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           box_cols == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
         set_error("cuTensorMapEncodeTiled failed (CUresult %d) for a [%lld, %lld] byte tensor at %p", (int)r, rows,

@@ -26,11 +26,12 @@
 // FP8 weights (FP8W): the weights arrive as OCP E4M3 codes with one FP32 scale
 // per weight row -- the ONNX Runtime operator's weight-only quantized experts
 // (BF16 activations), with E4M3 as the codec.  Every E4M3 value is exact in
-// BF16, so four more warps (6..9) convert each TMA-loaded FP8 box (128 rows x
-// 64 bytes, no swizzle) into the BF16 128-byte-swizzled K-major layout of a
-// separate ring of conversion slots, and the MMA stays BF16 with FP32
+// BF16, so eight more warps (6..13) convert each TMA-loaded FP8 box (128 rows x
+// 128 bytes, 128-byte swizzle: one 128-byte request per weight row, as for BF16) into
+// the BF16 128-byte-swizzled K-major layout of a separate ring of conversion
+// slots, one 64-wide K half per slot, and the MMA stays BF16 with FP32
 // accumulation; the row scale multiplies the accumulator in the epilogue.
-// The FP8 stage holds the activation box first, then the FP8 weight box(es).
+// The FP8 stage holds its two activation boxes first, then the FP8 weight box(es).
 #include "common.cuh"
 
 #include <mutex>
@@ -42,8 +43,10 @@ constexpr int DBM = 128;                   // weight rows per item (MMA M)
 constexpr int DBK = 64;                    // 64 BF16 = one 128-byte swizzle row
 constexpr int W_BYTES = DBM * DBK * 2;     // 16 KiB weight box
 constexpr int DTHREADS = 192;              // producer, MMA, 4 epilogue warps
-constexpr int DTHREADS_FP8 = 320;          // + 4 converter warps
-constexpr int W8_BYTES = DBM * DBK;        // 8 KiB FP8 weight box (128 rows x 64 codes)
+constexpr int CONV_WARPS = 8;              // FP8: converter warps (6 .. 6 + CONV_WARPS - 1)
+constexpr int DTHREADS_FP8 = 192 + 32 * CONV_WARPS;
+constexpr int DBK8 = 128;                  // FP8 stage: 128 codes (128 B) of each weight row
+constexpr int W8_BYTES = DBM * DBK8;       // 16 KiB FP8 weight box
 constexpr int MAX_CSLOTS = 4;
 constexpr int MAX_DSTAGES = 16;
 constexpr int MAX_DSMEM = 212 * 1024;
@@ -87,16 +90,25 @@ struct DCtl {
     int wsum[DTHREADS_FP8 / 32];
 };
 
-// Two E4M3 codes (low byte first) -> two BF16 values (low half first), exact:
-// E4M3 -> FP16 in hardware, FP16 -> FP32 -> BF16 without rounding.
-__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two) {
-    uint32_t h2, b;
-    float lo, hi;
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((unsigned short)two));
-    asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
-        : "=f"(lo), "=f"(hi) : "r"(h2));
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(b) : "f"(hi), "f"(lo));
-    return b;
+// Four E4M3 codes (bytes 0..3 of w) -> four BF16 values, exact, in integer and
+// one BF16 multiply per pair: prmt spreads two codes into 16-bit halves with
+// the sign byte replicated above each ([S|b]); shifting left 4 and masking
+// with 0x87F0 per half leaves the sign at bit 15 and the code's 7 exponent and
+// mantissa bits at bits 4..10 -- a BF16 whose exponent field is the E4M3
+// exponent field (bias 127 instead of 7) -- and multiplying by 2^120 rebiases
+// it.  An E4M3 subnormal (exponent field 0) is then a BF16 subnormal m*2^-129,
+// and the same multiply gives m*2^-9 exactly.  Out: lo = (b0, b1), hi = (b2, b3),
+// low half first.  The E4M3 NaN codes (S.1111.111) are not valid weights; they
+// decode to +-480 here.
+__device__ __forceinline__ void e4m3x4_to_bf16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    constexpr uint32_t kTwo120 = 0x7B807B80u;                 // (2^120, 2^120) in BF16
+    uint32_t t0, t1;
+    asm("prmt.b32 %0, %1, 0, 0x9180;" : "=r"(t0) : "r"(w));  // [S1 b1 S0 b0]
+    asm("prmt.b32 %0, %1, 0, 0xB3A2;" : "=r"(t1) : "r"(w));  // [S3 b3 S2 b2]
+    t0 = (t0 << 4) & 0x87F087F0u;
+    t1 = (t1 << 4) & 0x87F087F0u;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(lo) : "r"(t0), "r"(kTwo120));
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(hi) : "r"(t1), "r"(kTwo120));
 }
 
 __device__ __forceinline__ void clamped_bounds(const DParams& p, int g, int& lo, int& hi) {
@@ -137,7 +149,7 @@ decode_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
         }
         if (FP8W)
             for (int c = 0; c < p.conv_slots; ++c) {
-                mbar_init(smem_u32(&ctl->cfull[c]), 4);     // the 4 converter warps
+                mbar_init(smem_u32(&ctl->cfull[c]), CONV_WARPS);
                 mbar_init(smem_u32(&ctl->cempty[c]), 1);
             }
         mbar_init(smem_u32(&ctl->drain), 1);
@@ -202,8 +214,12 @@ decode_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
     volatile int* abort = &ctl->abort;
     const int ntn = (p.N + DBM - 1) / DBM;
     const int items = ctl->ng * ntn;
-    const int nkb = (p.K + DBK - 1) / DBK;
+    // K per stage: 64 (BF16 weights) or 128 (FP8: one 128-byte row per weight row
+    // and TMA request, split into two 64-wide halves for the MMA)
+    const int kstep = FP8W ? DBK8 : DBK;
+    const int nkb = (p.K + kstep - 1) / kstep;
     const int nk = nkb * p.nseg;
+    const uint32_t xbox = (uint32_t)(p.nb * DBK * 2);        // one activation box (nb rows x 64)
     const int nb = p.nb;
     const uint32_t acc_cols = (uint32_t)(NW * nb);
     const uint32_t x_off = p.x_off, w_off = p.w_off;
@@ -226,10 +242,12 @@ decode_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
                         const uint32_t full = smem_u32(&ctl->full[stage]);
                         mbar_arrive_expect_tx(full, (uint32_t)p.stage_bytes);
                         const uint32_t sa = smem_base + (uint32_t)(stage * p.stage_bytes);
-                        tma_load_2d(sa + w_off, &tmW, full, kb * DBK, w_row + seg * p.b_seg_row);
+                        tma_load_2d(sa + w_off, &tmW, full, kb * kstep, w_row + seg * p.b_seg_row);
                         if (MODE == kGemmSwiGLU)
-                            tma_load_2d(sa + w_off + w_box, &tmW, full, kb * DBK, w_row + p.up_off + seg * p.b_seg_row);
-                        tma_load_2d(sa + x_off, &tmX, full, seg * p.a_seg_col + kb * DBK, xr);
+                            tma_load_2d(sa + w_off + w_box, &tmW, full, kb * kstep, w_row + p.up_off + seg * p.b_seg_row);
+                        tma_load_2d(sa + x_off, &tmX, full, seg * p.a_seg_col + kb * kstep, xr);
+                        if (FP8W)   // the stage's second 64-wide activation half
+                            tma_load_2d(sa + x_off + xbox, &tmX, full, seg * p.a_seg_col + kb * kstep + DBK, xr);
                         if (++stage == p.stages) { stage = 0; ph ^= 1u; }
                     }
                 }
@@ -257,28 +275,32 @@ decode_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
                     const uint32_t d = tmem + (uint32_t)acc * acc_cols;
                     for (int i = 0; i < nk; ++i) {
                         if (!mbar_wait_bounded(smem_u32(&ctl->full[stage]), ph, abort)) { ok = false; break; }
-                        // FP8: the BF16 weights are in conversion slot cs (written by the
-                        // converter warps after this stage landed)
-                        if (FP8W && !mbar_wait_bounded(smem_u32(&ctl->cfull[cs]), cph, abort)) { ok = false; break; }
-                        tc_fence_after();
                         const uint32_t sa = smem_base + (uint32_t)(stage * p.stage_bytes);
-                        const uint32_t wa = FP8W ? smem_base + p.conv_off + (uint32_t)cs * p.conv_slot_bytes : sa + w_off;
-                        const uint64_t wd = sdesc_k_sw128(wa);
-                        const uint64_t xd = sdesc_k_sw128(sa + x_off);
+                        // FP8: each 64-wide half of the stage's weights is in a conversion
+                        // slot (written by the converter warps after the stage landed)
+                        for (int hf = 0; hf < (FP8W ? 2 : 1); ++hf) {
+                            if (FP8W && !mbar_wait_bounded(smem_u32(&ctl->cfull[cs]), cph, abort)) { ok = false; break; }
+                            tc_fence_after();
+                            const uint32_t wa =
+                                FP8W ? smem_base + p.conv_off + (uint32_t)cs * p.conv_slot_bytes : sa + w_off;
+                            const uint64_t wd = sdesc_k_sw128(wa);
+                            const uint64_t xd = sdesc_k_sw128(sa + x_off + (uint32_t)hf * xbox);
 #pragma unroll
-                        for (int kk = 0; kk < DBK / 16; ++kk) {
-                            const uint32_t accum = (i > 0 || kk > 0) ? 1u : 0u;
-                            tc_mma_bf16(d, wd + (uint64_t)(kk * 2), xd + (uint64_t)(kk * 2), idesc, accum);
-                            if (MODE == kGemmSwiGLU)
-                                tc_mma_bf16(d + (uint32_t)nb, sdesc_k_sw128(wa + W_BYTES) + (uint64_t)(kk * 2),
-                                            xd + (uint64_t)(kk * 2), idesc, accum);
+                            for (int kk = 0; kk < DBK / 16; ++kk) {
+                                const uint32_t accum = (i > 0 || hf > 0 || kk > 0) ? 1u : 0u;
+                                tc_mma_bf16(d, wd + (uint64_t)(kk * 2), xd + (uint64_t)(kk * 2), idesc, accum);
+                                if (MODE == kGemmSwiGLU)
+                                    tc_mma_bf16(d + (uint32_t)nb, sdesc_k_sw128(wa + W_BYTES) + (uint64_t)(kk * 2),
+                                                xd + (uint64_t)(kk * 2), idesc, accum);
+                            }
+                            if (FP8W) {
+                                tc_commit(smem_u32(&ctl->cempty[cs]));
+                                if (++cs == p.conv_slots) { cs = 0; cph ^= 1u; }
+                            }
                         }
+                        if (!ok) break;
                         tc_commit(smem_u32(&ctl->empty[stage]));
                         if (++stage == p.stages) { stage = 0; ph ^= 1u; }
-                        if (FP8W) {
-                            tc_commit(smem_u32(&ctl->cempty[cs]));
-                            if (++cs == p.conv_slots) { cs = 0; cph ^= 1u; }
-                        }
                     }
                     if (!ok) break;
                     tc_commit(smem_u32(&ctl->tfull[acc]));
@@ -296,10 +318,13 @@ decode_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
             }
         }
     } else if (FP8W && warp >= 6) {
-        // ---------------- FP8 -> BF16 converter (warps 6..9) ----------------
-        // Thread ct takes FP8 chunks ct + 128*j (j < 4) of each weight box: chunk
-        // (row r, 16 codes at K 16*c16) becomes BF16 chunks 2*c16 and 2*c16 + 1 of
-        // row r, stored at their 128-byte-swizzle positions.
+        // ---------------- FP8 -> BF16 converter (warps 6 .. 6 + CONV_WARPS - 1) ----
+        // A stage's FP8 box is 128 rows x 128 codes, 128-byte swizzled like the
+        // BF16 tiles (16-byte chunk c of row r at chunk c ^ (r & 7)); its K half hf
+        // (codes 64*hf .. +63) goes to one conversion slot.  Thread ct takes
+        // chunks ct + 32*CONV_WARPS*j of the half: chunk (row r, 16 codes at half-K
+        // 16*c4) becomes BF16 chunks 2*c4 and 2*c4 + 1 of row r, at their
+        // 128-byte-swizzle positions.
         const int ct = tid - 192;
         int stage = 0, cs = 0;
         uint32_t ph = 0, cph = 0;
@@ -307,41 +332,37 @@ decode_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
         for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
             const int rows = gcnt[it / ntn];
             for (int c0 = 0; c0 < rows && ok; c0 += nb) {
-                for (int i = 0; i < nk; ++i) {
-                    if (!mbar_wait_bounded(smem_u32(&ctl->full[stage]), ph, abort) ||
-                        !mbar_wait_bounded(smem_u32(&ctl->cempty[cs]), cph ^ 1u, abort)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint8_t* src = smem + (size_t)stage * p.stage_bytes + w_off;
-                    uint8_t* dst = smem + p.conv_off + (size_t)cs * p.conv_slot_bytes;
+                for (int i = 0; i < nk && ok; ++i) {
+                    if (!mbar_wait_bounded(smem_u32(&ctl->full[stage]), ph, abort)) { ok = false; break; }
+                    for (int hf = 0; hf < 2; ++hf) {
+                        if (!mbar_wait_bounded(smem_u32(&ctl->cempty[cs]), cph ^ 1u, abort)) { ok = false; break; }
+                        const uint8_t* src = smem + (size_t)stage * p.stage_bytes + w_off;
+                        uint8_t* dst = smem + p.conv_off + (size_t)cs * p.conv_slot_bytes;
 #pragma unroll
-                    for (int wb = 0; wb < NW; ++wb) {
+                        for (int wb = 0; wb < NW; ++wb) {
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const int idx = ct + 128 * j;
-                            const int r = idx >> 2, c16 = idx & 3;
-                            const uint4 v = *reinterpret_cast<const uint4*>(src + wb * W8_BYTES + r * 64 + c16 * 16);
-                            uint4 lo, hi;
-                            lo.x = e4m3x2_to_bf16x2(v.x & 0xffffu);
-                            lo.y = e4m3x2_to_bf16x2(v.x >> 16);
-                            lo.z = e4m3x2_to_bf16x2(v.y & 0xffffu);
-                            lo.w = e4m3x2_to_bf16x2(v.y >> 16);
-                            hi.x = e4m3x2_to_bf16x2(v.z & 0xffffu);
-                            hi.y = e4m3x2_to_bf16x2(v.z >> 16);
-                            hi.z = e4m3x2_to_bf16x2(v.w & 0xffffu);
-                            hi.w = e4m3x2_to_bf16x2(v.w >> 16);
-                            uint8_t* row = dst + wb * W_BYTES + r * 128;
-                            const int sw = r & 7;
-                            *reinterpret_cast<uint4*>(row + (((2 * c16) ^ sw) << 4)) = lo;
-                            *reinterpret_cast<uint4*>(row + (((2 * c16 + 1) ^ sw) << 4)) = hi;
+                            for (int j = 0; j < 512 / (32 * CONV_WARPS); ++j) {
+                                const int idx = ct + 32 * CONV_WARPS * j;
+                                const int r = idx >> 2, c16 = idx & 3;
+                                const int sw = r & 7;
+                                const uint4 v = *reinterpret_cast<const uint4*>(
+                                    src + wb * W8_BYTES + r * DBK8 + (((4 * hf + c16) ^ sw) << 4));
+                                uint4 lo, hi;
+                                e4m3x4_to_bf16x4(v.x, lo.x, lo.y);
+                                e4m3x4_to_bf16x4(v.y, lo.z, lo.w);
+                                e4m3x4_to_bf16x4(v.z, hi.x, hi.y);
+                                e4m3x4_to_bf16x4(v.w, hi.z, hi.w);
+                                uint8_t* row = dst + wb * W_BYTES + r * 128;
+                                *reinterpret_cast<uint4*>(row + (((2 * c16) ^ sw) << 4)) = lo;
+                                *reinterpret_cast<uint4*>(row + (((2 * c16 + 1) ^ sw) << 4)) = hi;
+                            }
                         }
+                        fence_proxy_async_smem();                   // generic writes -> tensor-core reads
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(smem_u32(&ctl->cfull[cs]));
+                        if (++cs == p.conv_slots) { cs = 0; cph ^= 1u; }
                     }
-                    fence_proxy_async_smem();                   // generic writes -> tensor-core reads
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(smem_u32(&ctl->cfull[cs]));
                     if (++stage == p.stages) { stage = 0; ph ^= 1u; }
-                    if (++cs == p.conv_slots) { cs = 0; cph ^= 1u; }
                 }
             }
         }
@@ -470,10 +491,11 @@ moe_status launch_decode_gemm(const GemmProblem& g, int nb, WsHeader* hdr, cudaS
     dp.nb = nb;
     dp.wscale = g.wscale;
     if (fp8) {
-        // stage: [activation box: nb rows x 128 B][FP8 weight box(es): 8 KiB each]
+        // stage (K 128): [two activation boxes: nb rows x 128 B each][FP8 weight
+        // box(es): 128 rows x 128 B = 16 KiB each]
         dp.x_off = 0;
-        dp.w_off = (uint32_t)(nb * DBK * 2);
-        dp.stage_bytes = nb * DBK * 2 + nw * W8_BYTES;
+        dp.w_off = (uint32_t)(2 * nb * DBK * 2);
+        dp.stage_bytes = 2 * nb * DBK * 2 + nw * W8_BYTES;
         dp.conv_slots = nw == 2 ? 2 : 3;
         dp.conv_slot_bytes = (uint32_t)(nw * W_BYTES);
     } else {
@@ -497,7 +519,7 @@ moe_status launch_decode_gemm(const GemmProblem& g, int nb, WsHeader* hdr, cudaS
     if (grid < 1) grid = 1;
     const size_t conv = (size_t)dp.conv_slots * dp.conv_slot_bytes;
     const size_t fixed = 1024 + conv + sizeof(DCtl) + (size_t)3 * g.groups * sizeof(int);
-    const int nk = ((g.K + DBK - 1) / DBK) * g.nseg;
+    const int nk = ((g.K + (fp8 ? DBK8 : DBK) - 1) / (fp8 ? DBK8 : DBK)) * g.nseg;
     long long stages = ((long long)MAX_DSMEM - (long long)fixed) / dp.stage_bytes;
     if (stages > MAX_DSTAGES) stages = MAX_DSTAGES;
     if (stages > 2 * nk) stages = 2 * nk;              // two items' worth is plenty
@@ -511,7 +533,7 @@ moe_status launch_decode_gemm(const GemmProblem& g, int nb, WsHeader* hdr, cudaS
     }
     CUtensorMap mx, mw;
     if (!make_tensor_map_bf16(&mx, g.a, g.a_rows, g.a_cols, (unsigned)nb)) return MOE_ERR_CUDA;
-    if (fp8 ? !make_tensor_map_u8_rows(&mw, g.b, g.b_rows, g.b_cols, (unsigned)DBK, (unsigned)DBM)
+    if (fp8 ? !make_tensor_map_u8_rows(&mw, g.b, g.b_rows, g.b_cols, (unsigned)DBK8, (unsigned)DBM)
             : !make_tensor_map_bf16(&mw, g.b, g.b_rows, g.b_cols, (unsigned)DBM))
         return MOE_ERR_CUDA;
     cudaError_t e;

@@ -145,3 +145,35 @@ def test_fp8_layer_is_graph_capturable_and_deterministic():
         torch.cuda.synchronize()
         assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
     assert N.moe_status_read(ws) == N.MOE_OK
+
+
+def test_fp8_every_finite_code_decodes_exactly():
+    """The down projection on one-hot rows returns single weights: y[r][c] =
+    decode(W2[c][r]) * 1, exact in BF16.  W2 cycles through all 254 finite
+    E4M3 codes (both zeros, the subnormals, +-448), so every code's decode in
+    the kernel -- subnormals included -- is checked bit for bit against the
+    oracle's decode."""
+    H = I = R = 256
+    wl = synth.Workload("codes", R, H, 1, 1, I, act=synth.ACT_RELU2)
+    codes = np.arange(H * I, dtype=np.int64) % 256
+    codes[(codes == 0x7F) | (codes == 0xFF)] = 0x38                    # the two NaN codes are not weights
+    codes = codes.astype(np.uint8).reshape(1, H, I)
+    rng = np.random.default_rng(3)
+    codes[0] = codes[0][:, rng.permutation(I)]                          # every column sees many codes
+    w2 = torch.from_numpy(codes).to(dev())
+    s2 = torch.ones(1, H, dtype=torch.float32, device=dev())
+    h = torch.eye(R, I, dtype=torch.bfloat16, device=dev())
+    offsets = i32_dev(np.array([0, R], np.int32))
+    shape = N.shape_of(wl)
+    ws = N.workspace(shape, dev())
+    y = torch.empty(R, H, dtype=torch.bfloat16, device=dev())
+    N.moe_expert_down_fp8(shape, h, offsets, w2, s2, y, ws)
+    assert N.moe_status_read(ws) == N.MOE_OK
+    want = oracle.fp8_e4m3_decode(codes[0].T)                           # y[r][c] = decode(W2[c][r])
+    want_bits = torch.from_numpy(want).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = bits(y)
+    # the sum adds the other columns' +0 products, so code 0x80 (-0) comes out
+    # as +0: compare values (equal as numbers, -0 == +0), every other code bitwise
+    neg_zero = codes[0].T == 0x80
+    assert np.array_equal(got[~neg_zero], want_bits[~neg_zero]), int((got != want_bits)[~neg_zero].sum())
+    assert np.all(got[neg_zero] == 0)
