@@ -27,10 +27,11 @@
 // per weight row -- the ONNX Runtime operator's weight-only quantized experts
 // (BF16 activations), with E4M3 as the codec.  Every E4M3 value is exact in
 // BF16, so eight more warps (6..13) convert each TMA-loaded FP8 box (128 rows x
-// 128 bytes, 128-byte swizzle: one 128-byte request per weight row, as for BF16) into
-// the BF16 128-byte-swizzled K-major layout of a separate ring of conversion
-// slots, one 64-wide K half per slot, and the MMA stays BF16 with FP32
-// accumulation; the row scale multiplies the accumulator in the epilogue.
+// 128 bytes, 128-byte swizzle: one 128-byte request per weight row, as for BF16)
+// straight into TMEM -- each thread one weight row, its TMEM lane -- where the
+// MMA reads its A operand (tcgen05.mma with A in TMEM), in a ring of slots.
+// The MMA stays BF16 with FP32 accumulation; the row scale multiplies the
+// accumulator in the epilogue.
 // The FP8 stage holds its two activation boxes first, then the FP8 weight box(es).
 #include "common.cuh"
 
@@ -68,9 +69,8 @@ struct DParams {
     uint32_t w_off;             // first weight box within a stage
     // FP8 weights
     const float* wscale;        // [weight rows] FP32 scale per weight row
-    uint32_t conv_off;          // conversion ring, from the aligned shared-memory base
-    uint32_t conv_slot_bytes;
-    int conv_slots;
+    uint32_t a_col;             // TMEM column of the first converted-weight slot
+    int conv_slots;             // converted-weight slots in TMEM (NW * 64 columns each)
 };
 
 template <int MODE> struct OutOfD { using T = __nv_bfloat16; };
@@ -118,6 +118,30 @@ __device__ __forceinline__ void clamped_bounds(const DParams& p, int g, int& lo,
     hi = hi < lo ? lo : (hi > p.a_rows ? p.a_rows : hi);
 }
 
+// D[tmem] (+)= A[tmem] * B[smem]^T: A (M x K, BF16) in TMEM, one row per lane
+// and two consecutive K elements per 32-bit column (lower K in the low half).
+__device__ __forceinline__ void tc_mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                               uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+        :: "r"(d_tmem), "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate) : "memory");
+}
+// 32 consecutive 32-bit columns of this warp's 32 TMEM lanes (one lane per thread).
+__device__ __forceinline__ void tmem_st_32cols(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
+        :: "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+           "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
+           "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]),
+           "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 template <int MODE, bool FP8W>
 __global__ void __launch_bounds__(FP8W ? DTHREADS_FP8 : DTHREADS, 1)
 decode_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
@@ -127,9 +151,8 @@ decode_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + ((1024u - (raw_u32 & 1023u)) & 1023u);
-    // [TMA stage ring][FP8 conversion ring][control block][group lists]
-    DCtl* ctl = reinterpret_cast<DCtl*>(smem + (size_t)p.stages * p.stage_bytes +
-                                        (size_t)p.conv_slots * p.conv_slot_bytes);
+    // [TMA stage ring][control block][group lists]
+    DCtl* ctl = reinterpret_cast<DCtl*>(smem + (size_t)p.stages * p.stage_bytes);
     int* gid = reinterpret_cast<int*>(ctl + 1);            // [groups] non-empty groups, in order
     int* gst = gid + p.groups;                              // first row
     int* gcnt = gst + p.groups;                             // rows
@@ -276,29 +299,41 @@ decode_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
                     for (int i = 0; i < nk; ++i) {
                         if (!mbar_wait_bounded(smem_u32(&ctl->full[stage]), ph, abort)) { ok = false; break; }
                         const uint32_t sa = smem_base + (uint32_t)(stage * p.stage_bytes);
-                        // FP8: each 64-wide half of the stage's weights is in a conversion
-                        // slot (written by the converter warps after the stage landed)
-                        for (int hf = 0; hf < (FP8W ? 2 : 1); ++hf) {
-                            if (FP8W && !mbar_wait_bounded(smem_u32(&ctl->cfull[cs]), cph, abort)) { ok = false; break; }
+                        if constexpr (FP8W) {
+                            // the stage's weights, converted to BF16, are in TMEM slot cs:
+                            // box wb, K half hf at columns a_col + cs*NW*64 + wb*64 + hf*32
+                            if (!mbar_wait_bounded(smem_u32(&ctl->cfull[cs]), cph, abort)) { ok = false; break; }
                             tc_fence_after();
-                            const uint32_t wa =
-                                FP8W ? smem_base + p.conv_off + (uint32_t)cs * p.conv_slot_bytes : sa + w_off;
-                            const uint64_t wd = sdesc_k_sw128(wa);
-                            const uint64_t xd = sdesc_k_sw128(sa + x_off + (uint32_t)hf * xbox);
+                            const uint32_t aslot = tmem + p.a_col + (uint32_t)(cs * NW * 64);
+#pragma unroll
+                            for (int hf = 0; hf < 2; ++hf) {
+                                const uint64_t xd = sdesc_k_sw128(sa + x_off + (uint32_t)hf * xbox);
+#pragma unroll
+                                for (int kk = 0; kk < DBK / 16; ++kk) {
+                                    const uint32_t accum = (i > 0 || hf > 0 || kk > 0) ? 1u : 0u;
+                                    const uint32_t acol = (uint32_t)(hf * 32 + kk * 8);
+                                    tc_mma_bf16_ts(d, aslot + acol, xd + (uint64_t)(kk * 2), idesc, accum);
+                                    if (MODE == kGemmSwiGLU)
+                                        tc_mma_bf16_ts(d + (uint32_t)nb, aslot + 64 + acol, xd + (uint64_t)(kk * 2),
+                                                       idesc, accum);
+                                }
+                            }
+                            tc_commit(smem_u32(&ctl->cempty[cs]));
+                            if (++cs == p.conv_slots) { cs = 0; cph ^= 1u; }
+                        } else {
+                            tc_fence_after();
+                            const uint64_t wd = sdesc_k_sw128(sa + w_off);
+                            const uint64_t xd = sdesc_k_sw128(sa + x_off);
 #pragma unroll
                             for (int kk = 0; kk < DBK / 16; ++kk) {
-                                const uint32_t accum = (i > 0 || hf > 0 || kk > 0) ? 1u : 0u;
+                                const uint32_t accum = (i > 0 || kk > 0) ? 1u : 0u;
                                 tc_mma_bf16(d, wd + (uint64_t)(kk * 2), xd + (uint64_t)(kk * 2), idesc, accum);
                                 if (MODE == kGemmSwiGLU)
-                                    tc_mma_bf16(d + (uint32_t)nb, sdesc_k_sw128(wa + W_BYTES) + (uint64_t)(kk * 2),
+                                    tc_mma_bf16(d + (uint32_t)nb,
+                                                sdesc_k_sw128(sa + w_off + W_BYTES) + (uint64_t)(kk * 2),
                                                 xd + (uint64_t)(kk * 2), idesc, accum);
                             }
-                            if (FP8W) {
-                                tc_commit(smem_u32(&ctl->cempty[cs]));
-                                if (++cs == p.conv_slots) { cs = 0; cph ^= 1u; }
-                            }
                         }
-                        if (!ok) break;
                         tc_commit(smem_u32(&ctl->empty[stage]));
                         if (++stage == p.stages) { stage = 0; ph ^= 1u; }
                     }
@@ -319,50 +354,52 @@ decode_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
         }
     } else if (FP8W && warp >= 6) {
         // ---------------- FP8 -> BF16 converter (warps 6 .. 6 + CONV_WARPS - 1) ----
-        // A stage's FP8 box is 128 rows x 128 codes, 128-byte swizzled like the
-        // BF16 tiles (16-byte chunk c of row r at chunk c ^ (r & 7)); its K half hf
-        // (codes 64*hf .. +63) goes to one conversion slot.  Thread ct takes
-        // chunks ct + 32*CONV_WARPS*j of the half: chunk (row r, 16 codes at half-K
-        // 16*c4) becomes BF16 chunks 2*c4 and 2*c4 + 1 of row r, at their
-        // 128-byte-swizzle positions.
-        const int ct = tid - 192;
+        // A stage's FP8 box is 128 rows x 128 codes, 128-byte swizzled (16-byte
+        // chunk c of row r at chunk c ^ (r & 7)).  Converter warp w owns TMEM lane
+        // quarter w % 4, i.e. weight rows r = 32*(w % 4) + lane, and K half
+        // hf = (w - 6) / 4 of every stage: each thread decodes its row's 64 codes
+        // of that half (four conflict-free 16-byte loads) and stores the 32 packed
+        // BF16 pairs to its TMEM lane, columns a_col + cs*NW*64 + wb*64 + hf*32.
+        const int q = warp & 3;
+        const int hf = (warp - 6) >> 2;
+        const int r = 32 * q + lane;
+        const int sw = r & 7;
         int stage = 0, cs = 0;
         uint32_t ph = 0, cph = 0;
         bool ok = true;
         for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
             const int rows = gcnt[it / ntn];
             for (int c0 = 0; c0 < rows && ok; c0 += nb) {
-                for (int i = 0; i < nk && ok; ++i) {
-                    if (!mbar_wait_bounded(smem_u32(&ctl->full[stage]), ph, abort)) { ok = false; break; }
-                    for (int hf = 0; hf < 2; ++hf) {
-                        if (!mbar_wait_bounded(smem_u32(&ctl->cempty[cs]), cph ^ 1u, abort)) { ok = false; break; }
-                        const uint8_t* src = smem + (size_t)stage * p.stage_bytes + w_off;
-                        uint8_t* dst = smem + p.conv_off + (size_t)cs * p.conv_slot_bytes;
-#pragma unroll
-                        for (int wb = 0; wb < NW; ++wb) {
-#pragma unroll
-                            for (int j = 0; j < 512 / (32 * CONV_WARPS); ++j) {
-                                const int idx = ct + 32 * CONV_WARPS * j;
-                                const int r = idx >> 2, c16 = idx & 3;
-                                const int sw = r & 7;
-                                const uint4 v = *reinterpret_cast<const uint4*>(
-                                    src + wb * W8_BYTES + r * DBK8 + (((4 * hf + c16) ^ sw) << 4));
-                                uint4 lo, hi;
-                                e4m3x4_to_bf16x4(v.x, lo.x, lo.y);
-                                e4m3x4_to_bf16x4(v.y, lo.z, lo.w);
-                                e4m3x4_to_bf16x4(v.z, hi.x, hi.y);
-                                e4m3x4_to_bf16x4(v.w, hi.z, hi.w);
-                                uint8_t* row = dst + wb * W_BYTES + r * 128;
-                                *reinterpret_cast<uint4*>(row + (((2 * c16) ^ sw) << 4)) = lo;
-                                *reinterpret_cast<uint4*>(row + (((2 * c16 + 1) ^ sw) << 4)) = hi;
-                            }
-                        }
-                        fence_proxy_async_smem();                   // generic writes -> tensor-core reads
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(smem_u32(&ctl->cfull[cs]));
-                        if (++cs == p.conv_slots) { cs = 0; cph ^= 1u; }
+                for (int i = 0; i < nk; ++i) {
+                    if (!mbar_wait_bounded(smem_u32(&ctl->full[stage]), ph, abort) ||
+                        !mbar_wait_bounded(smem_u32(&ctl->cempty[cs]), cph ^ 1u, abort)) {
+                        ok = false;
+                        break;
                     }
+                    tc_fence_after();                           // after the MMAs that read slot cs
+                    const uint8_t* src = smem + (size_t)stage * p.stage_bytes + w_off + (size_t)r * DBK8;
+                    const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + p.a_col + (uint32_t)(cs * NW * 64) +
+                                           (uint32_t)(hf * 32);
+#pragma unroll
+                    for (int wb = 0; wb < NW; ++wb) {
+                        uint32_t v32[32];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const uint4 v = *reinterpret_cast<const uint4*>(src + wb * W8_BYTES +
+                                                                            (((4 * hf + j) ^ sw) << 4));
+                            e4m3x4_to_bf16x4(v.x, v32[8 * j + 0], v32[8 * j + 1]);
+                            e4m3x4_to_bf16x4(v.y, v32[8 * j + 2], v32[8 * j + 3]);
+                            e4m3x4_to_bf16x4(v.z, v32[8 * j + 4], v32[8 * j + 5]);
+                            e4m3x4_to_bf16x4(v.w, v32[8 * j + 6], v32[8 * j + 7]);
+                        }
+                        tmem_st_32cols(taddr + (uint32_t)(wb * 64), v32);
+                    }
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&ctl->cfull[cs]));
                     if (++stage == p.stages) { stage = 0; ph ^= 1u; }
+                    if (++cs == p.conv_slots) { cs = 0; cph ^= 1u; }
                 }
             }
         }
@@ -496,19 +533,20 @@ moe_status launch_decode_gemm(const GemmProblem& g, int nb, WsHeader* hdr, cudaS
         dp.x_off = 0;
         dp.w_off = (uint32_t)(2 * nb * DBK * 2);
         dp.stage_bytes = 2 * nb * DBK * 2 + nw * W8_BYTES;
+        // TMEM: accumulators in columns 0..255, converted weights from 256 on
         dp.conv_slots = nw == 2 ? 2 : 3;
-        dp.conv_slot_bytes = (uint32_t)(nw * W_BYTES);
+        dp.a_col = 256;
     } else {
         // stage: [BF16 weight box(es): 16 KiB each][activation box]
         dp.x_off = (uint32_t)(nw * W_BYTES);
         dp.w_off = 0;
         dp.stage_bytes = nw * W_BYTES + nb * DBK * 2;
         dp.conv_slots = 0;
-        dp.conv_slot_bytes = 0;
+        dp.a_col = 0;
     }
     uint32_t cols = 32;
     while (cols < (uint32_t)(2 * nw * nb)) cols <<= 1;
-    dp.tmem_cols = cols;
+    dp.tmem_cols = fp8 ? 512u : cols;
 
     // items: (non-empty group) x (128-row weight block); at most one CTA per SM
     const long long ntn = (g.N + DBM - 1) / DBM;
@@ -517,15 +555,15 @@ moe_status launch_decode_gemm(const GemmProblem& g, int nb, WsHeader* hdr, cudaS
     const int sms = device_sm_count();
     if (grid > sms) grid = sms;
     if (grid < 1) grid = 1;
-    const size_t conv = (size_t)dp.conv_slots * dp.conv_slot_bytes;
-    const size_t fixed = 1024 + conv + sizeof(DCtl) + (size_t)3 * g.groups * sizeof(int);
+    const size_t fixed = 1024 + sizeof(DCtl) + (size_t)3 * g.groups * sizeof(int);
     const int nk = ((g.K + (fp8 ? DBK8 : DBK) - 1) / (fp8 ? DBK8 : DBK)) * g.nseg;
     long long stages = ((long long)MAX_DSMEM - (long long)fixed) / dp.stage_bytes;
     if (stages > MAX_DSTAGES) stages = MAX_DSTAGES;
-    if (stages > 2 * nk) stages = 2 * nk;              // two items' worth is plenty
+    // two items' worth is plenty; FP8 (512 TMEM columns) keeps a full ring so
+    // that one CTA holds an SM
+    if (!fp8 && stages > 2 * nk) stages = 2 * nk;
     if (stages < 2) stages = 2;
     dp.stages = (int)stages;
-    dp.conv_off = (uint32_t)((size_t)stages * dp.stage_bytes);           // a multiple of 1 KiB
     const size_t smem = fixed + (size_t)stages * dp.stage_bytes;
     if (smem > (size_t)MAX_DSMEM) {
         set_error("decode GEMM needs %zu bytes of shared memory", smem);
