@@ -354,10 +354,11 @@ moe_status moe_layer(const moe_shape* shape, const float* logits, const int32_t*
     const WsLayout L = ws_layout(s);
     const int32_t* ids = ids_in;
     const float* w = w_in;
+    const bool small = s.tokens <= kSmallDispatchTokens;   // one fused route + dispatch kernel
     if (logits) {
         int32_t* ids_ws = at<int32_t>(ws, L.ids);
         float* w_ws = at<float>(ws, L.w);
-        if ((r = do_route(s, logits, ids_ws, w_ws, ws, st)) != MOE_OK) return r;
+        if (!small && (r = do_route(s, logits, ids_ws, w_ws, ws, st)) != MOE_OK) return r;
         ids = ids_ws;
         w = w_ws;
     }
@@ -367,9 +368,16 @@ moe_status moe_layer(const moe_shape* shape, const float* logits, const int32_t*
     uint16_t* h = at<uint16_t>(ws, L.h);
     uint16_t* y_perm = at<uint16_t>(ws, L.y_perm);
     uint16_t* y_shared = s.shared > 0 ? at<uint16_t>(ws, L.y_shared) : nullptr;
-    if ((r = do_dispatch(s, x, ids, at<int32_t>(ws, L.counts), offsets, dest, at<int32_t>(ws, L.sorted_pair), x_perm,
-                         ws, st)) != MOE_OK)
+    if (small) {
+        if ((r = from_cuda(launch_small_dispatch(s, logits, ids_in, at<int32_t>(ws, L.ids), at<float>(ws, L.w), x,
+                                                 at<int32_t>(ws, L.counts), offsets, dest,
+                                                 at<int32_t>(ws, L.sorted_pair), x_perm, at<WsHeader>(ws, 0), st))) !=
+            MOE_OK)
+            return r;
+    } else if ((r = do_dispatch(s, x, ids, at<int32_t>(ws, L.counts), offsets, dest, at<int32_t>(ws, L.sorted_pair),
+                                x_perm, ws, st)) != MOE_OK) {
         return r;
+    }
     if ((r = do_up(s, x_perm, offsets, w13, x, ws13, h, ws, st)) != MOE_OK) return r;
     if ((r = do_down(s, h, offsets, w2, ws2, y_perm, y_shared, ws, st)) != MOE_OK) return r;
     return do_combine(s, y_perm, dest, w, y_shared, residual, out, st);
@@ -419,10 +427,11 @@ moe_status moe_layer_fp8(const moe_shape* shape, const float* logits, const int3
     const WsLayout L = ws_layout(s);
     const int32_t* ids = ids_in;
     const float* w = w_in;
+    const bool small = s.tokens <= kSmallDispatchTokens;   // one fused route + dispatch kernel
     if (logits) {
         int32_t* ids_ws = at<int32_t>(ws, L.ids);
         float* w_ws = at<float>(ws, L.w);
-        if ((r = do_route(s, logits, ids_ws, w_ws, ws, st)) != MOE_OK) return r;
+        if (!small && (r = do_route(s, logits, ids_ws, w_ws, ws, st)) != MOE_OK) return r;
         ids = ids_ws;
         w = w_ws;
     }
@@ -431,9 +440,16 @@ moe_status moe_layer_fp8(const moe_shape* shape, const float* logits, const int3
     uint16_t* x_perm = at<uint16_t>(ws, L.x_perm);
     uint16_t* h = at<uint16_t>(ws, L.h);
     uint16_t* y_perm = at<uint16_t>(ws, L.y_perm);
-    if ((r = do_dispatch(s, x, ids, at<int32_t>(ws, L.counts), offsets, dest, at<int32_t>(ws, L.sorted_pair), x_perm,
-                         ws, st)) != MOE_OK)
+    if (small) {
+        if ((r = from_cuda(launch_small_dispatch(s, logits, ids_in, at<int32_t>(ws, L.ids), at<float>(ws, L.w), x,
+                                                 at<int32_t>(ws, L.counts), offsets, dest,
+                                                 at<int32_t>(ws, L.sorted_pair), x_perm, at<WsHeader>(ws, 0), st))) !=
+            MOE_OK)
+            return r;
+    } else if ((r = do_dispatch(s, x, ids, at<int32_t>(ws, L.counts), offsets, dest, at<int32_t>(ws, L.sorted_pair),
+                                x_perm, ws, st)) != MOE_OK) {
         return r;
+    }
     if ((r = do_up_fp8(s, x_perm, offsets, w13, w13_scale, h, ws, st)) != MOE_OK) return r;
     if ((r = do_down_fp8(s, h, offsets, w2, w2_scale, y_perm, ws, st)) != MOE_OK) return r;
     return do_combine(s, y_perm, dest, w, nullptr, residual, out, st);

@@ -314,6 +314,13 @@ cudaError_t launch_count(const moe_shape& s, const int32_t* ids, int32_t* counts
 cudaError_t launch_scatter(const moe_shape& s, const uint16_t* x, const int32_t* ids,
                            const int32_t* offsets, const int32_t* rank, int32_t* dest,
                            int32_t* sorted_pair, uint16_t* x_perm, WsHeader* hdr, cudaStream_t st);
+// Route (when logits is not null; else take ids_in), count and scatter in one
+// kernel for batches of at most kSmallDispatchTokens tokens; results bitwise
+// those of launch_route + launch_count + launch_scatter.
+constexpr int kSmallDispatchTokens = 16;
+cudaError_t launch_small_dispatch(const moe_shape& s, const float* logits, const int32_t* ids_in, int32_t* ids_out,
+                                  float* w_out, const uint16_t* x, int32_t* counts, int32_t* offsets, int32_t* dest,
+                                  int32_t* sorted_pair, uint16_t* x_perm, WsHeader* hdr, cudaStream_t st);
 cudaError_t launch_combine(const moe_shape& s, const uint16_t* y_perm, const int32_t* dest,
                            const float* w, const uint16_t* y_shared, const uint16_t* residual, uint16_t* out,
                            cudaStream_t st);

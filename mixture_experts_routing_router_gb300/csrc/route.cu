@@ -12,18 +12,14 @@
 // the softmax over the k selected logits (the full softmax renormalised over
 // the selection), computed in FP32 with the max subtracted.
 #include "common.cuh"
+#include "route_warp.cuh"
 
 #include <climits>
 
 namespace moe {
 namespace {
 
-__device__ __forceinline__ bool better(float av, int ai, float bv, int bi) {
-    // a ranks before b; bi == INT_MAX marks "nothing yet"
-    return bi == INT_MAX || av > bv || (av == bv && ai < bi);
-}
-
-// EPL = logits per lane (E <= 32 * EPL); lane l holds experts l, l+32, ...
+// k rounds of register argmax per token: see route_warp.cuh.
 template <int EPL>
 __global__ void __launch_bounds__(256)
 route_kernel(int T, int E, int k, const float* __restrict__ logits, int32_t* __restrict__ ids,
@@ -34,50 +30,13 @@ route_kernel(int T, int E, int k, const float* __restrict__ logits, int32_t* __r
     const int gwarp = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
     const int nwarps = (int)((gridDim.x * blockDim.x) >> 5);
     for (int t = gwarp; t < T; t += nwarps) {
-        const float* row = logits + (size_t)t * E;
-        float v[EPL];
-        uint32_t taken = 0;   // bit i: slot i already selected or past E
-        bool bad = false;
-#pragma unroll
-        for (int i = 0; i < EPL; ++i) {
-            const int e = lane + 32 * i;
-            float x = -INFINITY;
-            if (e < E) {
-                x = __ldg(row + e);
-                if (!isfinite(x)) { bad = true; x = -INFINITY; }
-            } else {
-                taken |= 1u << i;
-            }
-            v[i] = x;
-        }
-        if (__any_sync(0xffffffffu, bad) && lane == 0) raise_status(hdr, MOE_ERR_NONFINITE);
-
-        float sel_v = 0.f, m = 0.f;
-        int sel_i = 0;
-        for (int j = 0; j < k; ++j) {
-            float bv = 0.f;
-            int bi = INT_MAX;
-#pragma unroll
-            for (int i = 0; i < EPL; ++i)
-                if (!((taken >> i) & 1u) && better(v[i], lane + 32 * i, bv, bi)) { bv = v[i]; bi = lane + 32 * i; }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-                const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-                if (oi != INT_MAX && better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
-            }
-            // k <= E, so a winner always exists: every lane holds the same (bv, bi)
-            if (lane == (bi & 31)) taken |= 1u << (bi >> 5);
-            if (j == 0) m = bv;
-            if (lane == j) { sel_v = bv; sel_i = bi; }
-        }
-        const float ex = (lane < k) ? expf(sel_v - m) : 0.f;
-        float z = ex;
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+        int sel_i;
+        float sel_w;
+        if (route_token_softmax<EPL>(logits + (size_t)t * E, E, k, lane, sel_i, sel_w) && lane == 0)
+            raise_status(hdr, MOE_ERR_NONFINITE);
         if (lane < k) {
             ids[(size_t)t * k + lane] = sel_i;
-            w[(size_t)t * k + lane] = ex / z;
+            w[(size_t)t * k + lane] = sel_w;
         }
     }
 }
@@ -129,7 +88,7 @@ route_sigmoid_kernel(int T, int E, int k, const float* __restrict__ logits, cons
             int bi = INT_MAX;
 #pragma unroll
             for (int i = 0; i < EPL; ++i)
-                if (!((taken >> i) & 1u) && better(key[i], lane + 32 * i, bv, bi)) {
+                if (!((taken >> i) & 1u) && route_better(key[i], lane + 32 * i, bv, bi)) {
                     bv = key[i]; bs = sc[i]; bi = lane + 32 * i;
                 }
 #pragma unroll
@@ -137,7 +96,7 @@ route_sigmoid_kernel(int T, int E, int k, const float* __restrict__ logits, cons
                 const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
                 const float os = __shfl_xor_sync(0xffffffffu, bs, off);
                 const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-                if (oi != INT_MAX && better(ov, oi, bv, bi)) { bv = ov; bs = os; bi = oi; }
+                if (oi != INT_MAX && route_better(ov, oi, bv, bi)) { bv = ov; bs = os; bi = oi; }
             }
             if (lane == (bi & 31)) taken |= 1u << (bi >> 5);
             if (lane == j) { sel_s = bs; sel_i = bi; }

@@ -157,3 +157,36 @@ def test_layer_with_residual():
                 residual=res)
     assert N.moe_status_read(ws) == N.MOE_OK
     assert_close(bits(out), ref["out"], "layer + residual")
+
+
+def test_layer_error_statuses_small_batch():
+    """The same device errors at 8 tokens, where routing, counting and the
+    scatter run as one fused kernel: non-finite logits, invalid preselected
+    routes, and a capacity overflow that moves no payload."""
+    wl = synth.Workload("small_err", 8, 64, 16, 2, 64)
+    g = inputs(wl, seed=6)
+    shape = N.shape_of(wl)
+    ws = N.workspace(shape, dev())
+    out = torch.empty(wl.tokens, wl.hidden, dtype=torch.bfloat16, device=dev())
+    lg = g["logits"].clone()
+    lg[2, 5] = float("inf")
+    N.moe_layer(shape, lg, None, None, g["x"], g["w13"], g["w2"], None, None, out, ws)
+    assert N.moe_status_read(ws) == N.MOE_ERR_NONFINITE
+    ids = torch.zeros(wl.tokens, wl.top_k, dtype=torch.int32, device=dev())
+    ids[:, 1] = 1
+    w = torch.full((wl.tokens, wl.top_k), 0.5, device=dev())
+    for bad in (-1, 16, 0):                         # negative, wide, duplicate of slot 0
+        ids2 = ids.clone()
+        ids2[3, 1] = bad
+        N.moe_layer(shape, None, ids2, w, g["x"], g["w13"], g["w2"], None, None, out, ws)
+        assert N.moe_status_read(ws) == N.MOE_ERR_INVALID_ROUTE
+    shape.capacity = 4                              # 8 rows on experts 0 and 1
+    N.moe_layer(shape, None, ids, w, g["x"], g["w13"], g["w2"], None, None, out, ws)
+    assert N.moe_status_read(ws) == N.MOE_ERR_CAPACITY
+    shape.capacity = wl.tokens
+    N.moe_layer(shape, None, ids, w, g["x"], g["w13"], g["w2"], None, None, out, ws)
+    assert N.moe_status_read(ws) == N.MOE_OK
+    # a valid call afterwards matches the oracle
+    ref = oracle.layer(bits(g["x"]), bits(g["w13"]), bits(g["w2"]), wl.act, wl.top_k, wl.cap,
+                       ids_in=ids.cpu().numpy(), w_in=w.cpu().numpy())
+    assert_close(bits(out), ref["out"], "small batch after errors")
