@@ -289,9 +289,11 @@ def run_native(args, wl, world, rank, local):
     T, H, E, k, I = wl.tokens, wl.hidden, wl.experts, wl.top_k, wl.inter
     R = T * k
     out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
-    # route, count (+ clearing its look-back state when R > 1024 pairs), scatter,
-    # up, down, combine (+ the shared experts' up and down)
-    kernels_per_layer = 6 + (1 if R > 1024 else 0) + (2 if wl.shared else 0)
+    # route, count (+ clearing its look-back state when R > 1024 pairs), scatter
+    # -- one fused kernel for batches of at most 16 tokens --, up, down, combine
+    # (+ the shared experts' up and down)
+    dispatch_kernels = 1 if T <= 16 else 3 + (1 if R > 1024 else 0)
+    kernels_per_layer = dispatch_kernels + 3 + (2 if wl.shared else 0)
 
     def layer_on(lg_d, x_d, out_d):
         if fp8:
