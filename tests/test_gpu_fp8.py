@@ -177,3 +177,31 @@ def test_fp8_every_finite_code_decodes_exactly():
     neg_zero = codes[0].T == 0x80
     assert np.array_equal(got[~neg_zero], want_bits[~neg_zero]), int((got != want_bits)[~neg_zero].sum())
     assert np.all(got[neg_zero] == 0)
+
+
+def random_fp8_workloads(n, seed):
+    """Seeded small shapes for the FP8 entry points: hidden and intermediate
+    multiples of 16 (K tails included), 1..100 tokens, both activations."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        E = int(rng.integers(1, 41))
+        k = int(rng.integers(1, min(E, 16) + 1))
+        T = int(rng.choice([1, 5, 16, 40, 100]))
+        H = int(16 * rng.integers(1, 25))
+        I = int(16 * rng.integers(1, 25))
+        out.append(synth.Workload(f"fp8rand{i}", T, H, E, k, I, act=int(rng.integers(0, 2))))
+    return out
+
+
+@pytest.mark.parametrize("wl", random_fp8_workloads(6, 2027),
+                         ids=lambda w: f"{w.name}-T{w.tokens}H{w.hidden}E{w.experts}k{w.top_k}I{w.inter}a{w.act}")
+def test_fp8_layer_random_shapes(wl):
+    g, q = fp8_inputs(wl, seed=98)
+    ref = oracle_fp8_layer(wl, g, q)
+    shape = N.shape_of(wl)
+    ws = N.workspace(shape, dev())
+    out = torch.empty(wl.tokens, wl.hidden, dtype=torch.bfloat16, device=dev())
+    N.moe_layer_fp8(shape, g["logits"], None, None, g["x"], q["w13"], q["s13"], q["w2"], q["s2"], out, ws)
+    assert N.moe_status_read(ws) == N.MOE_OK
+    assert_close(bits(out), ref["out"], f"{wl.name} fp8 layer")

@@ -190,3 +190,42 @@ def test_layer_error_statuses_small_batch():
     ref = oracle.layer(bits(g["x"]), bits(g["w13"]), bits(g["w2"]), wl.act, wl.top_k, wl.cap,
                        ids_in=ids.cpu().numpy(), w_in=w.cpu().numpy())
     assert_close(bits(out), ref["out"], "small batch after errors")
+
+
+def random_workloads(n, seed):
+    """Seeded small shapes across the kernels' paths: 1..300 tokens (fused,
+    single-CTA and CTA-pair dispatch / GEMM paths), hidden and intermediate
+    any multiple of 8, 1..64 experts, top-k up to min(E, 32), both
+    activations, with and without shared experts."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        E = int(rng.integers(1, 65))
+        k = int(rng.integers(1, min(E, 32) + 1))
+        T = int(rng.choice([1, 3, 16, 17, 64, 65, 150, 300]))
+        H = int(8 * rng.integers(1, 41))
+        I = int(8 * rng.integers(1, 41))
+        act = int(rng.integers(0, 2))
+        S = int(rng.choice([0, 0, 1, 2]))
+        Is = int(8 * rng.integers(1, 21)) if S else 0
+        out.append(synth.Workload(f"rand{i}", T, H, E, k, I, act=act, shared=S, shared_inter=Is))
+    # and two shapes with 256+ rows per expert (the CTA-pair GEMM with swapped tails)
+    out.append(synth.Workload(f"rand{n}", 300, 136, 2, 2, 120, act=1, shared=1, shared_inter=40))
+    out.append(synth.Workload(f"rand{n + 1}", 300, 264, 3, 1, 200, act=0))
+    return out
+
+
+@pytest.mark.parametrize("wl", random_workloads(12, 2026), ids=lambda w: f"{w.name}-T{w.tokens}H{w.hidden}E{w.experts}k{w.top_k}I{w.inter}a{w.act}S{w.shared}")
+def test_layer_random_shapes(wl):
+    g = inputs(wl, unit_scale=True, seed=97)
+    res = synth.normal((wl.tokens, wl.hidden), 1.0, 97, "residual", dev())
+    kw = dict(ws13=bits(g["ws13"]), ws2=bits(g["ws2"])) if wl.shared else {}
+    ref = oracle.layer(bits(g["x"]), bits(g["w13"]), bits(g["w2"]), wl.act, wl.top_k, wl.cap,
+                       logits=g["logits"].cpu().numpy(), residual=bits(res), **kw)
+    shape = N.shape_of(wl)
+    ws = N.workspace(shape, dev())
+    out = torch.empty(wl.tokens, wl.hidden, dtype=torch.bfloat16, device=dev())
+    N.moe_layer(shape, g["logits"], None, None, g["x"], g["w13"], g["w2"], g.get("ws13"), g.get("ws2"), out, ws,
+                residual=res)
+    assert N.moe_status_read(ws) == N.MOE_OK
+    assert_close(bits(out), ref["out"], f"{wl.name} layer")
