@@ -98,6 +98,12 @@ def _load():
             lib.oracle_expert_ffn_fp8.argtypes = [i, i, i, i] + [P] * 8
             lib.oracle_layer_fp8.restype = i
             lib.oracle_layer_fp8.argtypes = [i] * 7 + [P] * 19
+            lib.oracle_fp4_e2m1_decode.restype = None
+            lib.oracle_fp4_e2m1_decode.argtypes = [i, P, P]
+            lib.oracle_expert_ffn_nvfp4.restype = None
+            lib.oracle_expert_ffn_nvfp4.argtypes = [i, i, i, i] + [P] * 10
+            lib.oracle_layer_nvfp4.restype = i
+            lib.oracle_layer_nvfp4.argtypes = [i] * 7 + [P] * 21
             _lib = lib
     return _lib
 
@@ -335,5 +341,63 @@ def layer_fp8(x, w13, s13, w2, s2, act, k, capacity, logits=None, ids_in=None, w
                                   _p(w2), _p(s2), _p(res), _p(o["ids"]), _p(o["w"]), _p(o["counts"]),
                                   _p(o["offsets"]), _p(o["dest"]), _p(o["sorted_pair"]), _p(o["x_perm"]),
                                   _p(o["h"]), _p(o["y_perm"]), _p(o["out"]))
+    o["status"] = st
+    return o
+
+
+# ---- NVFP4 expert weights ---------------------------------------------------
+def fp4_e2m1_decode(codes):
+    """E2M1 codes (uint8, low 4 bits) -> float64 values."""
+    c = _c(codes, np.uint8)
+    out = np.zeros(c.shape, np.float64)
+    _load().oracle_fp4_e2m1_decode(int(c.size), _p(c), _p(out))
+    return out
+
+
+def expert_ffn_nvfp4(x_perm, offsets, w13, b13, s13, w2, b2, s2, act):
+    """Routed experts with NVFP4 weights: w13 uint8 [E, up, H/2] (two E2M1 per
+    byte, low nibble first), b13 uint8 [E, up, 16*ceil(H/256)] E4M3 block
+    scales (byte j scales elements 16j..16j+15; the rest is padding), s13
+    float32 [E, up] row scales; w2 [E, H, I/2], b2 [E, H, 16*ceil(I/256)],
+    s2 [E, H].  -> (h [R, I], y_perm [R, H]) as BF16 bits."""
+    x_perm = _c(x_perm, np.uint16)
+    offsets = _c(offsets, np.int32)
+    w13, b13, w2, b2 = (_c(a, np.uint8) for a in (w13, b13, w2, b2))
+    s13 = _c(s13, np.float32)
+    s2 = _c(s2, np.float32)
+    E, H, I2 = w2.shape
+    I = 2 * I2
+    R = x_perm.shape[0]
+    h = np.zeros((R, I), np.uint16)
+    y = np.zeros((R, H), np.uint16)
+    _load().oracle_expert_ffn_nvfp4(H, E, I, act, _p(x_perm), _p(offsets), _p(w13), _p(b13), _p(s13), _p(w2),
+                                    _p(b2), _p(s2), _p(h), _p(y))
+    return h, y
+
+
+def layer_nvfp4(x, w13, b13, s13, w2, b2, s2, act, k, capacity, logits=None, ids_in=None, w_in=None,
+                residual=None):
+    """The whole layer with NVFP4 expert weights (no shared experts)."""
+    x = _c(x, np.uint16)
+    w13, b13, w2, b2 = (_c(a, np.uint8) for a in (w13, b13, w2, b2))
+    s13 = _c(s13, np.float32)
+    s2 = _c(s2, np.float32)
+    T, H = x.shape
+    E, _, I2 = w2.shape
+    I = 2 * I2
+    R = T * k
+    o = dict(ids=np.zeros((T, k), np.int32), w=np.zeros((T, k), np.float32),
+             counts=np.zeros(E, np.int32), offsets=np.zeros(E + 1, np.int32),
+             dest=np.full(R, -7, np.int32), sorted_pair=np.full(R, -7, np.int32),
+             x_perm=np.zeros((R, H), np.uint16), h=np.zeros((R, I), np.uint16),
+             y_perm=np.zeros((R, H), np.uint16), out=np.zeros((T, H), np.uint16))
+    lg = None if logits is None else _c(logits, np.float32)
+    ii = None if ids_in is None else _c(ids_in, np.int32)
+    wi = None if w_in is None else _c(w_in, np.float32)
+    res = None if residual is None else _c(residual, np.uint16)
+    st = _load().oracle_layer_nvfp4(T, H, E, k, I, act, capacity, _p(lg), _p(ii), _p(wi), _p(x), _p(w13),
+                                    _p(b13), _p(s13), _p(w2), _p(b2), _p(s2), _p(res), _p(o["ids"]), _p(o["w"]),
+                                    _p(o["counts"]), _p(o["offsets"]), _p(o["dest"]), _p(o["sorted_pair"]),
+                                    _p(o["x_perm"]), _p(o["h"]), _p(o["y_perm"]), _p(o["out"]))
     o["status"] = st
     return o

@@ -27,6 +27,17 @@
 //          E4M3 follows the OCP 8-bit floating point definition: 1 sign bit, 4
 //          exponent bits with bias 7, 3 mantissa bits, subnormals at exponent
 //          field 0, no infinities, and the two codes S.1111.111 are NaN.
+//  [NVFP4] [ORT]'s NVFP4 weights (section "Current source and CI repair":
+//          the NVFP4 guard and the BF16/FP16 NVFP4 scale-before-cast cases).
+//          The page names the format without defining it; this is the standard
+//          NVFP4 layout: E2M1 elements (1 sign bit, 2 exponent bits with bias
+//          1, 1 mantissa bit; magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6), two per
+//          byte with the lower K index in the low nibble, one E4M3 block scale
+//          per 16 consecutive elements of a row, and one FP32 scale per row
+//          (a per-tensor scale is the case of equal row scales).  An element's value is e2m1 * block scale (formed first: the
+//          scale is applied before the cast), and the row scale multiplies the
+//          dot product.  A row's block scales sit at bytes 0 .. K/16 - 1 of a
+//          16 * ceil(K / 256)-byte row (the rest is padding, never read).
 //
 // Precision: every floating-point sum is taken in double (FP64) in the natural
 // index order; BF16 values are produced by one round-to-nearest-even from the
@@ -385,6 +396,72 @@ void oracle_expert_ffn_fp8(int H, int E, int I, int act, const uint16_t* x_perm,
     }
 }
 
+// ---- quantized (NVFP4) expert weights ---------------------------------------
+// [NVFP4] E2M1 code (4 bits) -> value, exactly.
+double fp4_e2m1_to_double(uint8_t c) {
+    const int sign = (c >> 3) & 1, e = (c >> 1) & 3, m = c & 1;
+    const double mag = (e == 0) ? 0.5 * m : std::ldexp(1.0 + 0.5 * m, e - 1);
+    return sign ? -mag : mag;
+}
+
+void oracle_fp4_e2m1_decode(int n, const uint8_t* codes, double* out) {
+    for (int i = 0; i < n; ++i) out[i] = fp4_e2m1_to_double(codes[i]);
+}
+
+// Element c of a packed NVFP4 row (two codes per byte, low nibble first),
+// times its block's E4M3 scale.
+double nvfp4_element(const uint8_t* row, const uint8_t* bscale_row, int c) {
+    const uint8_t b = row[c >> 1];
+    const uint8_t code = (c & 1) ? (b >> 4) : (b & 15);
+    return fp4_e2m1_to_double(code) * fp8_e4m3_to_double(bscale_row[c >> 4]);
+}
+
+// Bytes per row of block scales for K elements: 16 per 256 (padded).
+size_t nvfp4_bscale_stride(int K) { return 16 * (size_t)((K + 255) / 256); }
+
+// [NVFP4] Routed experts with NVFP4 weights: W13 codes [E][up][H/2] with block
+// scales [E][up][16*ceil(H/256)] and row scales [E][up]; W2 codes [E][H][I/2],
+// block scales [E][H][16*ceil(I/256)], row scales [E][H].  Dot products as for
+// FP8, with the element value e2m1 * block scale.
+void oracle_expert_ffn_nvfp4(int H, int E, int I, int act, const uint16_t* x_perm, const int32_t* offsets,
+                             const uint8_t* w13, const uint8_t* b13, const float* s13,
+                             const uint8_t* w2, const uint8_t* b2, const float* s2,
+                             uint16_t* h, uint16_t* y_perm) {
+    const size_t up = (act == ACT_SWIGLU) ? 2 * (size_t)I : (size_t)I;
+    for (int e = 0; e < E; ++e) {
+        for (int r = offsets[e]; r < offsets[e + 1]; ++r) {
+            const uint16_t* x_row = x_perm + (size_t)r * H;
+            uint16_t* h_row = h + (size_t)r * I;
+            auto dot = [&](size_t wr) {
+                const size_t row = (size_t)e * up + wr;
+                const uint8_t* codes = w13 + row * (H / 2);
+                const uint8_t* bs = b13 + row * nvfp4_bscale_stride(H);
+                double acc = 0.0;
+                for (int c = 0; c < H; ++c) acc += bf16_to_double(x_row[c]) * nvfp4_element(codes, bs, c);
+                return acc * (double)s13[row];
+            };
+            for (int n = 0; n < I; ++n) {
+                if (act == ACT_SWIGLU) {
+                    const double gv = dot((size_t)n), uv = dot((size_t)(I + n));
+                    h_row[n] = double_to_bf16(silu(gv) * uv);
+                } else {
+                    const double a = dot((size_t)n);
+                    const double ra = a > 0.0 ? a : 0.0;
+                    h_row[n] = double_to_bf16(ra * ra);
+                }
+            }
+            for (int c = 0; c < H; ++c) {
+                const size_t row = (size_t)e * H + c;
+                const uint8_t* codes = w2 + row * (I / 2);
+                const uint8_t* bs = b2 + row * nvfp4_bscale_stride(I);
+                double acc = 0.0;
+                for (int n = 0; n < I; ++n) acc += bf16_to_double(h_row[n]) * nvfp4_element(codes, bs, n);
+                y_perm[(size_t)r * H + c] = double_to_bf16(acc * (double)s2[row]);
+            }
+        }
+    }
+}
+
 // ---- combine ------------------------------------------------------------
 // [MI300] MOE_COMBINE_RESIDUAL (the weighted combine with the block's residual
 // add) and [ORT] "FP32 final routing/reduction": for token t,
@@ -465,6 +542,30 @@ int oracle_layer_fp8(int T, int H, int E, int k, int I, int act, int capacity,
                              sorted_pair, x_perm);
     if (st == ST_CAPACITY) return st;
     oracle_expert_ffn_fp8(H, E, I, act, x_perm, offsets, w13, s13, w2, s2, h, y_perm);
+    oracle_combine(T, k, H, y_perm, dest, w, nullptr, residual, out);
+    return st;
+}
+
+// The layer with NVFP4 expert weights (no shared experts).
+int oracle_layer_nvfp4(int T, int H, int E, int k, int I, int act, int capacity,
+                       const float* logits, const int32_t* ids_in, const float* w_in,
+                       const uint16_t* x, const uint8_t* w13, const uint8_t* b13, const float* s13,
+                       const uint8_t* w2, const uint8_t* b2, const float* s2, const uint16_t* residual,
+                       int32_t* ids, float* w, int32_t* counts, int32_t* offsets,
+                       int32_t* dest, int32_t* sorted_pair, uint16_t* x_perm,
+                       uint16_t* h, uint16_t* y_perm, uint16_t* out) {
+    const size_t R = (size_t)T * k;
+    if (logits) {
+        int st = oracle_route(T, E, k, logits, ids, w);
+        if (st != ST_OK) return st;
+    } else {
+        std::memcpy(ids, ids_in, R * sizeof(int32_t));
+        std::memcpy(w, w_in, R * sizeof(float));
+    }
+    int st = oracle_dispatch(T, E, k, H, capacity, ids, x, counts, offsets, dest,
+                             sorted_pair, x_perm);
+    if (st == ST_CAPACITY) return st;
+    oracle_expert_ffn_nvfp4(H, E, I, act, x_perm, offsets, w13, b13, s13, w2, b2, s2, h, y_perm);
     oracle_combine(T, k, H, y_perm, dest, w, nullptr, residual, out);
     return st;
 }

@@ -42,6 +42,15 @@ MUTANTS = {
     "fp8_nan_code_finite": ("if (e == 15 && m == 7) return std::nan(\"\");", "if (false) return std::nan(\"\");"),
     "fp8_up_scale_from_first_row": ("return acc * (double)s13_e[wr];", "return acc * (double)s13_e[0];"),
     "fp8_down_scale_from_first_row": ("double_to_bf16(acc * (double)s2_e[c])", "double_to_bf16(acc * (double)s2_e[0])"),
+    "fp4_nibbles_swapped": ("const uint8_t code = (c & 1) ? (b >> 4) : (b & 15);",
+                            "const uint8_t code = (c & 1) ? (b & 15) : (b >> 4);"),
+    "fp4_exponent_bias_0": ("std::ldexp(1.0 + 0.5 * m, e - 1)", "std::ldexp(1.0 + 0.5 * m, e)"),
+    "fp4_subnormal_read_as_normal": ("(e == 0) ? 0.5 * m :", "(e == 0) ? std::ldexp(1.0 + 0.5 * m, -1) :"),
+    "nvfp4_block_of_8": ("fp8_e4m3_to_double(bscale_row[c >> 4])", "fp8_e4m3_to_double(bscale_row[c >> 3])"),
+    "nvfp4_unpadded_scale_rows": ("return 16 * (size_t)((K + 255) / 256);", "return (size_t)(K / 16);"),
+    "nvfp4_up_row_scale_dropped": ("return acc * (double)s13[row];", "return acc;"),
+    "nvfp4_down_row_scale_from_first_row": ("double_to_bf16(acc * (double)s2[row])",
+                                            "double_to_bf16(acc * (double)s2[(size_t)e * H])"),
     "first_slot_dropped_in_combine": ("for (int j = 0; j < k; ++j) {\n            if (dest_t[j] < 0) continue;",
                                       "for (int j = 1; j < k; ++j) {\n            if (dest_t[j] < 0) continue;"),
 }
@@ -77,6 +86,10 @@ PINS = [
     (P.test_fp8_ffn_equals_bf16_path_on_exact_weights, dict(act=0)),
     (P.test_fp8_ffn_equals_bf16_path_on_exact_weights, dict(act=1)),
     (P.test_fp8_layer_equals_bf16_layer_on_exact_weights, {}),
+    (P.test_fp4_decode_values, {}),
+    (P.test_nvfp4_ffn_equals_bf16_path_on_exact_weights, dict(act=0, H=48, I=64)),
+    (P.test_nvfp4_ffn_equals_bf16_path_on_exact_weights, dict(act=1, H=288, I=32)),
+    (P.test_nvfp4_layer_equals_bf16_layer_on_exact_weights, {}),
 ]
 
 

@@ -557,3 +557,76 @@ def test_fp8_layer_equals_bf16_layer_on_exact_weights(oracle_mod):
     assert o8["status"] == ob["status"] == 0
     for key in ("ids", "offsets", "dest", "x_perm", "h", "y_perm", "out"):
         assert np.array_equal(o8[key], ob[key]), key
+
+
+# --------------------------------------------------------------------------
+# NVFP4 expert weights (E2M1 codes, an E4M3 scale per 16 elements, an FP32
+# scale per row)
+# --------------------------------------------------------------------------
+# The E2M1 element values as the OCP microscaling format lists them, code
+# 0..7 (positive) and 8..15 (the same magnitudes, negative).
+E2M1_VALUES = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0], np.float64)
+
+
+def test_fp4_decode_values(oracle_mod):
+    v = oracle_mod.fp4_e2m1_decode(np.arange(16, dtype=np.uint8))
+    assert np.array_equal(v[:8], E2M1_VALUES)
+    assert np.array_equal(v[8:], -E2M1_VALUES)
+    assert math.copysign(1.0, v[8]) < 0                              # code 8 is -0
+
+
+def nvfp4_bscale_bytes(K):
+    return 16 * ((K + 255) // 256)
+
+
+def nvfp4_exact_case(rng, E, rows, K):
+    """Random E2M1 codes, finite E4M3 block scales (subnormals included) and
+    power-of-two row scales, with the block-scale padding filled with NaN codes
+    (never read).  -> (codes [E, rows, K/2], bscale [E, rows, 16*ceil(K/256)],
+    rscale [E, rows], the dequantized weights as BF16 bits [E, rows, K]); every
+    dequantized weight e2m1 * block scale * row scale is exact in BF16, and
+    it is formed here from the OCP value list and torch's E4M3 decode."""
+    nib = rng.integers(0, 16, (E, rows, K))
+    codes = (nib[..., 0::2] | (nib[..., 1::2] << 4)).astype(np.uint8)
+    sb = rng.integers(0, 0x7F, (E, rows, K // 16)).astype(np.uint8)          # 0x00..0x7E: finite, >= 0
+    sb[..., 0] = 0x01                                                        # a subnormal scale in every row
+    bscale = np.full((E, rows, nvfp4_bscale_bytes(K)), 0x7F, np.uint8)
+    bscale[..., :K // 16] = sb
+    rscale = (2.0 ** rng.integers(-3, 4, (E, rows))).astype(np.float32)
+    elem = np.where(nib >= 8, -1.0, 1.0) * E2M1_VALUES[nib & 7]
+    sbv = torch.from_numpy(sb).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    w = elem * np.repeat(sbv, 16, axis=-1) * rscale[..., None].astype(np.float64)
+    return codes, bscale, rscale, bf16_of_exact(w)
+
+
+@pytest.mark.parametrize("act,H,I", [(0, 48, 64), (1, 288, 32), (0, 512, 272)])
+def test_nvfp4_ffn_equals_bf16_path_on_exact_weights(oracle_mod, act, H, I):
+    """K not a multiple of 256 (padded block-scale rows), K above 256 (two
+    16-byte scale groups per row), both activations."""
+    rng = np.random.default_rng(61 + act + H)
+    E, R = 3, 20
+    up = 2 * I if act == 0 else I
+    c13, b13, s13, w13 = nvfp4_exact_case(rng, E, up, H)
+    c2, b2, s2, w2 = nvfp4_exact_case(rng, E, H, I)
+    x_perm = rand_bf16(rng, (R, H))
+    offsets = np.array([0, 6, 6, R], np.int32)
+    h4, y4 = oracle_mod.expert_ffn_nvfp4(x_perm, offsets, c13, b13, s13, c2, b2, s2, act)
+    hb, yb, _, _ = oracle_mod.expert_ffn(x_perm, offsets, w13, w2, act)
+    assert np.array_equal(h4, hb)
+    assert np.array_equal(y4, yb)
+    assert np.mean(h4 != 0) > 0.3
+
+
+def test_nvfp4_layer_equals_bf16_layer_on_exact_weights(oracle_mod):
+    rng = np.random.default_rng(71)
+    T, E, k, H, I = 24, 6, 2, 32, 48
+    c13, b13, s13, w13 = nvfp4_exact_case(rng, E, 2 * I, H)
+    c2, b2, s2, w2 = nvfp4_exact_case(rng, E, H, I)
+    x = rand_bf16(rng, (T, H))
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    res = rand_bf16(rng, (T, H))
+    o4 = oracle_mod.layer_nvfp4(x, c13, b13, s13, c2, b2, s2, 0, k, T, logits=logits, residual=res)
+    ob = oracle_mod.layer(x, w13, w2, 0, k, T, logits=logits, residual=res)
+    assert o4["status"] == ob["status"] == 0
+    for key in ("ids", "offsets", "dest", "x_perm", "h", "y_perm", "out"):
+        assert np.array_equal(o4[key], ob[key]), key
