@@ -43,9 +43,19 @@ def describe(wl):
             + ", W ~ N(0,0.02), x ~ N(0,1), seed 0")
 
 
-def algorithmic(wl, counts=None, weight_bytes=2):
-    """Bytes / FLOPs the method itself must move or compute (no padding).
-    weight_bytes: 2 for BF16 weights, 1 for FP8 (plus a 4-byte scale per row)."""
+def weight_row_bytes(K, wfmt="bf16"):
+    """Bytes of one expert weight row of K elements: BF16 2 per element; FP8 1
+    per element + a 4-byte row scale; NVFP4 half a byte per element + one
+    E4M3 block scale per 16 elements + a 4-byte row scale."""
+    if wfmt == "fp8":
+        return K + 4
+    if wfmt == "nvfp4":
+        return K // 2 + K // 16 + 4
+    return 2 * K
+
+
+def algorithmic(wl, counts=None, wfmt="bf16"):
+    """Bytes / FLOPs the method itself must move or compute (no padding)."""
     T, H, E, k, I = wl.tokens, wl.hidden, wl.experts, wl.top_k, wl.inter
     R = T * k
     up = wl.up
@@ -58,9 +68,8 @@ def algorithmic(wl, counts=None, weight_bytes=2):
     if counts is not None:
         nz = int((counts > 0).sum())
         d["nonempty_experts"] = nz
-        scales = 4 if weight_bytes == 1 else 0
-        d["up_bytes"] = nz * up * (H * weight_bytes + scales) + R * H * 2 + R * I * 2
-        d["down_bytes"] = nz * H * (I * weight_bytes + scales) + R * I * 2 + R * H * 2
+        d["up_bytes"] = nz * up * weight_row_bytes(H, wfmt) + R * H * 2 + R * I * 2
+        d["down_bytes"] = nz * H * weight_row_bytes(I, wfmt) + R * I * 2 + R * H * 2
     return d
 
 
@@ -73,13 +82,21 @@ def load_peaks():
     return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
 
 
-def up_kernel_name(wl, sms, fp8=False):
+WEIGHT_FORMATS = {
+    "bf16": "BF16",
+    "fp8": "FP8 E4M3 codes + one FP32 scale per weight row (quantized from the BF16 draws); BF16 activations and MMA",
+    "nvfp4": ("NVFP4: E2M1 codes + one E4M3 scale per 16 elements + one FP32 scale per weight row (quantized from "
+              "the BF16 draws); BF16 activations and MMA"),
+}
+
+
+def up_kernel_name(wl, sms, quant=False):
     """Which kernel the library runs for the up projection (the library's own
-    host rule: the small-row kernel for FP8 weights, or when a group holds at
-    most 64 rows and its items fit in two waves; the CTA-pair kernel when groups
-    average 256 rows)."""
+    host rule: the small-row kernel for quantized weights, or when a group
+    holds at most 64 rows and its items fit in two waves; the CTA-pair kernel
+    when groups average 256 rows)."""
     R = wl.tokens * wl.top_k
-    if fp8 or (wl.tokens <= 64 and min(wl.experts, R) * ((wl.inter + 127) // 128) <= 2 * sms):
+    if quant or (wl.tokens <= 64 and min(wl.experts, R) * ((wl.inter + 127) // 128) <= 2 * sms):
         return "decode_gemm_kernel (expert up projection)"
     if R // wl.experts >= 256:
         return "grouped_gemm_pair_kernel (expert up projection)"
@@ -279,11 +296,14 @@ def run_native(args, wl, world, rank, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     stream = torch.cuda.Stream(device=dev)
-    fp8 = args.weights == "fp8"
-    if fp8 and wl.shared:
-        raise SystemExit("FP8 expert weights: the workload has shared experts, which the FP8 entry points omit")
-    g = synth.make_inputs(wl, seed=rank, device=dev, weights=not fp8)
-    q = synth.make_fp8_weights(wl, seed=rank, device=dev) if fp8 else None
+    wfmt = args.weights
+    quant = wfmt != "bf16"
+    if quant and wl.shared:
+        raise SystemExit("quantized expert weights: the workload has shared experts, which the quantized entry "
+                         "points omit")
+    g = synth.make_inputs(wl, seed=rank, device=dev, weights=not quant)
+    q = (synth.make_fp8_weights(wl, seed=rank, device=dev) if wfmt == "fp8" else
+         synth.make_nvfp4_weights(wl, seed=rank, device=dev) if wfmt == "nvfp4" else None)
     shape = N.shape_of(wl)
     ws = N.workspace(shape, dev)
     T, H, E, k, I = wl.tokens, wl.hidden, wl.experts, wl.top_k, wl.inter
@@ -296,8 +316,11 @@ def run_native(args, wl, world, rank, local):
     kernels_per_layer = dispatch_kernels + 3 + (2 if wl.shared else 0)
 
     def layer_on(lg_d, x_d, out_d):
-        if fp8:
+        if wfmt == "fp8":
             N.moe_layer_fp8(shape, lg_d, None, None, x_d, q["w13"], q["s13"], q["w2"], q["s2"], out_d, ws, stream)
+        elif wfmt == "nvfp4":
+            N.moe_layer_nvfp4(shape, lg_d, None, None, x_d, q["w13"], q["b13"], q["s13"], q["w2"], q["b2"], q["s2"],
+                              out_d, ws, stream)
         else:
             N.moe_layer(shape, lg_d, None, None, x_d, g["w13"], g["w2"], g.get("ws13"), g.get("ws2"), out_d, ws,
                         stream)
@@ -313,7 +336,7 @@ def run_native(args, wl, world, rank, local):
     stream.synchronize()
     l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 * 2**20) or 126 * 2**20
     cnt0 = ws_counts(N, shape, g, ws, stream, dev)
-    touched = int((cnt0 > 0).sum()) * (wl.up * H + H * I) * (1 if fp8 else 2) + \
+    touched = int((cnt0 > 0).sum()) * (wl.up * weight_row_bytes(H, wfmt) + H * weight_row_bytes(I, wfmt)) + \
         wl.shared * (wl.shared_up * H + H * wl.shared_inter) * 2
     flush = not (g["x"].numel() * 2 > l2 and touched > 4 * l2)
     flush_buf = torch.empty(4 * l2, dtype=torch.uint8, device=dev) if flush else None
@@ -378,9 +401,13 @@ def run_native(args, wl, world, rank, local):
     stage_fns = [
         lambda: N.moe_route(shape, g["logits"], ids, w, ws, stream),
         lambda: N.moe_dispatch(shape, g["x"], ids, counts, offsets, dest, sp, x_perm, ws, stream),
-        (lambda: N.moe_expert_up_fp8(shape, x_perm, offsets, q["w13"], q["s13"], h, ws, stream)) if fp8 else
+        (lambda: N.moe_expert_up_fp8(shape, x_perm, offsets, q["w13"], q["s13"], h, ws, stream)) if wfmt == "fp8"
+        else (lambda: N.moe_expert_up_nvfp4(shape, x_perm, offsets, q["w13"], q["b13"], q["s13"], h, ws, stream))
+        if wfmt == "nvfp4" else
         (lambda: N.moe_expert_up(shape, x_perm, offsets, g["w13"], g["x"], g.get("ws13"), h, ws, stream)),
-        (lambda: N.moe_expert_down_fp8(shape, h, offsets, q["w2"], q["s2"], y_perm, ws, stream)) if fp8 else
+        (lambda: N.moe_expert_down_fp8(shape, h, offsets, q["w2"], q["s2"], y_perm, ws, stream)) if wfmt == "fp8"
+        else (lambda: N.moe_expert_down_nvfp4(shape, h, offsets, q["w2"], q["b2"], q["s2"], y_perm, ws, stream))
+        if wfmt == "nvfp4" else
         (lambda: N.moe_expert_down(shape, h, offsets, g["w2"], g.get("ws2"), y_perm, y_sh, ws, stream)),
         lambda: N.moe_combine(shape, y_perm, dest, w, y_sh, out, ws, stream),
     ]
@@ -433,7 +460,7 @@ def run_native(args, wl, world, rank, local):
     if st != N.MOE_OK:
         raise RuntimeError(f"device status {st} after stage timing")
     cnt = counts.cpu().numpy()
-    alg = algorithmic(wl, cnt, 1 if fp8 else 2)
+    alg = algorithmic(wl, cnt, wfmt)
 
     # ---- end to end through the C-ABI with host buffers -----------------------
     # Every step copies its inputs (x, logits) from pinned host memory, runs
@@ -531,7 +558,7 @@ def run_native(args, wl, world, rank, local):
     gemm_tflops = (alg["up_flops"] + alg["down_flops"]) / ((stage_ms["expert_up"] + stage_ms["expert_down"]) / 1e3) / 1e12
 
     cpu = None
-    if rank == 0 and not args.no_cpu_baseline and not fp8:     # the oracle sample is the BF16 layer
+    if rank == 0 and not args.no_cpu_baseline and not quant:   # the oracle sample is the BF16 layer
         import oracle
         oracle.build()
         rng = np.random.default_rng(0)
@@ -552,12 +579,11 @@ def run_native(args, wl, world, rank, local):
                               f"events)" if flush else
                               f"inputs larger than L2 (x {g['x'].numel() * 2 >> 20} MiB, touched weights "
                               f"{touched >> 20} MiB): no flush"),
-                       "expert_weights": ("FP8 E4M3 codes + one FP32 scale per weight row (quantized from the BF16 "
-                                          "draws); BF16 activations and MMA" if fp8 else "BF16")},
+                       "expert_weights": WEIGHT_FORMATS[wfmt]},
             "roofline": {"kernel": up_kernel_name(wl, torch.cuda.get_device_properties(dev).multi_processor_count,
-                                                  fp8),
+                                                  quant),
                          **roof,
-                         "traffic": ncu_traffic() if wl.name == WORKLOAD and not fp8 else None},
+                         "traffic": ncu_traffic() if wl.name == WORKLOAD and not quant else None},
             "expert_up_tflops": achieved,
             "dispatch_combine_gbs": dc_gbs, "dispatch_combine_hbm_frac": dc_gbs / peaks["hbm_gbs"],
             "gemm_tflops": gemm_tflops, "gemm_frac": gemm_tflops / peak,
@@ -579,8 +605,9 @@ def main():
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--cpu-tokens", type=int, default=24)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--weights", default="bf16", choices=["bf16", "fp8"],
-                    help="expert weight format (fp8: E4M3 codes with a scale per row, moe_layer_fp8)")
+    ap.add_argument("--weights", default="bf16", choices=["bf16", "fp8", "nvfp4"],
+                    help="expert weight format (fp8: E4M3 codes with a scale per row, moe_layer_fp8; nvfp4: E2M1 "
+                         "codes with E4M3 block scales and a scale per row, moe_layer_nvfp4)")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be at least 3")

@@ -219,7 +219,7 @@ MOE_API moe_status moe_layer(const moe_shape* shape, const float* logits, const 
  *   w13_scale device f32 [E, up]     one scale per weight row
  *   w2        device u8  [E, H, I]   E4M3 codes; w2_scale device f32 [E, H]
  * A weight is decode(code) * scale of its row; the kernels decode the codes to
- * BF16 in shared memory (exactly), multiply in BF16 with FP32 accumulation and
+ * BF16 in tensor memory (exactly), multiply in BF16 with FP32 accumulation and
  * apply the row scale to the accumulator:
  *   SwiGLU: h[r][n] = bf16( silu(g) * u ), g = (x_r . dec(W13[e][n])) * s13[e][n],
  *           u = (x_r . dec(W13[e][I+n])) * s13[e][I+n];  ReLU^2 likewise with one row;
@@ -241,6 +241,41 @@ MOE_API moe_status moe_layer_fp8(const moe_shape* shape, const float* logits, co
                                  const float* w13_scale, const uint8_t* w2, const float* w2_scale,
                                  const uint16_t* residual, uint16_t* out, void* ws, size_t ws_bytes,
                                  void* stream);
+
+/* Quantized expert weights: NVFP4 (ONNX Runtime PR #33963, section "Current
+ * source and CI repair": the NVFP4 guard and the BF16/FP16 NVFP4
+ * scale-before-cast cases; the page names the format, this is the standard
+ * NVFP4 layout).  Activations stay BF16; every weight row of K elements
+ * (K = H for w13, I for w2) is
+ *   codes  u8 [K/2]               E2M1 codes, two per byte, element 2j in the
+ *                                 low nibble of byte j (1 sign bit, 2 exponent
+ *                                 bits with bias 1, 1 mantissa bit: magnitudes
+ *                                 0, 0.5, 1, 1.5, 2, 3, 4, 6)
+ *   bscale u8 [16*ceil(K/256)]    byte j (j < K/16): the E4M3 scale of elements
+ *                                 16j..16j+15; the padding bytes are never read
+ *   scale  f32                    one scale per row
+ * so that weight[c] = e2m1(code c) * e4m3(bscale[c/16]) * scale:
+ *   w13 device u8 [E, up, H/2], w13_bscale device u8 [E, up, 16*ceil(H/256)],
+ *   w13_scale device f32 [E, up]; w2 device u8 [E, H, I/2],
+ *   w2_bscale device u8 [E, H, 16*ceil(I/256)], w2_scale device f32 [E, H].
+ * The kernels form e2m1 * block scale (exact in BF16: the scale is applied
+ * before the cast), multiply in BF16 with FP32 accumulation and apply the row
+ * scale to the accumulator, with the output formulas of the FP8 calls.  The
+ * E4M3 NaN codes are not valid block scales (decoded as +-480).
+ * Host errors: MOE_ERR_UNSUPPORTED when shape->shared > 0; MOE_ERR_INVALID_ARG
+ * when hidden or inter is not a multiple of 32 or a pointer is not 16-byte
+ * aligned.  The rest is as for the FP8 calls (small-row kernel at any size). */
+MOE_API moe_status moe_expert_up_nvfp4(const moe_shape* shape, const uint16_t* x_perm, const int32_t* offsets,
+                                       const uint8_t* w13, const uint8_t* w13_bscale, const float* w13_scale,
+                                       uint16_t* h, void* ws, size_t ws_bytes, void* stream);
+MOE_API moe_status moe_expert_down_nvfp4(const moe_shape* shape, const uint16_t* h, const int32_t* offsets,
+                                         const uint8_t* w2, const uint8_t* w2_bscale, const float* w2_scale,
+                                         uint16_t* y_perm, void* ws, size_t ws_bytes, void* stream);
+MOE_API moe_status moe_layer_nvfp4(const moe_shape* shape, const float* logits, const int32_t* ids_in,
+                                   const float* w_in, const uint16_t* x, const uint8_t* w13,
+                                   const uint8_t* w13_bscale, const float* w13_scale, const uint8_t* w2,
+                                   const uint8_t* w2_bscale, const float* w2_scale, const uint16_t* residual,
+                                   uint16_t* out, void* ws, size_t ws_bytes, void* stream);
 
 /* moe_dispatch for callers that cannot allocate device memory, and so cannot
  * provide the workspace the other calls take: code that runs where cudaMalloc

@@ -155,9 +155,12 @@ moe_status do_down(const moe_shape& s, const uint16_t* h, const int32_t* offsets
     return launch_grouped_gemm(q, hdr, st);
 }
 
-// FP8 E4M3 expert weights (no shared experts): one FP32 scale per weight row.
-moe_status do_up_fp8(const moe_shape& s, const uint16_t* x_perm, const int32_t* offsets, const uint8_t* w13,
-                     const float* s13, uint16_t* h, void* ws, cudaStream_t st) {
+// FP8 E4M3 or NVFP4 expert weights (no shared experts): one FP32 scale per
+// weight row; NVFP4 adds the E4M3 block scales (16 bytes per 256 elements of a row).
+size_t nvfp4_bscale_stride(int K) { return 16 * (size_t)((K + 255) / 256); }
+
+moe_status do_up_q(const moe_shape& s, const uint16_t* x_perm, const int32_t* offsets, const uint8_t* w13,
+                   const uint8_t* b13, const float* s13, int wfmt, uint16_t* h, void* ws, cudaStream_t st) {
     const long long R = (long long)s.tokens * s.top_k;
     GemmProblem g{};
     g.mode = s.act == MOE_ACT_SWIGLU ? kGemmSwiGLU : kGemmReLU2;
@@ -168,12 +171,13 @@ moe_status do_up_fp8(const moe_shape& s, const uint16_t* x_perm, const int32_t* 
     g.N = s.inter; g.b_group_rows = up_rows(s, s.inter); g.up_off = s.inter;
     g.out = h; g.ldo = s.inter; g.out_group_col = 0;
     g.max_group_rows = s.tokens;
-    g.wfmt = kWeightFp8E4M3; g.wscale = s13;
+    g.wfmt = wfmt; g.wscale = s13;
+    g.bscale = b13; g.bscale_stride = (long long)nvfp4_bscale_stride(s.hidden);
     return launch_grouped_gemm(g, at<WsHeader>(ws, 0), st);
 }
 
-moe_status do_down_fp8(const moe_shape& s, const uint16_t* h, const int32_t* offsets, const uint8_t* w2,
-                       const float* s2, uint16_t* y_perm, void* ws, cudaStream_t st) {
+moe_status do_down_q(const moe_shape& s, const uint16_t* h, const int32_t* offsets, const uint8_t* w2,
+                     const uint8_t* b2, const float* s2, int wfmt, uint16_t* y_perm, void* ws, cudaStream_t st) {
     const long long R = (long long)s.tokens * s.top_k;
     GemmProblem g{};
     g.mode = kGemmPlain;
@@ -184,19 +188,24 @@ moe_status do_down_fp8(const moe_shape& s, const uint16_t* h, const int32_t* off
     g.N = s.hidden; g.b_group_rows = s.hidden; g.up_off = 0;
     g.out = y_perm; g.ldo = s.hidden; g.out_group_col = 0;
     g.max_group_rows = s.tokens;
-    g.wfmt = kWeightFp8E4M3; g.wscale = s2;
+    g.wfmt = wfmt; g.wscale = s2;
+    g.bscale = b2; g.bscale_stride = (long long)nvfp4_bscale_stride(s.inter);
     return launch_grouped_gemm(g, at<WsHeader>(ws, 0), st);
 }
 
-// FP8 weight rows are TMA-loaded: their byte stride (H or I) must be a
-// multiple of 16; shared experts are not part of the FP8 entry points.
-moe_status check_fp8_shape(const moe_shape* s) {
+// Quantized weight rows are TMA-loaded: their byte stride (H or I for FP8,
+// half that for NVFP4) must be a multiple of 16; shared experts are not part
+// of the quantized entry points.
+moe_status check_quant_shape(const moe_shape* s, int wfmt) {
+    const char* name = wfmt == kWeightNvfp4 ? "NVFP4" : "FP8";
+    const int mult = wfmt == kWeightNvfp4 ? 32 : 16;
     if (s->shared > 0) {
-        set_error("FP8 expert weights: shared experts are not supported (shape.shared must be 0)");
+        set_error("%s expert weights: shared experts are not supported (shape.shared must be 0)", name);
         return MOE_ERR_UNSUPPORTED;
     }
-    if (s->hidden % 16 != 0 || s->inter % 16 != 0) {
-        set_error("FP8 expert weights: hidden and inter must be multiples of 16 (got %d, %d)", s->hidden, s->inter);
+    if (s->hidden % mult != 0 || s->inter % mult != 0) {
+        set_error("%s expert weights: hidden and inter must be multiples of %d (got %d, %d)", name, mult, s->hidden,
+                  s->inter);
         return MOE_ERR_INVALID_ARG;
     }
     return MOE_OK;
@@ -205,6 +214,83 @@ moe_status check_fp8_shape(const moe_shape* s) {
 moe_status do_combine(const moe_shape& s, const uint16_t* y_perm, const int32_t* dest, const float* w,
                       const uint16_t* y_shared, const uint16_t* residual, uint16_t* out, cudaStream_t st) {
     return from_cuda(launch_combine(s, y_perm, dest, w, y_shared, residual, out, st));
+}
+
+moe_status expert_up_q(const moe_shape* shape, const uint16_t* x_perm, const int32_t* offsets, const uint8_t* w13,
+                       const uint8_t* w13_bscale, const float* w13_scale, int wfmt, uint16_t* h, void* ws,
+                       size_t ws_bytes, void* stream) {
+    clear_error();
+    moe_status r = check_shape(shape);
+    if (r != MOE_OK) return r;
+    if ((r = check_quant_shape(shape, wfmt)) != MOE_OK) return r;
+    if ((r = check_ws(shape, ws, ws_bytes, false)) != MOE_OK) return r;
+    if (!aligned(x_perm, 16) || !aligned(offsets, 16) || !aligned(w13, 16) || !aligned(w13_scale, 16) ||
+        !aligned(h, 16) || (wfmt == kWeightNvfp4 && !aligned(w13_bscale, 16)))
+        return MOE_ERR_INVALID_ARG;
+    return do_up_q(*shape, x_perm, offsets, w13, w13_bscale, w13_scale, wfmt, h, ws,
+                   static_cast<cudaStream_t>(stream));
+}
+
+moe_status expert_down_q(const moe_shape* shape, const uint16_t* h, const int32_t* offsets, const uint8_t* w2,
+                         const uint8_t* w2_bscale, const float* w2_scale, int wfmt, uint16_t* y_perm, void* ws,
+                         size_t ws_bytes, void* stream) {
+    clear_error();
+    moe_status r = check_shape(shape);
+    if (r != MOE_OK) return r;
+    if ((r = check_quant_shape(shape, wfmt)) != MOE_OK) return r;
+    if ((r = check_ws(shape, ws, ws_bytes, false)) != MOE_OK) return r;
+    if (!aligned(h, 16) || !aligned(offsets, 16) || !aligned(w2, 16) || !aligned(w2_scale, 16) ||
+        !aligned(y_perm, 16) || (wfmt == kWeightNvfp4 && !aligned(w2_bscale, 16)))
+        return MOE_ERR_INVALID_ARG;
+    return do_down_q(*shape, h, offsets, w2, w2_bscale, w2_scale, wfmt, y_perm, ws,
+                     static_cast<cudaStream_t>(stream));
+}
+
+moe_status layer_q(const moe_shape* shape, const float* logits, const int32_t* ids_in, const float* w_in,
+                   const uint16_t* x, const uint8_t* w13, const uint8_t* w13_bscale, const float* w13_scale,
+                   const uint8_t* w2, const uint8_t* w2_bscale, const float* w2_scale, int wfmt,
+                   const uint16_t* residual, uint16_t* out, void* ws, size_t ws_bytes, void* stream) {
+    clear_error();
+    moe_status r = check_shape(shape);
+    if (r != MOE_OK) return r;
+    if ((r = check_quant_shape(shape, wfmt)) != MOE_OK) return r;
+    if ((r = check_ws(shape, ws, ws_bytes, true)) != MOE_OK) return r;
+    if (logits ? !aligned(logits, 16) : (!aligned(ids_in, 16) || !aligned(w_in, 16))) return MOE_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(w13, 16) || !aligned(w13_scale, 16) || !aligned(w2, 16) ||
+        !aligned(w2_scale, 16) || !aligned(out, 16) || !aligned_or_null(residual, 16))
+        return MOE_ERR_INVALID_ARG;
+    if (wfmt == kWeightNvfp4 && (!aligned(w13_bscale, 16) || !aligned(w2_bscale, 16))) return MOE_ERR_INVALID_ARG;
+    const moe_shape& s = *shape;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const WsLayout L = ws_layout(s);
+    const int32_t* ids = ids_in;
+    const float* w = w_in;
+    const bool small = s.tokens <= kSmallDispatchTokens;   // one fused route + dispatch kernel
+    if (logits) {
+        int32_t* ids_ws = at<int32_t>(ws, L.ids);
+        float* w_ws = at<float>(ws, L.w);
+        if (!small && (r = do_route(s, logits, ids_ws, w_ws, ws, st)) != MOE_OK) return r;
+        ids = ids_ws;
+        w = w_ws;
+    }
+    int32_t* offsets = at<int32_t>(ws, L.offsets);
+    int32_t* dest = at<int32_t>(ws, L.dest);
+    uint16_t* x_perm = at<uint16_t>(ws, L.x_perm);
+    uint16_t* h = at<uint16_t>(ws, L.h);
+    uint16_t* y_perm = at<uint16_t>(ws, L.y_perm);
+    if (small) {
+        if ((r = from_cuda(launch_small_dispatch(s, logits, ids_in, at<int32_t>(ws, L.ids), at<float>(ws, L.w), x,
+                                                 at<int32_t>(ws, L.counts), offsets, dest,
+                                                 at<int32_t>(ws, L.sorted_pair), x_perm, at<WsHeader>(ws, 0), st))) !=
+            MOE_OK)
+            return r;
+    } else if ((r = do_dispatch(s, x, ids, at<int32_t>(ws, L.counts), offsets, dest, at<int32_t>(ws, L.sorted_pair),
+                                x_perm, ws, st)) != MOE_OK) {
+        return r;
+    }
+    if ((r = do_up_q(s, x_perm, offsets, w13, w13_bscale, w13_scale, wfmt, h, ws, st)) != MOE_OK) return r;
+    if ((r = do_down_q(s, h, offsets, w2, w2_bscale, w2_scale, wfmt, y_perm, ws, st)) != MOE_OK) return r;
+    return do_combine(s, y_perm, dest, w, nullptr, residual, out, st);
 }
 
 }  // namespace
@@ -386,73 +472,40 @@ moe_status moe_layer(const moe_shape* shape, const float* logits, const int32_t*
 moe_status moe_expert_up_fp8(const moe_shape* shape, const uint16_t* x_perm, const int32_t* offsets,
                              const uint8_t* w13, const float* w13_scale, uint16_t* h, void* ws, size_t ws_bytes,
                              void* stream) {
-    clear_error();
-    moe_status r = check_shape(shape);
-    if (r != MOE_OK) return r;
-    if ((r = check_fp8_shape(shape)) != MOE_OK) return r;
-    if ((r = check_ws(shape, ws, ws_bytes, false)) != MOE_OK) return r;
-    if (!aligned(x_perm, 16) || !aligned(offsets, 16) || !aligned(w13, 16) || !aligned(w13_scale, 16) ||
-        !aligned(h, 16))
-        return MOE_ERR_INVALID_ARG;
-    return do_up_fp8(*shape, x_perm, offsets, w13, w13_scale, h, ws, static_cast<cudaStream_t>(stream));
+    return expert_up_q(shape, x_perm, offsets, w13, nullptr, w13_scale, kWeightFp8E4M3, h, ws, ws_bytes, stream);
 }
 
 moe_status moe_expert_down_fp8(const moe_shape* shape, const uint16_t* h, const int32_t* offsets, const uint8_t* w2,
                                const float* w2_scale, uint16_t* y_perm, void* ws, size_t ws_bytes, void* stream) {
-    clear_error();
-    moe_status r = check_shape(shape);
-    if (r != MOE_OK) return r;
-    if ((r = check_fp8_shape(shape)) != MOE_OK) return r;
-    if ((r = check_ws(shape, ws, ws_bytes, false)) != MOE_OK) return r;
-    if (!aligned(h, 16) || !aligned(offsets, 16) || !aligned(w2, 16) || !aligned(w2_scale, 16) || !aligned(y_perm, 16))
-        return MOE_ERR_INVALID_ARG;
-    return do_down_fp8(*shape, h, offsets, w2, w2_scale, y_perm, ws, static_cast<cudaStream_t>(stream));
+    return expert_down_q(shape, h, offsets, w2, nullptr, w2_scale, kWeightFp8E4M3, y_perm, ws, ws_bytes, stream);
 }
 
 moe_status moe_layer_fp8(const moe_shape* shape, const float* logits, const int32_t* ids_in, const float* w_in,
                          const uint16_t* x, const uint8_t* w13, const float* w13_scale, const uint8_t* w2,
                          const float* w2_scale, const uint16_t* residual, uint16_t* out, void* ws, size_t ws_bytes,
                          void* stream) {
-    clear_error();
-    moe_status r = check_shape(shape);
-    if (r != MOE_OK) return r;
-    if ((r = check_fp8_shape(shape)) != MOE_OK) return r;
-    if ((r = check_ws(shape, ws, ws_bytes, true)) != MOE_OK) return r;
-    if (logits ? !aligned(logits, 16) : (!aligned(ids_in, 16) || !aligned(w_in, 16))) return MOE_ERR_INVALID_ARG;
-    if (!aligned(x, 16) || !aligned(w13, 16) || !aligned(w13_scale, 16) || !aligned(w2, 16) ||
-        !aligned(w2_scale, 16) || !aligned(out, 16) || !aligned_or_null(residual, 16))
-        return MOE_ERR_INVALID_ARG;
-    const moe_shape& s = *shape;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const WsLayout L = ws_layout(s);
-    const int32_t* ids = ids_in;
-    const float* w = w_in;
-    const bool small = s.tokens <= kSmallDispatchTokens;   // one fused route + dispatch kernel
-    if (logits) {
-        int32_t* ids_ws = at<int32_t>(ws, L.ids);
-        float* w_ws = at<float>(ws, L.w);
-        if (!small && (r = do_route(s, logits, ids_ws, w_ws, ws, st)) != MOE_OK) return r;
-        ids = ids_ws;
-        w = w_ws;
-    }
-    int32_t* offsets = at<int32_t>(ws, L.offsets);
-    int32_t* dest = at<int32_t>(ws, L.dest);
-    uint16_t* x_perm = at<uint16_t>(ws, L.x_perm);
-    uint16_t* h = at<uint16_t>(ws, L.h);
-    uint16_t* y_perm = at<uint16_t>(ws, L.y_perm);
-    if (small) {
-        if ((r = from_cuda(launch_small_dispatch(s, logits, ids_in, at<int32_t>(ws, L.ids), at<float>(ws, L.w), x,
-                                                 at<int32_t>(ws, L.counts), offsets, dest,
-                                                 at<int32_t>(ws, L.sorted_pair), x_perm, at<WsHeader>(ws, 0), st))) !=
-            MOE_OK)
-            return r;
-    } else if ((r = do_dispatch(s, x, ids, at<int32_t>(ws, L.counts), offsets, dest, at<int32_t>(ws, L.sorted_pair),
-                                x_perm, ws, st)) != MOE_OK) {
-        return r;
-    }
-    if ((r = do_up_fp8(s, x_perm, offsets, w13, w13_scale, h, ws, st)) != MOE_OK) return r;
-    if ((r = do_down_fp8(s, h, offsets, w2, w2_scale, y_perm, ws, st)) != MOE_OK) return r;
-    return do_combine(s, y_perm, dest, w, nullptr, residual, out, st);
+    return layer_q(shape, logits, ids_in, w_in, x, w13, nullptr, w13_scale, w2, nullptr, w2_scale, kWeightFp8E4M3,
+                   residual, out, ws, ws_bytes, stream);
+}
+
+moe_status moe_expert_up_nvfp4(const moe_shape* shape, const uint16_t* x_perm, const int32_t* offsets,
+                               const uint8_t* w13, const uint8_t* w13_bscale, const float* w13_scale, uint16_t* h,
+                               void* ws, size_t ws_bytes, void* stream) {
+    return expert_up_q(shape, x_perm, offsets, w13, w13_bscale, w13_scale, kWeightNvfp4, h, ws, ws_bytes, stream);
+}
+
+moe_status moe_expert_down_nvfp4(const moe_shape* shape, const uint16_t* h, const int32_t* offsets,
+                                 const uint8_t* w2, const uint8_t* w2_bscale, const float* w2_scale,
+                                 uint16_t* y_perm, void* ws, size_t ws_bytes, void* stream) {
+    return expert_down_q(shape, h, offsets, w2, w2_bscale, w2_scale, kWeightNvfp4, y_perm, ws, ws_bytes, stream);
+}
+
+moe_status moe_layer_nvfp4(const moe_shape* shape, const float* logits, const int32_t* ids_in, const float* w_in,
+                           const uint16_t* x, const uint8_t* w13, const uint8_t* w13_bscale, const float* w13_scale,
+                           const uint8_t* w2, const uint8_t* w2_bscale, const float* w2_scale,
+                           const uint16_t* residual, uint16_t* out, void* ws, size_t ws_bytes, void* stream) {
+    return layer_q(shape, logits, ids_in, w_in, x, w13, w13_bscale, w13_scale, w2, w2_bscale, w2_scale,
+                   kWeightNvfp4, residual, out, ws, ws_bytes, stream);
 }
 
 moe_status moe_status_read(void* ws, void* stream, moe_status* device_status) {

@@ -374,11 +374,14 @@ struct GemmProblem {
     int up_off;                                           // SwiGLU: rows from gate to up half
     void* out; long long ldo; int out_group_col;
     int max_group_rows;                                   // host bound on rows per group (0: a_rows)
-    int wfmt;                                             // kWeightBf16 or kWeightFp8E4M3 (B's format)
-    const float* wscale;                                  // FP8: FP32 scale per B row
+    int wfmt;                                             // B's format: kWeightBf16 / Fp8E4M3 / Nvfp4
+    const float* wscale;                                  // FP8, NVFP4: FP32 scale per B row
+    const uint8_t* bscale;                                // NVFP4: E4M3 scale per 16 K elements
+    long long bscale_stride;                              // NVFP4: bytes per B row of bscale
 };
 constexpr int kWeightBf16 = 0;
-constexpr int kWeightFp8E4M3 = 1;
+constexpr int kWeightFp8E4M3 = 1;   // one E4M3 code per element (b_cols bytes per row)
+constexpr int kWeightNvfp4 = 2;     // two E2M1 codes per byte, low nibble first (b_cols / 2 bytes per row)
 // Returns MOE_OK, MOE_ERR_CUDA (tensor map / launch) or MOE_ERR_UNSUPPORTED.
 // Problems whose groups hold at most kDecodeRows rows and whose work fits in
 // about two waves run the small-row kernel (launch_decode_gemm); the rest the
@@ -393,11 +396,11 @@ moe_status launch_decode_gemm(const GemmProblem& p, int nb, WsHeader* hdr, cudaS
 // Tensor map of a row-major [rows, cols] BF16 matrix, 128-byte swizzle, boxes
 // of 64 columns x box_rows rows (records the failure for moe_last_error_message).
 bool make_tensor_map_bf16(CUtensorMap* m, const void* base, long long rows, long long cols, unsigned box_rows);
-// Tensor map of a row-major [rows, cols] byte matrix (FP8 codes), boxes of
-// box_cols bytes x box_rows rows; 128-byte boxes are 128-byte swizzled, others
-// not swizzled.
-bool make_tensor_map_u8_rows(CUtensorMap* m, const void* base, long long rows, long long cols, unsigned box_cols,
-                             unsigned box_rows);
+// Tensor map of a [rows, cols] byte matrix with row stride `stride` bytes (a
+// multiple of 16; FP8 / NVFP4 codes, NVFP4 block scales), boxes of box_cols
+// bytes x box_rows rows; 128-byte boxes are 128-byte swizzled, others not.
+bool make_tensor_map_u8_rows(CUtensorMap* m, const void* base, long long rows, long long cols, long long stride,
+                             unsigned box_cols, unsigned box_rows);
 
 int device_sm_count();
 

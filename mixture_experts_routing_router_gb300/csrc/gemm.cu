@@ -882,8 +882,8 @@ bool make_tensor_map_bf16(CUtensorMap* m, const void* base, long long rows, long
     return make_map(m, base, rows, cols, box_rows);
 }
 
-bool make_tensor_map_u8_rows(CUtensorMap* m, const void* base, long long rows, long long cols, unsigned box_cols,
-                             unsigned box_rows) {
+bool make_tensor_map_u8_rows(CUtensorMap* m, const void* base, long long rows, long long cols, long long stride,
+                             unsigned box_cols, unsigned box_rows) {
     // 128-byte rows are 128-byte swizzled (the converter reads them conflict-free)
     auto enc = encode_fn();
     if (!enc) {
@@ -891,7 +891,7 @@ bool make_tensor_map_u8_rows(CUtensorMap* m, const void* base, long long rows, l
         return false;
     }
     cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)cols};
+    cuuint64_t strides[1] = {(cuuint64_t)stride};
     cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1u, 1u};
     const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
@@ -917,11 +917,11 @@ moe_status launch_grouped_gemm(const GemmProblem& g, WsHeader* hdr, cudaStream_t
     // starts sooner; with many more items the tile kernels' larger tiles
     // stream a few percent better (measured at 1 to 16 tokens over 240 experts).
     const long long row_bound = g.offsets ? (g.max_group_rows > 0 ? g.max_group_rows : g.a_rows) : g.rows_all;
-    if (g.wfmt == kWeightFp8E4M3) {
-        // FP8 weights are decoded by the small-row kernel at any size (groups of
-        // more than 64 rows are taken in 64-row chunks)
+    if (g.wfmt != kWeightBf16) {
+        // FP8 and NVFP4 weights are decoded by the small-row kernel at any size
+        // (groups of more than 64 rows are taken in 64-row chunks)
         if (g.nseg != 1) {
-            set_error("grouped GEMM: FP8 weights take one K segment");
+            set_error("grouped GEMM: quantized weights take one K segment");
             return MOE_ERR_UNSUPPORTED;
         }
         const int nb = row_bound >= kDecodeRows ? kDecodeRows : (row_bound < 16 ? 16 : (int)((row_bound + 15) / 16 * 16));

@@ -33,6 +33,15 @@
 // The MMA stays BF16 with FP32 accumulation; the row scale multiplies the
 // accumulator in the epilogue.
 // The FP8 stage holds its two activation boxes first, then the FP8 weight box(es).
+//
+// NVFP4 weights (the same page's NVFP4 cases; standard NVFP4 layout): E2M1
+// codes, two per byte with the lower K index in the low nibble, an E4M3 scale
+// per 16 consecutive elements of a row and an FP32 scale per row.  A stage is
+// 256 K elements: one 128-byte code row per weight row and TMA request (as for
+// FP8), the rows' 16 block scales (a 128 x 16-byte box) and four activation
+// boxes.  The converter warps form e2m1 * block scale * 2^-8 -- exact in BF16,
+// the scale applied before the cast -- into the TMEM slots in two 128-wide
+// chunks per stage, and the epilogue multiplies by the row scale * 2^8.
 #include "common.cuh"
 
 #include <mutex>
@@ -47,7 +56,9 @@ constexpr int DTHREADS = 192;              // producer, MMA, 4 epilogue warps
 constexpr int CONV_WARPS = 8;              // FP8: converter warps (6 .. 6 + CONV_WARPS - 1)
 constexpr int DTHREADS_FP8 = 192 + 32 * CONV_WARPS;
 constexpr int DBK8 = 128;                  // FP8 stage: 128 codes (128 B) of each weight row
-constexpr int W8_BYTES = DBM * DBK8;       // 16 KiB FP8 weight box
+constexpr int W8_BYTES = DBM * DBK8;       // 16 KiB FP8 / NVFP4 code box
+constexpr int DBK4 = 256;                  // NVFP4 stage: 256 codes (128 B) of each weight row
+constexpr int S4_BYTES = DBM * 16;         // NVFP4: the 16 block scales of 128 weight rows
 constexpr int MAX_CSLOTS = 4;
 constexpr int MAX_DSTAGES = 16;
 constexpr int MAX_DSMEM = 212 * 1024;
@@ -67,10 +78,11 @@ struct DParams {
     uint32_t tmem_cols;         // two accumulators of (SwiGLU ? 2 : 1) * nb columns, power of two
     uint32_t x_off;             // activation box within a stage
     uint32_t w_off;             // first weight box within a stage
-    // FP8 weights
+    // FP8 / NVFP4 weights
     const float* wscale;        // [weight rows] FP32 scale per weight row
     uint32_t a_col;             // TMEM column of the first converted-weight slot
     int conv_slots;             // converted-weight slots in TMEM (NW * 64 columns each)
+    uint32_t s_off;             // NVFP4: first block-scale box within a stage
 };
 
 template <int MODE> struct OutOfD { using T = __nv_bfloat16; };
@@ -81,8 +93,8 @@ struct DCtl {
     unsigned long long empty[MAX_DSTAGES];
     unsigned long long tfull[2];
     unsigned long long tempty[2];
-    unsigned long long cfull[MAX_CSLOTS];      // FP8: slot converted (4 converter warps)
-    unsigned long long cempty[MAX_CSLOTS];     // FP8: slot consumed by the MMA
+    unsigned long long cfull[MAX_CSLOTS];      // FP8 / NVFP4: slot converted (the converter warps)
+    unsigned long long cempty[MAX_CSLOTS];     // FP8 / NVFP4: slot consumed by the MMA
     unsigned long long drain;
     uint32_t tmem_base;
     int abort;
@@ -109,6 +121,29 @@ __device__ __forceinline__ void e4m3x4_to_bf16x4(uint32_t w, uint32_t& lo, uint3
     t1 = (t1 << 4) & 0x87F087F0u;
     asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(lo) : "r"(t0), "r"(kTwo120));
     asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(hi) : "r"(t1), "r"(kTwo120));
+}
+
+// Eight E2M1 codes (the nibbles of w, element 0 in the low nibble) times a
+// block scale -> four BF16 pairs (elements 2j, 2j+1 in out[j], low half
+// first), exact.  The codes are split into even and odd elements, one per
+// byte; prmt places element 2j in the low and 2j+1 in the high 16-bit half
+// (zero bytes from the sign-replicate selector on a byte below 0x80), and the
+// multiply by 0x1040 adds the copies shifted by 6 and by 12 (disjoint bits),
+// so the mask keeps the code's exponent and mantissa bits at bits 6..8 and
+// its sign at bit 15 of each half: the BF16 number e2m1 * 2^-126 (subnormal
+// for exponent field 0, where E2M1 is 0 or 0.5, exactly as E2M1 defines it).
+// m = (s, s) with s = block scale * 2^126 * 2^-8 finishes the value in one
+// BF16 multiply: at most 2 + 4 significant bits, within the normal range.
+__device__ __forceinline__ void e2m1x8_to_bf16x8(uint32_t w, uint32_t m, uint32_t* out) {
+    const uint32_t ev = w & 0x0F0F0F0Fu;                      // elements 0, 2, 4, 6
+    const uint32_t od = (w >> 4) & 0x0F0F0F0Fu;               // elements 1, 3, 5, 7
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        uint32_t t;
+        asm("prmt.b32 %0, %1, %2, %3;" : "=r"(t) : "r"(ev), "r"(od), "r"(0x8480u + 0x0101u * (uint32_t)j));
+        t = (t * 0x1040u) & 0x81C081C0u;
+        asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(out[j]) : "r"(t), "r"(m));
+    }
 }
 
 __device__ __forceinline__ void clamped_bounds(const DParams& p, int g, int& lo, int& hi) {
@@ -142,10 +177,13 @@ __device__ __forceinline__ void tmem_st_32cols(uint32_t taddr, const uint32_t (&
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-template <int MODE, bool FP8W>
-__global__ void __launch_bounds__(FP8W ? DTHREADS_FP8 : DTHREADS, 1)
+template <int MODE, int WF>
+__global__ void __launch_bounds__(WF != kWeightBf16 ? DTHREADS_FP8 : DTHREADS, 1)
 decode_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
-                   const DParams p) {
+                   const __grid_constant__ CUtensorMap tmS, const DParams p) {
+    constexpr bool FP8W = WF != kWeightBf16;               // converted weights (FP8 or NVFP4)
+    constexpr bool FP4W = WF == kWeightNvfp4;
+    constexpr int NCH = FP4W ? 2 : 1;                      // 128-wide converted chunks per stage
     constexpr int NW = (MODE == kGemmSwiGLU) ? 2 : 1;      // weight boxes per stage
     constexpr int NTH = FP8W ? DTHREADS_FP8 : DTHREADS;
     extern __shared__ uint8_t smem_raw[];
@@ -181,6 +219,7 @@ decode_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
         fence_proxy_async_smem();
         tma_prefetch_desc(&tmX);
         tma_prefetch_desc(&tmW);
+        if (FP4W) tma_prefetch_desc(&tmS);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(&ctl->tmem_base), p.tmem_cols);
@@ -237,9 +276,9 @@ decode_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
     volatile int* abort = &ctl->abort;
     const int ntn = (p.N + DBM - 1) / DBM;
     const int items = ctl->ng * ntn;
-    // K per stage: 64 (BF16 weights) or 128 (FP8: one 128-byte row per weight row
-    // and TMA request, split into two 64-wide halves for the MMA)
-    const int kstep = FP8W ? DBK8 : DBK;
+    // K per stage: 64 (BF16 weights), 128 (FP8) or 256 (NVFP4): one 128-byte row
+    // per weight row and TMA request; the MMA takes it in 64-wide activation boxes
+    const int kstep = FP4W ? DBK4 : (FP8W ? DBK8 : DBK);
     const int nkb = (p.K + kstep - 1) / kstep;
     const int nk = nkb * p.nseg;
     const uint32_t xbox = (uint32_t)(p.nb * DBK * 2);        // one activation box (nb rows x 64)
@@ -265,12 +304,18 @@ decode_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
                         const uint32_t full = smem_u32(&ctl->full[stage]);
                         mbar_arrive_expect_tx(full, (uint32_t)p.stage_bytes);
                         const uint32_t sa = smem_base + (uint32_t)(stage * p.stage_bytes);
-                        tma_load_2d(sa + w_off, &tmW, full, kb * kstep, w_row + seg * p.b_seg_row);
+                        const int wcol = FP4W ? kb * (DBK4 / 2) : kb * kstep;     // code bytes
+                        tma_load_2d(sa + w_off, &tmW, full, wcol, w_row + seg * p.b_seg_row);
                         if (MODE == kGemmSwiGLU)
-                            tma_load_2d(sa + w_off + w_box, &tmW, full, kb * kstep, w_row + p.up_off + seg * p.b_seg_row);
-                        tma_load_2d(sa + x_off, &tmX, full, seg * p.a_seg_col + kb * kstep, xr);
-                        if (FP8W)   // the stage's second 64-wide activation half
-                            tma_load_2d(sa + x_off + xbox, &tmX, full, seg * p.a_seg_col + kb * kstep + DBK, xr);
+                            tma_load_2d(sa + w_off + w_box, &tmW, full, wcol, w_row + p.up_off + seg * p.b_seg_row);
+                        if (FP4W) {     // the rows' block scales of these 256 elements
+                            tma_load_2d(sa + p.s_off, &tmS, full, kb * (DBK4 / 16), w_row);
+                            if (MODE == kGemmSwiGLU)
+                                tma_load_2d(sa + p.s_off + S4_BYTES, &tmS, full, kb * (DBK4 / 16), w_row + p.up_off);
+                        }
+                        for (int xb = 0; xb < kstep / DBK; ++xb)   // 64-wide activation boxes
+                            tma_load_2d(sa + x_off + (uint32_t)xb * xbox, &tmX, full,
+                                        seg * p.a_seg_col + kb * kstep + xb * DBK, xr);
                         if (++stage == p.stages) { stage = 0; ph ^= 1u; }
                     }
                 }
@@ -300,26 +345,30 @@ decode_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
                         if (!mbar_wait_bounded(smem_u32(&ctl->full[stage]), ph, abort)) { ok = false; break; }
                         const uint32_t sa = smem_base + (uint32_t)(stage * p.stage_bytes);
                         if constexpr (FP8W) {
-                            // the stage's weights, converted to BF16, are in TMEM slot cs:
-                            // box wb, K half hf at columns a_col + cs*NW*64 + wb*64 + hf*32
-                            if (!mbar_wait_bounded(smem_u32(&ctl->cfull[cs]), cph, abort)) { ok = false; break; }
-                            tc_fence_after();
-                            const uint32_t aslot = tmem + p.a_col + (uint32_t)(cs * NW * 64);
+                            // each 128-wide chunk ch of the stage's weights, converted to BF16,
+                            // is in a TMEM slot cs: box wb, K half hf at columns
+                            // a_col + cs*NW*64 + wb*64 + hf*32; its activations are boxes 2ch + hf
+                            for (int ch = 0; ch < NCH && ok; ++ch) {
+                                if (!mbar_wait_bounded(smem_u32(&ctl->cfull[cs]), cph, abort)) { ok = false; break; }
+                                tc_fence_after();
+                                const uint32_t aslot = tmem + p.a_col + (uint32_t)(cs * NW * 64);
 #pragma unroll
-                            for (int hf = 0; hf < 2; ++hf) {
-                                const uint64_t xd = sdesc_k_sw128(sa + x_off + (uint32_t)hf * xbox);
+                                for (int hf = 0; hf < 2; ++hf) {
+                                    const uint64_t xd = sdesc_k_sw128(sa + x_off + (uint32_t)(2 * ch + hf) * xbox);
 #pragma unroll
-                                for (int kk = 0; kk < DBK / 16; ++kk) {
-                                    const uint32_t accum = (i > 0 || hf > 0 || kk > 0) ? 1u : 0u;
-                                    const uint32_t acol = (uint32_t)(hf * 32 + kk * 8);
-                                    tc_mma_bf16_ts(d, aslot + acol, xd + (uint64_t)(kk * 2), idesc, accum);
-                                    if (MODE == kGemmSwiGLU)
-                                        tc_mma_bf16_ts(d + (uint32_t)nb, aslot + 64 + acol, xd + (uint64_t)(kk * 2),
-                                                       idesc, accum);
+                                    for (int kk = 0; kk < DBK / 16; ++kk) {
+                                        const uint32_t accum = (i > 0 || ch > 0 || hf > 0 || kk > 0) ? 1u : 0u;
+                                        const uint32_t acol = (uint32_t)(hf * 32 + kk * 8);
+                                        tc_mma_bf16_ts(d, aslot + acol, xd + (uint64_t)(kk * 2), idesc, accum);
+                                        if (MODE == kGemmSwiGLU)
+                                            tc_mma_bf16_ts(d + (uint32_t)nb, aslot + 64 + acol,
+                                                           xd + (uint64_t)(kk * 2), idesc, accum);
+                                    }
                                 }
+                                tc_commit(smem_u32(&ctl->cempty[cs]));
+                                if (++cs == p.conv_slots) { cs = 0; cph ^= 1u; }
                             }
-                            tc_commit(smem_u32(&ctl->cempty[cs]));
-                            if (++cs == p.conv_slots) { cs = 0; cph ^= 1u; }
+                            if (!ok) break;
                         } else {
                             tc_fence_after();
                             const uint64_t wd = sdesc_k_sw128(sa + w_off);
@@ -353,13 +402,14 @@ decode_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
             }
         }
     } else if (FP8W && warp >= 6) {
-        // ---------------- FP8 -> BF16 converter (warps 6 .. 6 + CONV_WARPS - 1) ----
-        // A stage's FP8 box is 128 rows x 128 codes, 128-byte swizzled (16-byte
+        // ---------------- FP8 / NVFP4 -> BF16 converter (warps 6 .. 6 + CONV_WARPS - 1)
+        // A stage's code box is 128 rows x 128 bytes, 128-byte swizzled (16-byte
         // chunk c of row r at chunk c ^ (r & 7)).  Converter warp w owns TMEM lane
         // quarter w % 4, i.e. weight rows r = 32*(w % 4) + lane, and K half
-        // hf = (w - 6) / 4 of every stage: each thread decodes its row's 64 codes
-        // of that half (four conflict-free 16-byte loads) and stores the 32 packed
-        // BF16 pairs to its TMEM lane, columns a_col + cs*NW*64 + wb*64 + hf*32.
+        // hf = (w - 6) / 4 of every 128-wide chunk: each thread decodes its row's
+        // 64 elements of that half (FP8: four conflict-free 16-byte loads; NVFP4:
+        // two, with the row's four block scales of the half) and stores the 32
+        // packed BF16 pairs to its TMEM lane, columns a_col + cs*NW*64 + wb*64 + hf*32.
         const int q = warp & 3;
         const int hf = (warp - 6) >> 2;
         const int r = 32 * q + lane;
@@ -370,36 +420,65 @@ decode_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
         for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
             const int rows = gcnt[it / ntn];
             for (int c0 = 0; c0 < rows && ok; c0 += nb) {
-                for (int i = 0; i < nk; ++i) {
-                    if (!mbar_wait_bounded(smem_u32(&ctl->full[stage]), ph, abort) ||
-                        !mbar_wait_bounded(smem_u32(&ctl->cempty[cs]), cph ^ 1u, abort)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();                           // after the MMAs that read slot cs
-                    const uint8_t* src = smem + (size_t)stage * p.stage_bytes + w_off + (size_t)r * DBK8;
-                    const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + p.a_col + (uint32_t)(cs * NW * 64) +
-                                           (uint32_t)(hf * 32);
+                for (int i = 0; i < nk && ok; ++i) {
+                    if (!mbar_wait_bounded(smem_u32(&ctl->full[stage]), ph, abort)) { ok = false; break; }
+                    const uint8_t* st = smem + (size_t)stage * p.stage_bytes;
+                    const uint8_t* src = st + w_off + (size_t)r * DBK8;
+                    uint4 scl[NW];                              // NVFP4: the row's 16 block scales, per box
+                    if (FP4W)
 #pragma unroll
-                    for (int wb = 0; wb < NW; ++wb) {
-                        uint32_t v32[32];
+                        for (int wb = 0; wb < NW; ++wb)
+                            scl[wb] = *reinterpret_cast<const uint4*>(st + p.s_off + wb * S4_BYTES + r * 16);
+                    for (int ch = 0; ch < NCH; ++ch) {
+                        if (!mbar_wait_bounded(smem_u32(&ctl->cempty[cs]), cph ^ 1u, abort)) { ok = false; break; }
+                        tc_fence_after();                       // after the MMAs that read slot cs
+                        const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + p.a_col +
+                                               (uint32_t)(cs * NW * 64) + (uint32_t)(hf * 32);
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const uint4 v = *reinterpret_cast<const uint4*>(src + wb * W8_BYTES +
-                                                                            (((4 * hf + j) ^ sw) << 4));
-                            e4m3x4_to_bf16x4(v.x, v32[8 * j + 0], v32[8 * j + 1]);
-                            e4m3x4_to_bf16x4(v.y, v32[8 * j + 2], v32[8 * j + 3]);
-                            e4m3x4_to_bf16x4(v.z, v32[8 * j + 4], v32[8 * j + 5]);
-                            e4m3x4_to_bf16x4(v.w, v32[8 * j + 6], v32[8 * j + 7]);
+                        for (int wb = 0; wb < NW; ++wb) {
+                            uint32_t v32[32];
+                            if constexpr (FP4W) {
+                                // block scales of this half's 64 elements: bytes 8ch + 4hf .. +3
+                                const uint32_t s4 = (ch == 0) ? (hf == 0 ? scl[wb].x : scl[wb].y)
+                                                              : (hf == 0 ? scl[wb].z : scl[wb].w);
+                                constexpr uint32_t kTwo118 = 0x7A807A80u;     // (2^118, 2^118) in BF16
+                                uint32_t s01, s23, mb[4];
+                                e4m3x4_to_bf16x4(s4, s01, s23);
+                                asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(s01) : "r"(s01), "r"(kTwo118));
+                                asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(s23) : "r"(s23), "r"(kTwo118));
+                                asm("prmt.b32 %0, %1, 0, 0x1010;" : "=r"(mb[0]) : "r"(s01));
+                                asm("prmt.b32 %0, %1, 0, 0x3232;" : "=r"(mb[1]) : "r"(s01));
+                                asm("prmt.b32 %0, %1, 0, 0x1010;" : "=r"(mb[2]) : "r"(s23));
+                                asm("prmt.b32 %0, %1, 0, 0x3232;" : "=r"(mb[3]) : "r"(s23));
+#pragma unroll
+                                for (int j = 0; j < 2; ++j) {
+                                    const uint4 v = *reinterpret_cast<const uint4*>(
+                                        src + wb * W8_BYTES + (((4 * ch + 2 * hf + j) ^ sw) << 4));
+                                    e2m1x8_to_bf16x8(v.x, mb[2 * j], &v32[16 * j + 0]);
+                                    e2m1x8_to_bf16x8(v.y, mb[2 * j], &v32[16 * j + 4]);
+                                    e2m1x8_to_bf16x8(v.z, mb[2 * j + 1], &v32[16 * j + 8]);
+                                    e2m1x8_to_bf16x8(v.w, mb[2 * j + 1], &v32[16 * j + 12]);
+                                }
+                            } else {
+#pragma unroll
+                                for (int j = 0; j < 4; ++j) {
+                                    const uint4 v = *reinterpret_cast<const uint4*>(src + wb * W8_BYTES +
+                                                                                    (((4 * hf + j) ^ sw) << 4));
+                                    e4m3x4_to_bf16x4(v.x, v32[8 * j + 0], v32[8 * j + 1]);
+                                    e4m3x4_to_bf16x4(v.y, v32[8 * j + 2], v32[8 * j + 3]);
+                                    e4m3x4_to_bf16x4(v.z, v32[8 * j + 4], v32[8 * j + 5]);
+                                    e4m3x4_to_bf16x4(v.w, v32[8 * j + 6], v32[8 * j + 7]);
+                                }
+                            }
+                            tmem_st_32cols(taddr + (uint32_t)(wb * 64), v32);
                         }
-                        tmem_st_32cols(taddr + (uint32_t)(wb * 64), v32);
+                        tmem_st_wait();
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(smem_u32(&ctl->cfull[cs]));
+                        if (++cs == p.conv_slots) { cs = 0; cph ^= 1u; }
                     }
-                    tmem_st_wait();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(smem_u32(&ctl->cfull[cs]));
                     if (++stage == p.stages) { stage = 0; ph ^= 1u; }
-                    if (++cs == p.conv_slots) { cs = 0; cph ^= 1u; }
                 }
             }
         }
@@ -415,11 +494,13 @@ decode_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
             const int n = nt * DBM + 32 * q + lane;             // weight row = output column
             typename OutOfD<MODE>::T* ocol = reinterpret_cast<typename OutOfD<MODE>::T*>(p.out) +
                                              (size_t)g * p.out_group_col + (n < p.N ? n : 0);
-            // FP8: the weight rows' FP32 scales (gate and up rows for SwiGLU)
+            // FP8 / NVFP4: the weight rows' FP32 scales (gate and up rows for
+            // SwiGLU); NVFP4 weights were converted at 2^-8 of their value
             float sg = 1.f, su = 1.f;
             if (FP8W && n < p.N) {
-                sg = p.wscale[(size_t)g * p.b_group_rows + n];
-                if (MODE == kGemmSwiGLU) su = p.wscale[(size_t)g * p.b_group_rows + p.up_off + n];
+                constexpr float kUndo = FP4W ? 256.f : 1.f;
+                sg = p.wscale[(size_t)g * p.b_group_rows + n] * kUndo;
+                if (MODE == kGemmSwiGLU) su = p.wscale[(size_t)g * p.b_group_rows + p.up_off + n] * kUndo;
             }
             for (int c0 = 0; c0 < rows; c0 += nb) {
                 if (!mbar_wait_bounded(smem_u32(&ctl->tfull[acc]), aph, abort)) {
@@ -476,13 +557,13 @@ decode_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
     }
 }
 
-template <int MODE, bool FP8W>
-cudaError_t launch_d(const CUtensorMap& mx, const CUtensorMap& mw, const DParams& dp, unsigned grid, size_t smem,
-                     cudaStream_t st) {
+template <int MODE, int WF>
+cudaError_t launch_d(const CUtensorMap& mx, const CUtensorMap& mw, const CUtensorMap& ms, const DParams& dp,
+                     unsigned grid, size_t smem, cudaStream_t st) {
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(decode_gemm_kernel<MODE, FP8W>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        attr_err = cudaFuncSetAttribute(decode_gemm_kernel<MODE, WF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         MAX_DSMEM);
     });
     if (attr_err != cudaSuccess) {
@@ -490,8 +571,8 @@ cudaError_t launch_d(const CUtensorMap& mx, const CUtensorMap& mw, const DParams
         return attr_err;
     }
     const cudaError_t e =
-        launch_kernel(decode_gemm_kernel<MODE, FP8W>, dim3(grid), dim3(FP8W ? DTHREADS_FP8 : DTHREADS), smem, st, 1,
-                      kUsePdl, mx, mw, dp);
+        launch_kernel(decode_gemm_kernel<MODE, WF>, dim3(grid), dim3(WF != kWeightBf16 ? DTHREADS_FP8 : DTHREADS),
+                      smem, st, 1, kUsePdl, mx, mw, ms, dp);
     if (e != cudaSuccess) set_error("decode GEMM launch: %s", cudaGetErrorString(e));
     return e;
 }
@@ -504,9 +585,14 @@ moe_status launch_decode_gemm(const GemmProblem& g, int nb, WsHeader* hdr, cudaS
         return MOE_ERR_INTERNAL;
     }
     const int nw = g.mode == kGemmSwiGLU ? 2 : 1;
-    const bool fp8 = g.wfmt == kWeightFp8E4M3;
+    const bool fp4 = g.wfmt == kWeightNvfp4;
+    const bool fp8 = g.wfmt == kWeightFp8E4M3 || fp4;      // converted weights
     if (fp8 && (g.mode == kGemmF32 || !g.wscale)) {
-        set_error("decode GEMM: FP8 weights need a scale per weight row and a BF16 output");
+        set_error("decode GEMM: quantized weights need a scale per weight row and a BF16 output");
+        return MOE_ERR_UNSUPPORTED;
+    }
+    if (fp4 && (!g.bscale || g.K % 32 != 0 || g.bscale_stride % 16 != 0 || g.bscale_stride * 16 < g.K)) {
+        set_error("decode GEMM: NVFP4 weights need K %% 32 == 0 and block-scale rows of 16-byte multiples");
         return MOE_ERR_UNSUPPORTED;
     }
     DParams dp;
@@ -527,7 +613,17 @@ moe_status launch_decode_gemm(const GemmProblem& g, int nb, WsHeader* hdr, cudaS
     dp.hdr = hdr;
     dp.nb = nb;
     dp.wscale = g.wscale;
-    if (fp8) {
+    dp.s_off = 0;
+    if (fp4) {
+        // stage (K 256): [four activation boxes: nb rows x 128 B each][code box(es):
+        // 128 rows x 128 B = 16 KiB each][block-scale box(es): 128 rows x 16 B]
+        dp.x_off = 0;
+        dp.w_off = (uint32_t)(4 * nb * DBK * 2);
+        dp.s_off = dp.w_off + (uint32_t)(nw * W8_BYTES);
+        dp.stage_bytes = (int)dp.s_off + nw * S4_BYTES;
+        dp.conv_slots = nw == 2 ? 2 : 3;
+        dp.a_col = 256;
+    } else if (fp8) {
         // stage (K 128): [two activation boxes: nb rows x 128 B each][FP8 weight
         // box(es): 128 rows x 128 B = 16 KiB each]
         dp.x_off = 0;
@@ -556,7 +652,8 @@ moe_status launch_decode_gemm(const GemmProblem& g, int nb, WsHeader* hdr, cudaS
     if (grid > sms) grid = sms;
     if (grid < 1) grid = 1;
     const size_t fixed = 1024 + sizeof(DCtl) + (size_t)3 * g.groups * sizeof(int);
-    const int nk = ((g.K + (fp8 ? DBK8 : DBK) - 1) / (fp8 ? DBK8 : DBK)) * g.nseg;
+    const int kstep = fp4 ? DBK4 : (fp8 ? DBK8 : DBK);
+    const int nk = ((g.K + kstep - 1) / kstep) * g.nseg;
     long long stages = ((long long)MAX_DSMEM - (long long)fixed) / dp.stage_bytes;
     if (stages > MAX_DSTAGES) stages = MAX_DSTAGES;
     // two items' worth is plenty; FP8 (512 TMEM columns) keeps a full ring so
@@ -569,24 +666,39 @@ moe_status launch_decode_gemm(const GemmProblem& g, int nb, WsHeader* hdr, cudaS
         set_error("decode GEMM needs %zu bytes of shared memory", smem);
         return MOE_ERR_UNSUPPORTED;
     }
-    CUtensorMap mx, mw;
+    CUtensorMap mx, mw, ms;
     if (!make_tensor_map_bf16(&mx, g.a, g.a_rows, g.a_cols, (unsigned)nb)) return MOE_ERR_CUDA;
-    if (fp8 ? !make_tensor_map_u8_rows(&mw, g.b, g.b_rows, g.b_cols, (unsigned)DBK8, (unsigned)DBM)
+    // code rows: K bytes (FP8) or K/2 bytes (NVFP4, two codes per byte)
+    const long long code_cols = fp4 ? g.b_cols / 2 : g.b_cols;
+    if (fp8 ? !make_tensor_map_u8_rows(&mw, g.b, g.b_rows, code_cols, code_cols, (unsigned)DBK8, (unsigned)DBM)
             : !make_tensor_map_bf16(&mw, g.b, g.b_rows, g.b_cols, (unsigned)DBM))
         return MOE_ERR_CUDA;
+    if (fp4) {
+        // block scales: K/16 bytes of each padded row, 16 per stage
+        if (!make_tensor_map_u8_rows(&ms, g.bscale, g.b_rows, g.b_cols / 16, g.bscale_stride, 16u, (unsigned)DBM))
+            return MOE_ERR_CUDA;
+    } else {
+        ms = mw;   // unused
+    }
     cudaError_t e;
-    if (fp8) {
+    if (fp4) {
         switch (g.mode) {
-            case kGemmSwiGLU: e = launch_d<kGemmSwiGLU, true>(mx, mw, dp, (unsigned)grid, smem, st); break;
-            case kGemmReLU2: e = launch_d<kGemmReLU2, true>(mx, mw, dp, (unsigned)grid, smem, st); break;
-            default: e = launch_d<kGemmPlain, true>(mx, mw, dp, (unsigned)grid, smem, st); break;
+            case kGemmSwiGLU: e = launch_d<kGemmSwiGLU, kWeightNvfp4>(mx, mw, ms, dp, (unsigned)grid, smem, st); break;
+            case kGemmReLU2: e = launch_d<kGemmReLU2, kWeightNvfp4>(mx, mw, ms, dp, (unsigned)grid, smem, st); break;
+            default: e = launch_d<kGemmPlain, kWeightNvfp4>(mx, mw, ms, dp, (unsigned)grid, smem, st); break;
+        }
+    } else if (fp8) {
+        switch (g.mode) {
+            case kGemmSwiGLU: e = launch_d<kGemmSwiGLU, kWeightFp8E4M3>(mx, mw, ms, dp, (unsigned)grid, smem, st); break;
+            case kGemmReLU2: e = launch_d<kGemmReLU2, kWeightFp8E4M3>(mx, mw, ms, dp, (unsigned)grid, smem, st); break;
+            default: e = launch_d<kGemmPlain, kWeightFp8E4M3>(mx, mw, ms, dp, (unsigned)grid, smem, st); break;
         }
     } else {
         switch (g.mode) {
-            case kGemmSwiGLU: e = launch_d<kGemmSwiGLU, false>(mx, mw, dp, (unsigned)grid, smem, st); break;
-            case kGemmReLU2: e = launch_d<kGemmReLU2, false>(mx, mw, dp, (unsigned)grid, smem, st); break;
-            case kGemmF32: e = launch_d<kGemmF32, false>(mx, mw, dp, (unsigned)grid, smem, st); break;
-            default: e = launch_d<kGemmPlain, false>(mx, mw, dp, (unsigned)grid, smem, st); break;
+            case kGemmSwiGLU: e = launch_d<kGemmSwiGLU, kWeightBf16>(mx, mw, ms, dp, (unsigned)grid, smem, st); break;
+            case kGemmReLU2: e = launch_d<kGemmReLU2, kWeightBf16>(mx, mw, ms, dp, (unsigned)grid, smem, st); break;
+            case kGemmF32: e = launch_d<kGemmF32, kWeightBf16>(mx, mw, ms, dp, (unsigned)grid, smem, st); break;
+            default: e = launch_d<kGemmPlain, kWeightBf16>(mx, mw, ms, dp, (unsigned)grid, smem, st); break;
         }
     }
     return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;

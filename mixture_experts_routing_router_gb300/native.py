@@ -33,7 +33,8 @@ MOE_ACT_RELU2 = 1
 EXPORTS = ("moe_workspace_size", "moe_workspace_init", "moe_route", "moe_dispatch", "moe_expert_up",
            "moe_expert_down", "moe_expert_ffn", "moe_combine", "moe_layer", "moe_status_read",
            "moe_status_string", "moe_last_error_message", "moe_dispatch_noalloc", "moe_gate",
-           "moe_route_sigmoid", "moe_expert_up_fp8", "moe_expert_down_fp8", "moe_layer_fp8")
+           "moe_route_sigmoid", "moe_expert_up_fp8", "moe_expert_down_fp8", "moe_layer_fp8",
+           "moe_expert_up_nvfp4", "moe_expert_down_nvfp4", "moe_layer_nvfp4")
 
 
 class MoEError(RuntimeError):
@@ -92,6 +93,9 @@ def lib():
                 "moe_expert_up_fp8": [SP, P, P, P, P, P, P, S, P],
                 "moe_expert_down_fp8": [SP, P, P, P, P, P, P, S, P],
                 "moe_layer_fp8": [SP, P, P, P, P, P, P, P, P, P, P, P, S, P],
+                "moe_expert_up_nvfp4": [SP, P, P, P, P, P, P, P, S, P],
+                "moe_expert_down_nvfp4": [SP, P, P, P, P, P, P, P, S, P],
+                "moe_layer_nvfp4": [SP, P, P, P, P, P, P, P, P, P, P, P, P, P, S, P],
             }
             for name, args in sig.items():
                 fn = getattr(L, name)
@@ -231,6 +235,30 @@ def moe_layer_fp8(shape, logits, ids_in, w_in, x, w13, w13_scale, w2, w2_scale, 
     _check(lib().moe_layer_fp8(ctypes.byref(shape), _ptr(logits), _ptr(ids_in), _ptr(w_in), _ptr(x), _ptr(w13),
                                _ptr(w13_scale), _ptr(w2), _ptr(w2_scale), _ptr(residual), _ptr(out), _ptr(ws),
                                _wsb(ws), _stream(stream)), "moe_layer_fp8")
+
+
+def moe_expert_up_nvfp4(shape, x_perm, offsets, w13, w13_bscale, w13_scale, h, ws, stream=None):
+    """Up projection with NVFP4 weights: codes uint8 [E, up, H/2], E4M3 block
+    scales uint8 [E, up, 16*ceil(H/256)], FP32 row scales [E, up]."""
+    _check(lib().moe_expert_up_nvfp4(ctypes.byref(shape), _ptr(x_perm), _ptr(offsets), _ptr(w13), _ptr(w13_bscale),
+                                     _ptr(w13_scale), _ptr(h), _ptr(ws), _wsb(ws), _stream(stream)),
+           "moe_expert_up_nvfp4")
+
+
+def moe_expert_down_nvfp4(shape, h, offsets, w2, w2_bscale, w2_scale, y_perm, ws, stream=None):
+    """Down projection with NVFP4 weights: codes uint8 [E, H, I/2], block
+    scales uint8 [E, H, 16*ceil(I/256)], FP32 row scales [E, H]."""
+    _check(lib().moe_expert_down_nvfp4(ctypes.byref(shape), _ptr(h), _ptr(offsets), _ptr(w2), _ptr(w2_bscale),
+                                       _ptr(w2_scale), _ptr(y_perm), _ptr(ws), _wsb(ws), _stream(stream)),
+           "moe_expert_down_nvfp4")
+
+
+def moe_layer_nvfp4(shape, logits, ids_in, w_in, x, w13, w13_bscale, w13_scale, w2, w2_bscale, w2_scale, out, ws,
+                    stream=None, residual=None):
+    """The layer with NVFP4 expert weights (no shared experts)."""
+    _check(lib().moe_layer_nvfp4(ctypes.byref(shape), _ptr(logits), _ptr(ids_in), _ptr(w_in), _ptr(x), _ptr(w13),
+                                 _ptr(w13_bscale), _ptr(w13_scale), _ptr(w2), _ptr(w2_bscale), _ptr(w2_scale),
+                                 _ptr(residual), _ptr(out), _ptr(ws), _wsb(ws), _stream(stream)), "moe_layer_nvfp4")
 
 
 def moe_dispatch_noalloc(shape, x, topk_ids, counts, offsets, dest, sorted_pair, x_perm, device_status=None,

@@ -210,6 +210,56 @@ def make_fp8_weights(wl: Workload, seed: int = 0, device="cpu", unit_scale: bool
     return d
 
 
+E2M1_MAGNITUDES = (0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0)
+
+
+def quantize_rows_nvfp4(w: torch.Tensor):
+    """Input preparation for NVFP4 expert weights: each row of ``w`` [..., rows,
+    K] (K a multiple of 16) gets a row scale max|row| / (6 * 448) (1 for an
+    all-zero row), E4M3 block scales (torch's round-to-nearest float8_e4m3fn
+    conversion) of max|block| / (6 * row scale) per 16 elements, and E2M1
+    codes of w / (block scale * row scale) rounded to the nearest magnitude.
+    -> (codes uint8 [..., rows, K/2], two per byte, low nibble first;
+        bscale uint8 [..., rows, 16*ceil(K/256)], zero padded;
+        scale float32 [..., rows])."""
+    wf = w.float()
+    K = wf.shape[-1]
+    amax = wf.abs().amax(dim=-1, keepdim=True)
+    rs = torch.where(amax > 0, amax / (6.0 * 448.0), torch.ones_like(amax))
+    blk = wf.unflatten(-1, (K // 16, 16))
+    bmax = blk.abs().amax(dim=-1) / (6.0 * rs)
+    bs = bmax.to(torch.float8_e4m3fn)
+    bsf = bs.float()
+    v = blk / torch.where(bsf > 0, bsf, torch.ones_like(bsf)).unsqueeze(-1) / rs.unsqueeze(-1)
+    mags = torch.tensor(E2M1_MAGNITUDES, device=w.device)
+    mid = (mags[1:] + mags[:-1]) / 2
+    code = torch.bucketize(v.abs(), mid) | torch.where(v < 0, 8, 0)
+    code = code.flatten(-2).to(torch.uint8)
+    codes = (code[..., 0::2] | (code[..., 1::2] << 4)).contiguous()
+    bscale = torch.zeros(wf.shape[:-1] + (16 * ((K + 255) // 256),), dtype=torch.uint8, device=w.device)
+    bscale[..., :K // 16] = bs.view(torch.uint8)
+    return codes, bscale, rs.squeeze(-1).contiguous()
+
+
+def make_nvfp4_weights(wl: Workload, seed: int = 0, device="cpu", unit_scale: bool = False) -> dict:
+    """NVFP4 expert weights quantized from the same per-expert BF16 draws as
+    make_inputs: w13 uint8 [E, up, H/2], b13 uint8 [E, up, 16*ceil(H/256)],
+    s13 float32 [E, up]; w2 uint8 [E, H, I/2], b2 uint8 [E, H, 16*ceil(I/256)],
+    s2 float32 [E, H]."""
+    E, H, I = wl.experts, wl.hidden, wl.inter
+    d = {"w13": torch.empty((E, wl.up, H // 2), dtype=torch.uint8, device=device),
+         "b13": torch.empty((E, wl.up, 16 * ((H + 255) // 256)), dtype=torch.uint8, device=device),
+         "s13": torch.empty((E, wl.up), dtype=torch.float32, device=device),
+         "w2": torch.empty((E, H, I // 2), dtype=torch.uint8, device=device),
+         "b2": torch.empty((E, H, 16 * ((I + 255) // 256)), dtype=torch.uint8, device=device),
+         "s2": torch.empty((E, H), dtype=torch.float32, device=device)}
+    for e in range(E):
+        a, b = expert_weights(wl, e, seed, device, unit_scale)
+        d["w13"][e], d["b13"][e], d["s13"][e] = quantize_rows_nvfp4(a)
+        d["w2"][e], d["b2"][e], d["s2"][e] = quantize_rows_nvfp4(b)
+    return d
+
+
 def gate_weights(wl: Workload, seed: int = 0, device="cpu") -> torch.Tensor:
     """Router projection W_gate [E, H] ~ N(0, 1/H): x ~ N(0,1) gives logits of
     about unit scale."""

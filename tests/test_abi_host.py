@@ -108,6 +108,31 @@ def test_status_strings(L):
     assert N.status_string(3).startswith("an expert")
 
 
+def test_nvfp4_entry_points_validate_on_the_host(L):
+    fake = ctypes.c_void_p(4096)
+    ws = ctypes.c_void_p(1 << 20)
+    s = shape(shared=1, shared_inter=64)
+    n = N.moe_workspace_size(s)
+    assert L.moe_expert_up_nvfp4(ctypes.byref(s), fake, fake, fake, fake, fake, fake, ws, n,
+                                 None) == N.MOE_ERR_UNSUPPORTED
+    # two codes per byte: TMA-loaded rows need hidden and inter multiples of 32
+    s = shape(hidden=272)
+    n = N.moe_workspace_size(s)
+    assert L.moe_layer_nvfp4(ctypes.byref(s), fake, None, None, fake, fake, fake, fake, fake, fake, fake, None, fake,
+                             ws, n, None) == N.MOE_ERR_INVALID_ARG
+    s = shape(inter=528)
+    n = N.moe_workspace_size(s)
+    assert L.moe_expert_down_nvfp4(ctypes.byref(s), fake, fake, fake, fake, fake, fake, ws, n,
+                                   None) == N.MOE_ERR_INVALID_ARG
+    # misaligned or missing block scales
+    s = shape()
+    n = N.moe_workspace_size(s)
+    assert L.moe_expert_up_nvfp4(ctypes.byref(s), fake, fake, fake, ctypes.c_void_p(4100), fake, fake, ws, n,
+                                 None) == N.MOE_ERR_INVALID_ARG
+    assert L.moe_expert_down_nvfp4(ctypes.byref(s), fake, fake, fake, None, fake, fake, ws, n,
+                                   None) == N.MOE_ERR_INVALID_ARG
+
+
 def test_fp8_entry_points_validate_on_the_host(L):
     fake = ctypes.c_void_p(4096)
     # shared experts are not part of the FP8 entry points
