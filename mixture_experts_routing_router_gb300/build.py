@@ -8,6 +8,7 @@ run time, so the library needs only libcuda from the system.
 from __future__ import annotations
 
 import concurrent.futures as cf
+import fcntl
 import os
 import shutil
 import subprocess
@@ -36,10 +37,24 @@ def _deps_mtime() -> float:
     return max(os.path.getmtime(f) for f in files)
 
 
+def _up_to_date() -> bool:
+    return os.path.exists(LIB) and os.path.getmtime(LIB) >= _deps_mtime()
+
+
 def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _deps_mtime() and not extra_flags:
+    if not force and not extra_flags and _up_to_date():
         return LIB
     os.makedirs(BUILD, exist_ok=True)
+    # one build at a time (parallel test workers share the object directory);
+    # a process that waited finds the library already rebuilt
+    with open(os.path.join(BUILD, ".lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        if not force and not extra_flags and _up_to_date():
+            return LIB
+        return _build_locked(verbose, extra_flags)
+
+
+def _build_locked(verbose, extra_flags) -> str:
     cc = nvcc()
 
     def compile_one(src):
