@@ -23,16 +23,20 @@
 // plain, or the FP32 accumulator.  Every wait is bounded (MOE_ERR_TIMEOUT,
 // TMEM freed, no trap).
 //
-// FP8 weights (FP8W): the weights arrive as OCP E4M3 codes with one FP32 scale
-// per weight row -- the ONNX Runtime operator's weight-only quantized experts
-// (BF16 activations), with E4M3 as the codec.  Every E4M3 value is exact in
-// BF16, so eight more warps (6..13) convert each TMA-loaded FP8 box (128 rows x
-// 128 bytes, 128-byte swizzle: one 128-byte request per weight row, as for BF16)
-// straight into TMEM -- each thread one weight row, its TMEM lane -- where the
-// MMA reads its A operand (tcgen05.mma with A in TMEM), in a ring of slots.
-// The MMA stays BF16 with FP32 accumulation; the row scale multiplies the
-// accumulator in the epilogue.
-// The FP8 stage holds its two activation boxes first, then the FP8 weight box(es).
+// FP8 weights (WF = kWeightFp8E4M3): the weights arrive as OCP E4M3 codes with
+// one FP32 scale per weight row -- the ONNX Runtime operator's weight-only
+// quantized experts (BF16 activations), with E4M3 as the codec.  Every E4M3
+// value is exact in BF16, so eight more warps (6..13) convert each TMA-loaded
+// code box (128 rows x 128 bytes, 128-byte swizzle: one 128-byte request per
+// weight row, as for BF16) straight into TMEM -- each thread one weight row,
+// its TMEM lane -- where the MMA reads its A operand (tcgen05.mma with A in
+// TMEM), in a ring of slots.  The MMA stays BF16 with FP32 accumulation; the
+// row scale multiplies the accumulator in the epilogue.
+// A stage holds its activation boxes first, then the code boxes.  With one
+// weight block per stage (ReLU^2, plain) a stage is 256 K elements (two code
+// boxes) converted as one chunk into a 128-column slot; SwiGLU (gate and up
+// blocks) takes 128 K elements per stage.  The converter-to-MMA handshake per
+// chunk, not the bytes, sets this kernel's pace, so larger chunks are faster.
 //
 // NVFP4 weights (the same page's NVFP4 cases; standard NVFP4 layout): E2M1
 // codes, two per byte with the lower K index in the low nibble, an E4M3 scale
@@ -40,8 +44,9 @@
 // 256 K elements: one 128-byte code row per weight row and TMA request (as for
 // FP8), the rows' 16 block scales (a 128 x 16-byte box) and four activation
 // boxes.  The converter warps form e2m1 * block scale * 2^-8 -- exact in BF16,
-// the scale applied before the cast -- into the TMEM slots in two 128-wide
-// chunks per stage, and the epilogue multiplies by the row scale * 2^8.
+// the scale applied before the cast -- into the TMEM slots (the whole stage as
+// one chunk with one weight block, two 128-wide chunks for SwiGLU), and the
+// epilogue multiplies by the row scale * 2^8.
 #include "common.cuh"
 
 #include <mutex>
@@ -53,9 +58,9 @@ constexpr int DBM = 128;                   // weight rows per item (MMA M)
 constexpr int DBK = 64;                    // 64 BF16 = one 128-byte swizzle row
 constexpr int W_BYTES = DBM * DBK * 2;     // 16 KiB weight box
 constexpr int DTHREADS = 192;              // producer, MMA, 4 epilogue warps
-constexpr int CONV_WARPS = 8;              // FP8: converter warps (6 .. 6 + CONV_WARPS - 1)
+constexpr int CONV_WARPS = 8;              // FP8 / NVFP4: converter warps (6 .. 6 + CONV_WARPS - 1)
 constexpr int DTHREADS_FP8 = 192 + 32 * CONV_WARPS;
-constexpr int DBK8 = 128;                  // FP8 stage: 128 codes (128 B) of each weight row
+constexpr int DBK8 = 128;                  // FP8 code box: 128 codes (128 B) of each weight row
 constexpr int W8_BYTES = DBM * DBK8;       // 16 KiB FP8 / NVFP4 code box
 constexpr int DBK4 = 256;                  // NVFP4 stage: 256 codes (128 B) of each weight row
 constexpr int S4_BYTES = DBM * 16;         // NVFP4: the 16 block scales of 128 weight rows
@@ -81,7 +86,7 @@ struct DParams {
     // FP8 / NVFP4 weights
     const float* wscale;        // [weight rows] FP32 scale per weight row
     uint32_t a_col;             // TMEM column of the first converted-weight slot
-    int conv_slots;             // converted-weight slots in TMEM (NW * 64 columns each)
+    int conv_slots;             // converted-weight slots in TMEM (one chunk each)
     uint32_t s_off;             // NVFP4: first block-scale box within a stage
 };
 
@@ -183,8 +188,15 @@ decode_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
                    const __grid_constant__ CUtensorMap tmS, const DParams p) {
     constexpr bool FP8W = WF != kWeightBf16;               // converted weights (FP8 or NVFP4)
     constexpr bool FP4W = WF == kWeightNvfp4;
-    constexpr int NCH = FP4W ? 2 : 1;                      // 128-wide converted chunks per stage
     constexpr int NW = (MODE == kGemmSwiGLU) ? 2 : 1;      // weight boxes per stage
+    // K per stage: 64 (BF16), 256 (NVFP4; FP8 with one weight box), 128 (FP8
+    // SwiGLU).  K per converted chunk: the whole stage when one weight box fills
+    // a slot, else 128.  Code boxes (128 bytes per row) per weight block.
+    constexpr int KSTEP = FP4W ? DBK4 : (FP8W ? (NW == 1 ? 256 : DBK8) : DBK);
+    constexpr int CK = (FP8W && NW == 1) ? 256 : 128;
+    constexpr int NCH = FP8W ? KSTEP / CK : 1;
+    constexpr int SLOT_COLS = NW * CK / 2;
+    constexpr int NB8 = FP8W && !FP4W ? KSTEP / DBK8 : 1;
     constexpr int NTH = FP8W ? DTHREADS_FP8 : DTHREADS;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -276,9 +288,8 @@ decode_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
     volatile int* abort = &ctl->abort;
     const int ntn = (p.N + DBM - 1) / DBM;
     const int items = ctl->ng * ntn;
-    // K per stage: 64 (BF16 weights), 128 (FP8) or 256 (NVFP4): one 128-byte row
-    // per weight row and TMA request; the MMA takes it in 64-wide activation boxes
-    const int kstep = FP4W ? DBK4 : (FP8W ? DBK8 : DBK);
+    // the MMA takes a stage in 64-wide activation boxes
+    const int kstep = KSTEP;
     const int nkb = (p.K + kstep - 1) / kstep;
     const int nk = nkb * p.nseg;
     const uint32_t xbox = (uint32_t)(p.nb * DBK * 2);        // one activation box (nb rows x 64)
@@ -305,7 +316,10 @@ decode_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
                         mbar_arrive_expect_tx(full, (uint32_t)p.stage_bytes);
                         const uint32_t sa = smem_base + (uint32_t)(stage * p.stage_bytes);
                         const int wcol = FP4W ? kb * (DBK4 / 2) : kb * kstep;     // code bytes
-                        tma_load_2d(sa + w_off, &tmW, full, wcol, w_row + seg * p.b_seg_row);
+#pragma unroll
+                        for (int h = 0; h < NB8; ++h)   // FP8, 256-wide stage: two 128-byte code boxes
+                            tma_load_2d(sa + w_off + (uint32_t)h * w_box, &tmW, full, wcol + h * DBK8,
+                                        w_row + seg * p.b_seg_row);
                         if (MODE == kGemmSwiGLU)
                             tma_load_2d(sa + w_off + w_box, &tmW, full, wcol, w_row + p.up_off + seg * p.b_seg_row);
                         if (FP4W) {     // the rows' block scales of these 256 elements
@@ -345,23 +359,25 @@ decode_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
                         if (!mbar_wait_bounded(smem_u32(&ctl->full[stage]), ph, abort)) { ok = false; break; }
                         const uint32_t sa = smem_base + (uint32_t)(stage * p.stage_bytes);
                         if constexpr (FP8W) {
-                            // each 128-wide chunk ch of the stage's weights, converted to BF16,
-                            // is in a TMEM slot cs: box wb, K half hf at columns
-                            // a_col + cs*NW*64 + wb*64 + hf*32; its activations are boxes 2ch + hf
+                            // each chunk ch (CK wide) of the stage's weights, converted to
+                            // BF16, is in a TMEM slot cs: weight block wb, K element k of
+                            // the chunk at column a_col + cs*SLOT_COLS + wb*CK/2 + k/2; its
+                            // activations are boxes ch*CK/64 .. +CK/64-1
                             for (int ch = 0; ch < NCH && ok; ++ch) {
                                 if (!mbar_wait_bounded(smem_u32(&ctl->cfull[cs]), cph, abort)) { ok = false; break; }
                                 tc_fence_after();
-                                const uint32_t aslot = tmem + p.a_col + (uint32_t)(cs * NW * 64);
+                                const uint32_t aslot = tmem + p.a_col + (uint32_t)(cs * SLOT_COLS);
 #pragma unroll
-                                for (int hf = 0; hf < 2; ++hf) {
-                                    const uint64_t xd = sdesc_k_sw128(sa + x_off + (uint32_t)(2 * ch + hf) * xbox);
+                                for (int xb = 0; xb < CK / 64; ++xb) {
+                                    const uint64_t xd =
+                                        sdesc_k_sw128(sa + x_off + (uint32_t)(ch * (CK / 64) + xb) * xbox);
 #pragma unroll
                                     for (int kk = 0; kk < DBK / 16; ++kk) {
-                                        const uint32_t accum = (i > 0 || ch > 0 || hf > 0 || kk > 0) ? 1u : 0u;
-                                        const uint32_t acol = (uint32_t)(hf * 32 + kk * 8);
+                                        const uint32_t accum = (i > 0 || ch > 0 || xb > 0 || kk > 0) ? 1u : 0u;
+                                        const uint32_t acol = (uint32_t)(xb * 32 + kk * 8);
                                         tc_mma_bf16_ts(d, aslot + acol, xd + (uint64_t)(kk * 2), idesc, accum);
                                         if (MODE == kGemmSwiGLU)
-                                            tc_mma_bf16_ts(d + (uint32_t)nb, aslot + 64 + acol,
+                                            tc_mma_bf16_ts(d + (uint32_t)nb, aslot + CK / 2 + acol,
                                                            xd + (uint64_t)(kk * 2), idesc, accum);
                                     }
                                 }
@@ -403,13 +419,14 @@ decode_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
         }
     } else if (FP8W && warp >= 6) {
         // ---------------- FP8 / NVFP4 -> BF16 converter (warps 6 .. 6 + CONV_WARPS - 1)
-        // A stage's code box is 128 rows x 128 bytes, 128-byte swizzled (16-byte
-        // chunk c of row r at chunk c ^ (r & 7)).  Converter warp w owns TMEM lane
-        // quarter w % 4, i.e. weight rows r = 32*(w % 4) + lane, and K half
-        // hf = (w - 6) / 4 of every 128-wide chunk: each thread decodes its row's
-        // 64 elements of that half (FP8: four conflict-free 16-byte loads; NVFP4:
-        // two, with the row's four block scales of the half) and stores the 32
-        // packed BF16 pairs to its TMEM lane, columns a_col + cs*NW*64 + wb*64 + hf*32.
+        // A code box is 128 rows x 128 bytes, 128-byte swizzled (16-byte chunk c
+        // of row r at chunk c ^ (r & 7)).  Converter warp w owns TMEM lane quarter
+        // w % 4, i.e. weight rows r = 32*(w % 4) + lane, and K half hf = (w - 6) / 4
+        // of every chunk: each thread decodes its row's CK/2 elements of that half
+        // in 64-element sub-blocks (FP8: four conflict-free 16-byte loads each;
+        // NVFP4: two, with the row's four block scales of the sub-block) and stores
+        // each sub-block's 32 packed BF16 pairs to its TMEM lane, columns
+        // a_col + cs*SLOT_COLS + wb*CK/2 + hf*CK/4 + 32*sub-block.
         const int q = warp & 3;
         const int hf = (warp - 6) >> 2;
         const int r = 32 * q + lane;
@@ -433,44 +450,50 @@ decode_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
                         if (!mbar_wait_bounded(smem_u32(&ctl->cempty[cs]), cph ^ 1u, abort)) { ok = false; break; }
                         tc_fence_after();                       // after the MMAs that read slot cs
                         const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + p.a_col +
-                                               (uint32_t)(cs * NW * 64) + (uint32_t)(hf * 32);
+                                               (uint32_t)(cs * SLOT_COLS) + (uint32_t)(hf * (CK / 4));
 #pragma unroll
                         for (int wb = 0; wb < NW; ++wb) {
-                            uint32_t v32[32];
-                            if constexpr (FP4W) {
-                                // block scales of this half's 64 elements: bytes 8ch + 4hf .. +3
-                                const uint32_t s4 = (ch == 0) ? (hf == 0 ? scl[wb].x : scl[wb].y)
-                                                              : (hf == 0 ? scl[wb].z : scl[wb].w);
-                                constexpr uint32_t kTwo118 = 0x7A807A80u;     // (2^118, 2^118) in BF16
-                                uint32_t s01, s23, mb[4];
-                                e4m3x4_to_bf16x4(s4, s01, s23);
-                                asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(s01) : "r"(s01), "r"(kTwo118));
-                                asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(s23) : "r"(s23), "r"(kTwo118));
-                                asm("prmt.b32 %0, %1, 0, 0x1010;" : "=r"(mb[0]) : "r"(s01));
-                                asm("prmt.b32 %0, %1, 0, 0x3232;" : "=r"(mb[1]) : "r"(s01));
-                                asm("prmt.b32 %0, %1, 0, 0x1010;" : "=r"(mb[2]) : "r"(s23));
-                                asm("prmt.b32 %0, %1, 0, 0x3232;" : "=r"(mb[3]) : "r"(s23));
 #pragma unroll
-                                for (int j = 0; j < 2; ++j) {
-                                    const uint4 v = *reinterpret_cast<const uint4*>(
-                                        src + wb * W8_BYTES + (((4 * ch + 2 * hf + j) ^ sw) << 4));
-                                    e2m1x8_to_bf16x8(v.x, mb[2 * j], &v32[16 * j + 0]);
-                                    e2m1x8_to_bf16x8(v.y, mb[2 * j], &v32[16 * j + 4]);
-                                    e2m1x8_to_bf16x8(v.z, mb[2 * j + 1], &v32[16 * j + 8]);
-                                    e2m1x8_to_bf16x8(v.w, mb[2 * j + 1], &v32[16 * j + 12]);
-                                }
-                            } else {
+                            for (int sb = 0; sb < CK / 128; ++sb) {   // 64-element sub-blocks of this half
+                                uint32_t v32[32];
+                                if constexpr (FP4W) {
+                                    const int e0 = ch * CK + hf * (CK / 2) + sb * 64;    // within the stage
+                                    const int wi = e0 >> 6;                               // its 4 block scales
+                                    const uint32_t s4 = wi == 0 ? scl[wb].x : wi == 1 ? scl[wb].y
+                                                      : wi == 2 ? scl[wb].z : scl[wb].w;
+                                    constexpr uint32_t kTwo118 = 0x7A807A80u;     // (2^118, 2^118) in BF16
+                                    uint32_t s01, s23, mb[4];
+                                    e4m3x4_to_bf16x4(s4, s01, s23);
+                                    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(s01) : "r"(s01), "r"(kTwo118));
+                                    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(s23) : "r"(s23), "r"(kTwo118));
+                                    asm("prmt.b32 %0, %1, 0, 0x1010;" : "=r"(mb[0]) : "r"(s01));
+                                    asm("prmt.b32 %0, %1, 0, 0x3232;" : "=r"(mb[1]) : "r"(s01));
+                                    asm("prmt.b32 %0, %1, 0, 0x1010;" : "=r"(mb[2]) : "r"(s23));
+                                    asm("prmt.b32 %0, %1, 0, 0x3232;" : "=r"(mb[3]) : "r"(s23));
 #pragma unroll
-                                for (int j = 0; j < 4; ++j) {
-                                    const uint4 v = *reinterpret_cast<const uint4*>(src + wb * W8_BYTES +
-                                                                                    (((4 * hf + j) ^ sw) << 4));
-                                    e4m3x4_to_bf16x4(v.x, v32[8 * j + 0], v32[8 * j + 1]);
-                                    e4m3x4_to_bf16x4(v.y, v32[8 * j + 2], v32[8 * j + 3]);
-                                    e4m3x4_to_bf16x4(v.z, v32[8 * j + 4], v32[8 * j + 5]);
-                                    e4m3x4_to_bf16x4(v.w, v32[8 * j + 6], v32[8 * j + 7]);
+                                    for (int j = 0; j < 2; ++j) {
+                                        const uint4 v = *reinterpret_cast<const uint4*>(
+                                            src + wb * W8_BYTES + ((((e0 >> 5) + j) ^ sw) << 4));
+                                        e2m1x8_to_bf16x8(v.x, mb[2 * j], &v32[16 * j + 0]);
+                                        e2m1x8_to_bf16x8(v.y, mb[2 * j], &v32[16 * j + 4]);
+                                        e2m1x8_to_bf16x8(v.z, mb[2 * j + 1], &v32[16 * j + 8]);
+                                        e2m1x8_to_bf16x8(v.w, mb[2 * j + 1], &v32[16 * j + 12]);
+                                    }
+                                } else {
+                                    const int e0 = ch * CK + hf * (CK / 2) + sb * 64;    // byte in the stage row
+                                    const uint8_t* bsrc = src + (wb * NB8 + (e0 >> 7)) * W8_BYTES;
+#pragma unroll
+                                    for (int j = 0; j < 4; ++j) {
+                                        const uint4 v = *reinterpret_cast<const uint4*>(
+                                            bsrc + (((((e0 & 127) >> 4) + j) ^ sw) << 4));
+                                        e4m3x4_to_bf16x4(v.x, v32[8 * j + 0], v32[8 * j + 1]);
+                                        e4m3x4_to_bf16x4(v.y, v32[8 * j + 2], v32[8 * j + 3]);
+                                        e4m3x4_to_bf16x4(v.z, v32[8 * j + 4], v32[8 * j + 5]);
+                                        e4m3x4_to_bf16x4(v.w, v32[8 * j + 6], v32[8 * j + 7]);
+                                    }
                                 }
+                                tmem_st_32cols(taddr + (uint32_t)(wb * (CK / 2) + sb * 32), v32);
                             }
-                            tmem_st_32cols(taddr + (uint32_t)(wb * 64), v32);
                         }
                         tmem_st_wait();
                         tc_fence_before();
@@ -621,17 +644,22 @@ moe_status launch_decode_gemm(const GemmProblem& g, int nb, WsHeader* hdr, cudaS
         dp.w_off = (uint32_t)(4 * nb * DBK * 2);
         dp.s_off = dp.w_off + (uint32_t)(nw * W8_BYTES);
         dp.stage_bytes = (int)dp.s_off + nw * S4_BYTES;
-        dp.conv_slots = nw == 2 ? 2 : 3;
-        dp.a_col = 256;
+        // one weight box: whole-stage chunks of 128 columns after at most 128
+        // accumulator columns (3 slots); SwiGLU: 128-wide chunks, 2 slots
+        dp.a_col = nw == 1 ? 128 : 256;
+        dp.conv_slots = nw == 1 ? 3 : 2;
     } else if (fp8) {
-        // stage (K 128): [two activation boxes: nb rows x 128 B each][FP8 weight
-        // box(es): 128 rows x 128 B = 16 KiB each]
+        // stage: one weight box: K 256 = [four activation boxes][two code boxes:
+        // K 0..127 and 128..255 of the 128 rows]; SwiGLU: K 128 = [two activation
+        // boxes][gate and up code boxes].  Boxes of codes are 128 rows x 128 B.
+        const int xboxes = nw == 1 ? 4 : 2;
         dp.x_off = 0;
-        dp.w_off = (uint32_t)(2 * nb * DBK * 2);
-        dp.stage_bytes = 2 * nb * DBK * 2 + nw * W8_BYTES;
-        // TMEM: accumulators in columns 0..255, converted weights from 256 on
-        dp.conv_slots = nw == 2 ? 2 : 3;
-        dp.a_col = 256;
+        dp.w_off = (uint32_t)(xboxes * nb * DBK * 2);
+        dp.stage_bytes = xboxes * nb * DBK * 2 + 2 * W8_BYTES;
+        // TMEM: one weight box: accumulators in columns 0..127, three 128-column
+        // slots; SwiGLU: accumulators in 0..255, two slots of 2 x 64 columns
+        dp.a_col = nw == 1 ? 128 : 256;
+        dp.conv_slots = nw == 1 ? 3 : 2;
     } else {
         // stage: [BF16 weight box(es): 16 KiB each][activation box]
         dp.x_off = (uint32_t)(nw * W_BYTES);
@@ -652,7 +680,7 @@ moe_status launch_decode_gemm(const GemmProblem& g, int nb, WsHeader* hdr, cudaS
     if (grid > sms) grid = sms;
     if (grid < 1) grid = 1;
     const size_t fixed = 1024 + sizeof(DCtl) + (size_t)3 * g.groups * sizeof(int);
-    const int kstep = fp4 ? DBK4 : (fp8 ? DBK8 : DBK);
+    const int kstep = fp4 ? DBK4 : (fp8 ? (nw == 1 ? 256 : DBK8) : DBK);
     const int nk = ((g.K + kstep - 1) / kstep) * g.nseg;
     long long stages = ((long long)MAX_DSMEM - (long long)fixed) / dp.stage_bytes;
     if (stages > MAX_DSTAGES) stages = MAX_DSTAGES;
