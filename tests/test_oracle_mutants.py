@@ -90,6 +90,7 @@ PINS = [
     (P.test_nvfp4_ffn_equals_bf16_path_on_exact_weights, dict(act=0, H=48, I=64)),
     (P.test_nvfp4_ffn_equals_bf16_path_on_exact_weights, dict(act=1, H=288, I=32)),
     (P.test_nvfp4_layer_equals_bf16_layer_on_exact_weights, {}),
+    (P.test_nvfp4_layer_preselected_routes_and_capacity, {}),
 ]
 
 

@@ -630,3 +630,26 @@ def test_nvfp4_layer_equals_bf16_layer_on_exact_weights(oracle_mod):
     assert o4["status"] == ob["status"] == 0
     for key in ("ids", "offsets", "dest", "x_perm", "h", "y_perm", "out"):
         assert np.array_equal(o4[key], ob[key]), key
+
+
+def test_nvfp4_layer_preselected_routes_and_capacity(oracle_mod):
+    """The NVFP4 layer takes the same routing and dispatch as the BF16 layer:
+    preselected routes equal internal routing bitwise, and a bucket over
+    capacity stops the layer before any payload moves."""
+    rng = np.random.default_rng(81)
+    T, E, k, H, I = 20, 5, 2, 64, 32
+    c13, b13, s13, _ = nvfp4_exact_case(rng, E, 2 * I, H)
+    c2, b2, s2, _ = nvfp4_exact_case(rng, E, H, I)
+    x = rand_bf16(rng, (T, H))
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    a = oracle_mod.layer_nvfp4(x, c13, b13, s13, c2, b2, s2, 0, k, T, logits=logits)
+    st, ids, w = oracle_mod.route(logits, k)
+    b = oracle_mod.layer_nvfp4(x, c13, b13, s13, c2, b2, s2, 0, k, T, ids_in=ids, w_in=w)
+    assert a["status"] == b["status"] == 0
+    assert np.array_equal(a["out"], b["out"]) and np.abs(bits_to_f64(a["out"])).max() > 0
+    # every token routed to experts 0 and 1: 20 rows each, capacity 19
+    ids_full = np.tile(np.array([[0, 1]], np.int32), (T, 1))
+    w_full = np.full((T, k), 0.5, np.float32)
+    c = oracle_mod.layer_nvfp4(x, c13, b13, s13, c2, b2, s2, 0, k, T - 1, ids_in=ids_full, w_in=w_full)
+    assert c["status"] == oracle_mod.ST_CAPACITY
+    assert np.all(c["x_perm"] == 0) and np.all(c["out"] == 0)
