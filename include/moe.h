@@ -201,7 +201,10 @@ MOE_API moe_status moe_combine(const moe_shape* shape, const uint16_t* y_perm, c
  * every intermediate in the workspace.  Given the ids and weights moe_route
  * returns, the output is bitwise the same either way (ONNX Runtime PR #33963:
  * internal and preselected routing give bitwise-equal outputs).
- * out: device bf16 [T, H] (may alias residual). */
+ * out: device bf16 [T, H] (may alias residual).
+ * Device errors are those of the stages.  When a bucket exceeds `capacity`
+ * (MOE_ERR_CAPACITY) no payload moves and the expert GEMMs and the combine do
+ * nothing: out (and so an aliased residual) keeps its contents. */
 MOE_API moe_status moe_layer(const moe_shape* shape, const float* logits, const int32_t* ids_in,
                              const float* w_in, const uint16_t* x, const uint16_t* w13,
                              const uint16_t* w2, const uint16_t* ws13, const uint16_t* ws2,
@@ -304,8 +307,36 @@ MOE_API moe_status moe_dispatch_noalloc(const moe_shape* shape, const uint16_t* 
                                         uint16_t* x_perm, int32_t* device_status, void* stream);
 
 /* Synchronise `stream`, return in *device_status the largest status code raised
- * by kernels on this workspace since the last read, and clear it. */
+ * by kernels on this workspace since the last read, and clear it (together
+ * with the timeout site below). */
 MOE_API moe_status moe_status_read(void* ws, void* stream, moe_status* device_status);
+
+/* Test controls of the count kernel's bounded look-back wait, modelled on the
+ * afdEP-comm count-first record's bounded timeout_while spins and its must-fail
+ * case of counts that never arrive (.faults_shipped), injected from the host:
+ * nothing here faults, traps or hangs a GPU.
+ *   lookback_wait_ns  how long a count tile waits for a predecessor tile's
+ *                     published counts before it gives up, raising
+ *                     MOE_ERR_TIMEOUT (site 1); 0 restores the default 2 s.
+ *   count_tile_skip   0 (normal) or 1.  With 1 the count kernel hands out tile
+ *                     ids from 1, so no block ever publishes tile 0's counts:
+ *                     on a dispatch of more than one count tile (T*k > 1024
+ *                     pairs) the look-back waits for a flag that nothing sets
+ *                     and gives up after lookback_wait_ns.  The dispatch's
+ *                     outputs are then unspecified; every access stays inside
+ *                     the buffers.  A single-tile dispatch is unaffected.
+ * Both settings stay in the workspace header until changed (moe_workspace_init
+ * resets them to 0) and apply to moe_dispatch and moe_layer calls on it.  The
+ * GEMM kernels' waits keep their fixed 2 s limit.  Enqueued on `stream`.
+ * Host error: MOE_ERR_INVALID_ARG for a bad workspace or count_tile_skip. */
+MOE_API moe_status moe_workspace_set_wait(void* ws, size_t ws_bytes, uint64_t lookback_wait_ns,
+                                          int32_t count_tile_skip, void* stream);
+
+/* Synchronise `stream` and return in *site where the last bounded wait that
+ * ran out on this workspace gave up: 0 none, 1 the count kernel's look-back,
+ * 2 a GEMM TMA producer, 3 a GEMM MMA issuer, 4 a GEMM epilogue, 5 the
+ * small-row GEMM.  Read it before moe_status_read, which clears it. */
+MOE_API moe_status moe_timeout_site_read(void* ws, void* stream, int32_t* site);
 
 /* A static, human-readable name for a status code. */
 MOE_API const char* moe_status_string(moe_status status);

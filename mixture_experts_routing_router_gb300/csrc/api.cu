@@ -96,8 +96,11 @@ moe_status do_dispatch(const moe_shape& s, const uint16_t* x, const int32_t* ids
     return from_cuda(launch_scatter(s, x, ids, offsets, rank, dest, sorted_pair, x_perm, hdr, st));
 }
 
+// `gated` (moe_layer): the GEMMs and the combine skip their work when this
+// call's dispatch found a bucket over capacity, so no output is touched.
 moe_status do_up(const moe_shape& s, const uint16_t* x_perm, const int32_t* offsets, const uint16_t* w13,
-                 const uint16_t* x, const uint16_t* ws13, uint16_t* h, void* ws, cudaStream_t st) {
+                 const uint16_t* x, const uint16_t* ws13, uint16_t* h, void* ws, cudaStream_t st,
+                 bool gated = false) {
     const WsLayout L = ws_layout(s);
     WsHeader* hdr = at<WsHeader>(ws, 0);
     const long long R = (long long)s.tokens * s.top_k;
@@ -111,6 +114,7 @@ moe_status do_up(const moe_shape& s, const uint16_t* x_perm, const int32_t* offs
     g.N = s.inter; g.b_group_rows = up_rows(s, s.inter); g.up_off = s.inter;
     g.out = h; g.ldo = s.inter; g.out_group_col = 0;
     g.max_group_rows = s.tokens;   // a token's k experts are distinct
+    g.gated = gated;
     moe_status r = launch_grouped_gemm(g, hdr, st);
     if (r != MOE_OK || s.shared == 0) return r;
     GemmProblem q{};
@@ -122,11 +126,13 @@ moe_status do_up(const moe_shape& s, const uint16_t* x_perm, const int32_t* offs
     q.K = s.hidden; q.nseg = 1; q.a_seg_col = 0; q.b_seg_row = 0;
     q.N = Is; q.b_group_rows = up_rows(s, Is); q.up_off = Is;
     q.out = at<uint16_t>(ws, L.h_shared); q.ldo = (long long)s.shared * Is; q.out_group_col = Is;
+    q.gated = gated;
     return launch_grouped_gemm(q, hdr, st);
 }
 
 moe_status do_down(const moe_shape& s, const uint16_t* h, const int32_t* offsets, const uint16_t* w2,
-                   const uint16_t* ws2, uint16_t* y_perm, uint16_t* y_shared, void* ws, cudaStream_t st) {
+                   const uint16_t* ws2, uint16_t* y_perm, uint16_t* y_shared, void* ws, cudaStream_t st,
+                   bool gated = false) {
     const WsLayout L = ws_layout(s);
     WsHeader* hdr = at<WsHeader>(ws, 0);
     const long long R = (long long)s.tokens * s.top_k;
@@ -139,6 +145,7 @@ moe_status do_down(const moe_shape& s, const uint16_t* h, const int32_t* offsets
     g.N = s.hidden; g.b_group_rows = s.hidden; g.up_off = 0;
     g.out = y_perm; g.ldo = s.hidden; g.out_group_col = 0;
     g.max_group_rows = s.tokens;
+    g.gated = gated;
     moe_status r = launch_grouped_gemm(g, hdr, st);
     if (r != MOE_OK || s.shared == 0) return r;
     // all shared experts in one accumulation: K runs over (s, n), so their sum
@@ -152,6 +159,7 @@ moe_status do_down(const moe_shape& s, const uint16_t* h, const int32_t* offsets
     q.K = Is; q.nseg = s.shared; q.a_seg_col = Is; q.b_seg_row = s.hidden;
     q.N = s.hidden; q.b_group_rows = 0; q.up_off = 0;
     q.out = y_shared; q.ldo = s.hidden; q.out_group_col = 0;
+    q.gated = gated;
     return launch_grouped_gemm(q, hdr, st);
 }
 
@@ -160,7 +168,8 @@ moe_status do_down(const moe_shape& s, const uint16_t* h, const int32_t* offsets
 size_t nvfp4_bscale_stride(int K) { return 16 * (size_t)((K + 255) / 256); }
 
 moe_status do_up_q(const moe_shape& s, const uint16_t* x_perm, const int32_t* offsets, const uint8_t* w13,
-                   const uint8_t* b13, const float* s13, int wfmt, uint16_t* h, void* ws, cudaStream_t st) {
+                   const uint8_t* b13, const float* s13, int wfmt, uint16_t* h, void* ws, cudaStream_t st,
+                   bool gated = false) {
     const long long R = (long long)s.tokens * s.top_k;
     GemmProblem g{};
     g.mode = s.act == MOE_ACT_SWIGLU ? kGemmSwiGLU : kGemmReLU2;
@@ -173,11 +182,13 @@ moe_status do_up_q(const moe_shape& s, const uint16_t* x_perm, const int32_t* of
     g.max_group_rows = s.tokens;
     g.wfmt = wfmt; g.wscale = s13;
     g.bscale = b13; g.bscale_stride = (long long)nvfp4_bscale_stride(s.hidden);
+    g.gated = gated;
     return launch_grouped_gemm(g, at<WsHeader>(ws, 0), st);
 }
 
 moe_status do_down_q(const moe_shape& s, const uint16_t* h, const int32_t* offsets, const uint8_t* w2,
-                     const uint8_t* b2, const float* s2, int wfmt, uint16_t* y_perm, void* ws, cudaStream_t st) {
+                     const uint8_t* b2, const float* s2, int wfmt, uint16_t* y_perm, void* ws, cudaStream_t st,
+                     bool gated = false) {
     const long long R = (long long)s.tokens * s.top_k;
     GemmProblem g{};
     g.mode = kGemmPlain;
@@ -190,6 +201,7 @@ moe_status do_down_q(const moe_shape& s, const uint16_t* h, const int32_t* offse
     g.max_group_rows = s.tokens;
     g.wfmt = wfmt; g.wscale = s2;
     g.bscale = b2; g.bscale_stride = (long long)nvfp4_bscale_stride(s.inter);
+    g.gated = gated;
     return launch_grouped_gemm(g, at<WsHeader>(ws, 0), st);
 }
 
@@ -212,8 +224,9 @@ moe_status check_quant_shape(const moe_shape* s, int wfmt) {
 }
 
 moe_status do_combine(const moe_shape& s, const uint16_t* y_perm, const int32_t* dest, const float* w,
-                      const uint16_t* y_shared, const uint16_t* residual, uint16_t* out, cudaStream_t st) {
-    return from_cuda(launch_combine(s, y_perm, dest, w, y_shared, residual, out, st));
+                      const uint16_t* y_shared, const uint16_t* residual, uint16_t* out, cudaStream_t st,
+                      const WsHeader* gate = nullptr) {
+    return from_cuda(launch_combine(s, y_perm, dest, w, y_shared, residual, out, gate, st));
 }
 
 moe_status expert_up_q(const moe_shape* shape, const uint16_t* x_perm, const int32_t* offsets, const uint8_t* w13,
@@ -288,9 +301,9 @@ moe_status layer_q(const moe_shape* shape, const float* logits, const int32_t* i
                                 x_perm, ws, st)) != MOE_OK) {
         return r;
     }
-    if ((r = do_up_q(s, x_perm, offsets, w13, w13_bscale, w13_scale, wfmt, h, ws, st)) != MOE_OK) return r;
-    if ((r = do_down_q(s, h, offsets, w2, w2_bscale, w2_scale, wfmt, y_perm, ws, st)) != MOE_OK) return r;
-    return do_combine(s, y_perm, dest, w, nullptr, residual, out, st);
+    if ((r = do_up_q(s, x_perm, offsets, w13, w13_bscale, w13_scale, wfmt, h, ws, st, true)) != MOE_OK) return r;
+    if ((r = do_down_q(s, h, offsets, w2, w2_bscale, w2_scale, wfmt, y_perm, ws, st, true)) != MOE_OK) return r;
+    return do_combine(s, y_perm, dest, w, nullptr, residual, out, st, at<WsHeader>(ws, 0));
 }
 
 }  // namespace
@@ -464,9 +477,9 @@ moe_status moe_layer(const moe_shape* shape, const float* logits, const int32_t*
                                 x_perm, ws, st)) != MOE_OK) {
         return r;
     }
-    if ((r = do_up(s, x_perm, offsets, w13, x, ws13, h, ws, st)) != MOE_OK) return r;
-    if ((r = do_down(s, h, offsets, w2, ws2, y_perm, y_shared, ws, st)) != MOE_OK) return r;
-    return do_combine(s, y_perm, dest, w, y_shared, residual, out, st);
+    if ((r = do_up(s, x_perm, offsets, w13, x, ws13, h, ws, st, true)) != MOE_OK) return r;
+    if ((r = do_down(s, h, offsets, w2, ws2, y_perm, y_shared, ws, st, true)) != MOE_OK) return r;
+    return do_combine(s, y_perm, dest, w, y_shared, residual, out, st, at<WsHeader>(ws, 0));
 }
 
 moe_status moe_expert_up_fp8(const moe_shape* shape, const uint16_t* x_perm, const int32_t* offsets,
@@ -506,6 +519,25 @@ moe_status moe_layer_nvfp4(const moe_shape* shape, const float* logits, const in
                            const uint16_t* residual, uint16_t* out, void* ws, size_t ws_bytes, void* stream) {
     return layer_q(shape, logits, ids_in, w_in, x, w13, w13_bscale, w13_scale, w2, w2_bscale, w2_scale,
                    kWeightNvfp4, residual, out, ws, ws_bytes, stream);
+}
+
+moe_status moe_workspace_set_wait(void* ws, size_t ws_bytes, uint64_t lookback_wait_ns, int32_t count_tile_skip,
+                                  void* stream) {
+    clear_error();
+    if (!aligned(ws, 256) || ws_bytes < 4096) return MOE_ERR_INVALID_ARG;
+    if (count_tile_skip != 0 && count_tile_skip != 1) return MOE_ERR_INVALID_ARG;
+    return from_cuda(launch_set_wait(at<WsHeader>(ws, 0), (unsigned long long)lookback_wait_ns, count_tile_skip,
+                                     static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_timeout_site_read(void* ws, void* stream, int32_t* site) {
+    if (!aligned(ws, 256) || !site) return MOE_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    WsHeader h;
+    if (cudaMemcpyAsync(&h, ws, sizeof(h), cudaMemcpyDeviceToHost, st) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+    *site = h.timeout_site;
+    return MOE_OK;
 }
 
 moe_status moe_status_read(void* ws, void* stream, moe_status* device_status) {

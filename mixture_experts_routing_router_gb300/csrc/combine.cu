@@ -30,9 +30,11 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __global__ void __launch_bounds__(256)
 combine_kernel(int T, int HV, int k, const uint4* __restrict__ y_perm, const int32_t* __restrict__ dest,
                const float* __restrict__ w, const uint4* __restrict__ y_shared, const uint4* residual,
-               uint4* out) {   // out may alias residual: each 16-byte group is read, then written, by one thread
+               uint4* out,     // out may alias residual: each 16-byte group is read, then written, by one thread
+               const WsHeader* gate) {
     pdl_wait();
     pdl_trigger();
+    if (gate && gate->cap_exceeded) return;     // over capacity in this layer call: out stays untouched
     __shared__ int dsh[32];
     __shared__ float wsh[32];
     const long long R = (long long)T * k;
@@ -76,7 +78,8 @@ combine_kernel(int T, int HV, int k, const uint4* __restrict__ y_perm, const int
 }  // namespace
 
 cudaError_t launch_combine(const moe_shape& s, const uint16_t* y_perm, const int32_t* dest, const float* w,
-                           const uint16_t* y_shared, const uint16_t* residual, uint16_t* out, cudaStream_t st) {
+                           const uint16_t* y_shared, const uint16_t* residual, uint16_t* out, const WsHeader* gate,
+                           cudaStream_t st) {
     const int HV = s.hidden / 8;
     int threads = 32;
     while (threads < 256 && threads < HV) threads *= 2;
@@ -89,7 +92,7 @@ cudaError_t launch_combine(const moe_shape& s, const uint16_t* y_perm, const int
     const bool pdl = kUsePdl && s.tokens <= kDecodeRows;
     return launch_kernel(combine_kernel, dim3((unsigned)blocks), dim3(threads), 0, st, 1, pdl, s.tokens, HV,
                          s.top_k, reinterpret_cast<const uint4*>(y_perm), dest, w, reinterpret_cast<const uint4*>(y_shared),
-                         reinterpret_cast<const uint4*>(residual), reinterpret_cast<uint4*>(out));
+                         reinterpret_cast<const uint4*>(residual), reinterpret_cast<uint4*>(out), gate);
 }
 
 }  // namespace moe

@@ -29,6 +29,10 @@ struct WsHeader {
     int timeout_site;       // which bounded wait gave up (diagnostic)
     unsigned tile_counter;  // dynamic tile ids of the count kernel (reset per dispatch)
     int cap_exceeded;       // this dispatch's capacity verdict (written by the count kernel)
+    // test controls (moe_workspace_set_wait); zero = normal operation
+    unsigned long long lookback_wait_ns;   // look-back give-up time; 0 = kWaitLimitNs
+    int count_tile_skip;                   // first tile id the count kernel hands out (0 or 1)
+    int pad_;
 };
 
 constexpr int kCountChunk = 1024;      // pairs per count tile (one 256-thread block)
@@ -142,6 +146,28 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
             if (globaltimer_ns() - t0 > kWaitLimitNs) { *abort = 1; return false; }
         }
     }
+}
+
+// After a TMA producer gave up: wait (bounded, on a never-set abort flag of its
+// own) for the full-barrier phases of the last stages it armed, so that no bulk
+// copy it issued is still writing this CTA's shared memory when the CTA exits.
+// `armed` counts the stages armed since the kernel began; the ring has `stages`
+// slots whose full barriers are 8 bytes apart from `full0`.  Returns false if
+// some phase did not complete within the limit.
+__device__ __forceinline__ bool wait_armed_stages(uint32_t full0, int stages, long long armed) {
+    volatile int never = 0;
+    bool all = true;
+    for (long long j = armed > stages ? armed - stages : 0; j < armed; ++j) {
+        const uint32_t bar = full0 + 8u * (uint32_t)(j % stages);
+        if (!mbar_wait_bounded(bar, (uint32_t)((j / stages) & 1), &never)) all = false;
+    }
+    return all;
+}
+
+// Last resort after wait_armed_stages failed: a fixed 1 ms delay.
+__device__ __forceinline__ void settle_delay() {
+    const unsigned long long t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 1000000ull) { }
 }
 
 // ---- programmatic dependent launch ----------------------------------------------
@@ -321,9 +347,14 @@ constexpr int kSmallDispatchTokens = 16;
 cudaError_t launch_small_dispatch(const moe_shape& s, const float* logits, const int32_t* ids_in, int32_t* ids_out,
                                   float* w_out, const uint16_t* x, int32_t* counts, int32_t* offsets, int32_t* dest,
                                   int32_t* sorted_pair, uint16_t* x_perm, WsHeader* hdr, cudaStream_t st);
+// gate: NULL, or (inside moe_layer) the workspace header whose capacity verdict,
+// when set, makes the kernel leave `out` untouched.
 cudaError_t launch_combine(const moe_shape& s, const uint16_t* y_perm, const int32_t* dest,
                            const float* w, const uint16_t* y_shared, const uint16_t* residual, uint16_t* out,
-                           cudaStream_t st);
+                           const WsHeader* gate, cudaStream_t st);
+// The test controls of the look-back wait (moe_workspace_set_wait).
+cudaError_t launch_set_wait(WsHeader* hdr, unsigned long long lookback_wait_ns, int count_tile_skip,
+                            cudaStream_t st);
 
 // Launch with programmatic stream serialization (the kernel may start while
 // the preceding kernel of the stream finishes; it waits in pdl_wait), and an
@@ -378,6 +409,8 @@ struct GemmProblem {
     const float* wscale;                                  // FP8, NVFP4: FP32 scale per B row
     const uint8_t* bscale;                                // NVFP4: E4M3 scale per 16 K elements
     long long bscale_stride;                              // NVFP4: bytes per B row of bscale
+    int gated;                                            // 1: do nothing if this layer's dispatch
+                                                          //    exceeded the capacity (hdr->cap_exceeded)
 };
 constexpr int kWeightBf16 = 0;
 constexpr int kWeightFp8E4M3 = 1;   // one E4M3 code per element (b_cols bytes per row)

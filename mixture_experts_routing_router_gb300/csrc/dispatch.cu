@@ -45,7 +45,16 @@ clear_lookback_kernel(unsigned long long* flags, long long n, WsHeader* hdr) {
     pdl_trigger();
     const long long i0 = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     for (long long i = i0; i < n; i += (long long)gridDim.x * blockDim.x) flags[i] = 0ull;
-    if (i0 == 0) hdr->tile_counter = 0u;
+    // normally 0; a test may start the ids at 1 (moe_workspace_set_wait)
+    if (i0 == 0) hdr->tile_counter = hdr->count_tile_skip == 1 ? 1u : 0u;
+}
+
+// The test controls of a workspace's look-back wait, written in stream order.
+__global__ void set_wait_kernel(WsHeader* hdr, unsigned long long lookback_wait_ns, int count_tile_skip) {
+    pdl_wait();
+    pdl_trigger();
+    hdr->lookback_wait_ns = lookback_wait_ns;
+    hdr->count_tile_skip = count_tile_skip;
 }
 
 __global__ void __launch_bounds__(kCountThreads)
@@ -67,7 +76,8 @@ count_kernel(long long R, int k, int E, int capacity, const int32_t* __restrict_
     for (int e = tid; e < E; e += kCountThreads) hist[e] = 0;
     __syncthreads();
     const unsigned tile = tile_s;
-    if (tile >= (unsigned)ntiles) return;            // cannot happen with grid == ntiles
+    if (tile >= (unsigned)ntiles) return;            // only with a skipped first tile
+    const unsigned long long wait_ns = hdr->lookback_wait_ns ? hdr->lookback_wait_ns : kWaitLimitNs;
     const long long p0 = (long long)tile * kCountChunk;
 
     int item_e[kItems], item_r[kItems];
@@ -120,7 +130,7 @@ count_kernel(long long R, int k, int E, int capacity, const int32_t* __restrict_
                 const unsigned long long st = f & 0xffffffff00000000ull;
                 if (st == 0) {
                     if (++spins == 64) t0 = globaltimer_ns();
-                    if (spins > 64 && (spins & 63u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) {
+                    if (spins > 64 && (spins & 63u) == 0 && globaltimer_ns() - t0 > wait_ns) {
                         raise_status(hdr, MOE_ERR_TIMEOUT);
                         hdr->timeout_site = kSiteLookback;
                         break;
@@ -256,6 +266,10 @@ cudaError_t launch_count(const moe_shape& s, const int32_t* ids, int32_t* counts
     const size_t smem = (size_t)2 * s.experts * sizeof(int);
     return launch_kernel(count_kernel, dim3((unsigned)count_tiles), dim3(kCountThreads), smem, st, 1, kUsePdl, R,
                          s.top_k, s.experts, s.capacity, ids, counts, offsets, rank, flags, count_tiles, hdr);
+}
+
+cudaError_t launch_set_wait(WsHeader* hdr, unsigned long long lookback_wait_ns, int count_tile_skip, cudaStream_t st) {
+    return launch_kernel(set_wait_kernel, dim3(1), dim3(1), 0, st, 1, kUsePdl, hdr, lookback_wait_ns, count_tile_skip);
 }
 
 cudaError_t launch_scatter(const moe_shape& s, const uint16_t* x, const int32_t* ids, const int32_t* offsets,

@@ -94,6 +94,7 @@ struct KParams {
     long long ldo;
     int out_group_col;
     WsHeader* hdr;
+    int gated;                  // 1: no tiles when hdr->cap_exceeded (the layer's capacity verdict)
 };
 
 template <int HALVES>
@@ -281,10 +282,16 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     }
     pdl_wait();
     pdl_trigger();
+    // After a capacity overflow in the same layer call no payload moved: leave
+    // the outputs alone (no tiles).
+    const bool skip = p.gated && p.hdr->cap_exceeded;
     // Group rows.  Each bucket is clamped to [0, a_rows] on its own, so even
     // malformed offsets keep every row access inside A and the output.
     for (int g = tid; g < p.groups; g += C::THREADS) {
-        if (p.offsets) {
+        if (skip) {
+            rstart[g] = 0;
+            rcount[g] = 0;
+        } else if (p.offsets) {
             int lo = p.offsets[g], hi = p.offsets[g + 1];
             lo = lo < 0 ? 0 : (lo > p.a_rows ? p.a_rows : lo);
             hi = hi < lo ? lo : (hi > p.a_rows ? p.a_rows : hi);
@@ -338,6 +345,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             int stage = 0;
             uint32_t ph = 0;
             bool ok = true;
+            long long armed = 0;
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
                 const Tile t = decode_tile<MODE == kGemmSwiGLU || MODE == kGemmReLU2>(tile, prefix, rstart, rcount, p, ntn, C::BMT);
                 const int a_row = t.row0 + t.mt * C::BMT;
@@ -358,13 +366,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     if (second) tma_load_2d(sa + A_BYTES, &tmA, full, ax, a_row + BM);
                     tma_load_2d(sb, &tmB, full, kb * BK, b_lo + seg * p.b_seg_row);
                     tma_load_2d(sb + B_HALF_BYTES, &tmB, full, kb * BK, b_hi + seg * p.b_seg_row);
+                    ++armed;
                     if (++stage == C::STAGES) { stage = 0; ph ^= 1u; }
                 }
             }
             if (!ok) {
-                // let copies already issued land before the CTA exits
-                const unsigned long long t0 = globaltimer_ns();
-                while (globaltimer_ns() - t0 < 1000000ull) { }
+                // let the copies already issued land before the CTA exits
+                if (!wait_armed_stages(smem_u32(&ctl->full[0]), C::STAGES, armed)) settle_delay();
                 raise_status(p.hdr, MOE_ERR_TIMEOUT);
                 p.hdr->timeout_site = kSiteGemmProducer;
             }
@@ -542,8 +550,12 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
     }
     pdl_wait();
     pdl_trigger();
+    const bool skip = p.gated && p.hdr->cap_exceeded;   // as in grouped_gemm_kernel
     for (int g = tid; g < p.groups; g += P_THREADS) {
-        if (p.offsets) {
+        if (skip) {
+            rstart[g] = 0;
+            rcount[g] = 0;
+        } else if (p.offsets) {
             int lo = p.offsets[g], hi = p.offsets[g + 1];
             lo = lo < 0 ? 0 : (lo > p.a_rows ? p.a_rows : lo);
             hi = hi < lo ? lo : (hi > p.a_rows ? p.a_rows : hi);
@@ -598,6 +610,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
             int stage = 0;
             uint32_t ph = 0;
             bool ok = true;
+            long long armed = 0;
             for (int tile = pair; tile < total && ok; tile += npairs) {
                 const Tile t = decode_tile<MODE == kGemmSwiGLU || MODE == kGemmReLU2>(tile, prefix, rstart, rcount, p, ntn, P_BMT);
                 const int rows_t = t.mrows - t.mt * P_BMT;             // rows of this tile
@@ -628,12 +641,16 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
                     } else {
                         tma_load_2d_pair(s_w, &tmB, full_leader, kb * BK, b_row + seg * p.b_seg_row);
                     }
+                    ++armed;
                     if (++stage == P_STAGES) { stage = 0; ph ^= 1u; }
                 }
             }
             if (!ok) {
-                const unsigned long long t0 = globaltimer_ns();
-                while (globaltimer_ns() - t0 < 1000000ull) { }
+                // Both CTAs' copies of a stage complete on the leader's full barrier,
+                // armed for the pair's bytes: the leader waits for the phases it armed
+                // (and the closing cluster barrier holds the peer until then); the
+                // peer, which cannot wait on a remote barrier, adds the fixed delay.
+                if (rank != 0 || !wait_armed_stages(smem_u32(&ctl->full[0]), P_STAGES, armed)) settle_delay();
                 raise_status(p.hdr, MOE_ERR_TIMEOUT);
                 p.hdr->timeout_site = kSiteGemmProducer;
             }
@@ -955,6 +972,7 @@ moe_status launch_grouped_gemm(const GemmProblem& g, WsHeader* hdr, cudaStream_t
     kp.ldo = g.ldo;
     kp.out_group_col = g.out_group_col;
     kp.hdr = hdr;
+    kp.gated = g.gated;
     if (pairs) {
         const size_t smem = pair_smem_bytes(g.groups);
         if (smem > (size_t)MAX_DYN_SMEM) {

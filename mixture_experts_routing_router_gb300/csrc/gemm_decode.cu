@@ -78,6 +78,7 @@ struct DParams {
     long long ldo;
     int out_group_col;
     WsHeader* hdr;
+    int gated;                  // 1: no work items when hdr->cap_exceeded (the layer's capacity verdict)
     int nb;                     // activation rows per chunk (MMA N): 16, 32, 48 or 64
     int stages, stage_bytes;
     uint32_t tmem_cols;         // two accumulators of (SwiGLU ? 2 : 1) * nb columns, power of two
@@ -239,9 +240,13 @@ decode_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
     }
     pdl_wait();
     pdl_trigger();
+    // after a capacity overflow in the same layer call no payload moved: no items
+    const bool skip = p.gated && p.hdr->cap_exceeded;
 
     // ---- the non-empty groups (block-wide compaction of the offsets) --------
-    if (p.offsets) {
+    if (skip) {
+        if (tid == 0) ctl->ng = 0;
+    } else if (p.offsets) {
         const int per = (p.groups + NTH - 1) / NTH;
         const int g0 = tid * per;
         int cnt = 0;
@@ -304,6 +309,7 @@ decode_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
             int stage = 0;
             uint32_t ph = 0;
             bool ok = true;
+            long long armed = 0;
             for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
                 const int slot = it / ntn, nt = it - slot * ntn;
                 const int g = gid[slot], row0 = gst[slot], rows = gcnt[slot];
@@ -330,14 +336,14 @@ decode_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
                         for (int xb = 0; xb < kstep / DBK; ++xb)   // 64-wide activation boxes
                             tma_load_2d(sa + x_off + (uint32_t)xb * xbox, &tmX, full,
                                         seg * p.a_seg_col + kb * kstep + xb * DBK, xr);
+                        ++armed;
                         if (++stage == p.stages) { stage = 0; ph ^= 1u; }
                     }
                 }
             }
             if (!ok) {
-                // let copies already issued land before the CTA exits
-                const unsigned long long t0 = globaltimer_ns();
-                while (globaltimer_ns() - t0 < 1000000ull) { }
+                // let the copies already issued land before the CTA exits
+                if (!wait_armed_stages(smem_u32(&ctl->full[0]), p.stages, armed)) settle_delay();
                 raise_status(p.hdr, MOE_ERR_TIMEOUT);
                 p.hdr->timeout_site = kSiteGemmDecode;
             }
@@ -634,6 +640,7 @@ moe_status launch_decode_gemm(const GemmProblem& g, int nb, WsHeader* hdr, cudaS
     dp.ldo = g.ldo;
     dp.out_group_col = g.out_group_col;
     dp.hdr = hdr;
+    dp.gated = g.gated;
     dp.nb = nb;
     dp.wscale = g.wscale;
     dp.s_off = 0;

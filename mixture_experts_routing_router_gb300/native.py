@@ -34,7 +34,8 @@ EXPORTS = ("moe_workspace_size", "moe_workspace_init", "moe_route", "moe_dispatc
            "moe_expert_down", "moe_expert_ffn", "moe_combine", "moe_layer", "moe_status_read",
            "moe_status_string", "moe_last_error_message", "moe_dispatch_noalloc", "moe_gate",
            "moe_route_sigmoid", "moe_expert_up_fp8", "moe_expert_down_fp8", "moe_layer_fp8",
-           "moe_expert_up_nvfp4", "moe_expert_down_nvfp4", "moe_layer_nvfp4")
+           "moe_expert_up_nvfp4", "moe_expert_down_nvfp4", "moe_layer_nvfp4", "moe_workspace_set_wait",
+           "moe_timeout_site_read")
 
 
 class MoEError(RuntimeError):
@@ -96,6 +97,8 @@ def lib():
                 "moe_expert_up_nvfp4": [SP, P, P, P, P, P, P, P, S, P],
                 "moe_expert_down_nvfp4": [SP, P, P, P, P, P, P, P, S, P],
                 "moe_layer_nvfp4": [SP, P, P, P, P, P, P, P, P, P, P, P, P, P, S, P],
+                "moe_workspace_set_wait": [P, S, ctypes.c_uint64, ctypes.c_int32, P],
+                "moe_timeout_site_read": [P, P, ctypes.POINTER(ctypes.c_int32)],
             }
             for name, args in sig.items():
                 fn = getattr(L, name)
@@ -273,3 +276,15 @@ def moe_status_read(ws, stream=None) -> int:
     st = ctypes.c_int(0)
     _check(lib().moe_status_read(_ptr(ws), _stream(stream), ctypes.byref(st)), "moe_status_read")
     return st.value
+
+
+def moe_workspace_set_wait(ws, lookback_wait_ns: int, count_tile_skip: int = 0, stream=None):
+    """Test controls of the count kernel's bounded look-back wait."""
+    _check(lib().moe_workspace_set_wait(_ptr(ws), _wsb(ws), int(lookback_wait_ns), int(count_tile_skip),
+                                        _stream(stream)), "moe_workspace_set_wait")
+
+
+def moe_timeout_site_read(ws, stream=None) -> int:
+    site = ctypes.c_int32(0)
+    _check(lib().moe_timeout_site_read(_ptr(ws), _stream(stream), ctypes.byref(site)), "moe_timeout_site_read")
+    return site.value

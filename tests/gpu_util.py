@@ -8,6 +8,9 @@ to the oracle.
 """
 from __future__ import annotations
 
+import concurrent.futures as cf
+import os
+
 import numpy as np
 import torch
 
@@ -88,28 +91,32 @@ def run_layer(wl, g, preselected=None, stream=None):
     return out, N.moe_status_read(ws, stream)
 
 
-def oracle_expert_rows(wl, g, x_host, rows_tok, rows_exp):
-    """Oracle h and y for routed rows given (token, expert) pairs, from generator inputs only."""
-    hs, ys = [], []
-    cache = {}
-    for t, e in zip(rows_tok, rows_exp):
-        if e not in cache:
-            cache[e] = (bits(g["w13"][e]), bits(g["w2"][e]))
-        w13e, w2e = cache[e]
-        h, y = oracle.expert_row(x_host[t], w13e, w2e, wl.act)
-        hs.append(h)
-        ys.append(y)
-    return np.stack(hs), np.stack(ys)
+def oracle_threads() -> int:
+    """Host threads for the oracle's independent rows (ctypes releases the GIL
+    inside the C++ oracle, which keeps no shared state between calls)."""
+    return max(1, min(os.cpu_count() or 1, 32))
 
 
-def oracle_token_out(wl, g, x_host, ids_o, w_o, tokens, shared_w=None):
-    """Oracle out rows of sampled tokens: k routed rows each, then the combine
-    (plus the shared experts), all from generator inputs."""
-    outs = []
-    for t in tokens:
-        _, ys = oracle_expert_rows(wl, g, x_host, [t] * wl.top_k, list(ids_o[t]))
-        ysh = None
-        if wl.shared:
-            _, ysh = oracle.shared_row(x_host[t], shared_w[0], shared_w[1], wl.act)
-        outs.append(oracle.combine_row(ys, np.arange(wl.top_k, dtype=np.int32), w_o[t], ysh))
-    return np.stack(outs)
+def oracle_rows_parallel(wl, g, x_host, pairs):
+    """Oracle (h, y) of routed rows, given unique (token, expert) pairs, from
+    generator inputs only.  Rows are grouped by expert so each expert's
+    weights are copied to the host once; the rows of an expert run on a pool
+    of host threads.  -> dict (token, expert) -> (h_row, y_row)."""
+    by_e = {}
+    for t, e in pairs:
+        by_e.setdefault(int(e), []).append(int(t))
+    res = {}
+    with cf.ThreadPoolExecutor(oracle_threads()) as ex:
+        for e, toks in sorted(by_e.items()):
+            w13e, w2e = bits(g["w13"][e]), bits(g["w2"][e])
+            for t, hy in zip(toks, ex.map(lambda t: oracle.expert_row(x_host[t], w13e, w2e, wl.act), toks)):
+                res[(t, e)] = hy
+    return res
+
+
+def oracle_shared_rows_parallel(wl, g, x_host, tokens):
+    """Oracle y_shared rows of the given tokens (generator inputs only)."""
+    ws13, ws2 = bits(g["ws13"]), bits(g["ws2"])
+    with cf.ThreadPoolExecutor(oracle_threads()) as ex:
+        ys = list(ex.map(lambda t: oracle.shared_row(x_host[t], ws13, ws2, wl.act)[1], tokens))
+    return np.stack(ys)

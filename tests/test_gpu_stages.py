@@ -13,8 +13,7 @@ import oracle
 from mixture_experts_routing_router_gb300 import native as N
 from mixture_experts_routing_router_gb300 import synth
 
-from gpu_util import (W_TOL, alloc_stage_outputs, assert_close, bits, dev, f32_dev, i32_dev, inputs,
-                      oracle_expert_rows, to_bf16_dev)
+from gpu_util import W_TOL, alloc_stage_outputs, assert_close, bits, dev, f32_dev, i32_dev, inputs, to_bf16_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -260,35 +259,6 @@ def test_expert_ffn_buckets_above_the_row_bound(act):
     N.moe_expert_down(shape, to_bf16_dev(h_ref), i32_dev(offsets), g["w2"], None, o["y_perm"], None, ws)
     assert N.moe_status_read(ws) == N.MOE_OK
     assert_close(bits(o["y_perm"]), y_ref, "chunked y_perm")
-
-
-@pytest.mark.parametrize("name", ["count_first", "deepseek", "large"])
-def test_expert_up_sampled_rows_full_size(name):
-    """Full-size up projection (the bench's launch configuration) checked on
-    sampled rows: the first and last row of the hottest, the coldest non-empty
-    and a few random buckets."""
-    wl = W[name]
-    g = inputs(wl, seed=0)
-    lg = g["logits"].cpu().numpy()
-    st, ids, w = oracle.route(lg, wl.top_k)
-    x = bits(g["x"])
-    st, counts, offsets, dest, sp, _ = oracle.dispatch(ids, x[:, :8], wl.experts, wl.cap)   # placement only
-    # the x_perm the GPU consumes: gathered on the device from x (a copy, no arithmetic)
-    x_perm = g["x"][torch.from_numpy(sp // wl.top_k).to(dev()).long()]
-    shape = N.shape_of(wl)
-    ws = N.workspace(shape, dev())
-    h = torch.empty(wl.pairs, wl.inter, dtype=torch.bfloat16, device=dev())
-    N.moe_expert_up(shape, x_perm, i32_dev(offsets), g["w13"], g["x"], g.get("ws13"), h, ws)
-    assert N.moe_status_read(ws) == N.MOE_OK
-    nz = np.nonzero(counts)[0]
-    hot, cold = nz[np.argmax(counts[nz])], nz[np.argmin(counts[nz])]
-    rng = np.random.default_rng(0)
-    exps = [hot, cold] + list(rng.choice(nz, 4, replace=False))
-    rows = sorted({r for e in exps for r in (offsets[e], offsets[e + 1] - 1)})
-    toks = [sp[r] // wl.top_k for r in rows]
-    eids = [int(np.searchsorted(offsets, r, side="right") - 1) for r in rows]
-    oh, _ = oracle_expert_rows(wl, g, x, toks, eids)
-    assert_close(bits(h[torch.tensor(rows, device=dev())]), oh, f"{name} h sampled")
 
 
 # ---------------------------------------------------------------------------
