@@ -100,7 +100,7 @@ moe_status do_dispatch(const moe_shape& s, const uint16_t* x, const int32_t* ids
 // call's dispatch found a bucket over capacity, so no output is touched.
 moe_status do_up(const moe_shape& s, const uint16_t* x_perm, const int32_t* offsets, const uint16_t* w13,
                  const uint16_t* x, const uint16_t* ws13, uint16_t* h, void* ws, cudaStream_t st,
-                 bool gated = false) {
+                 bool gated = false, int early = 0) {
     const WsLayout L = ws_layout(s);
     WsHeader* hdr = at<WsHeader>(ws, 0);
     const long long R = (long long)s.tokens * s.top_k;
@@ -115,6 +115,7 @@ moe_status do_up(const moe_shape& s, const uint16_t* x_perm, const int32_t* offs
     g.out = h; g.ldo = s.inter; g.out_group_col = 0;
     g.max_group_rows = s.tokens;   // a token's k experts are distinct
     g.gated = gated;
+    g.early = early;
     moe_status r = launch_grouped_gemm(g, hdr, st);
     if (r != MOE_OK || s.shared == 0) return r;
     GemmProblem q{};
@@ -132,7 +133,7 @@ moe_status do_up(const moe_shape& s, const uint16_t* x_perm, const int32_t* offs
 
 moe_status do_down(const moe_shape& s, const uint16_t* h, const int32_t* offsets, const uint16_t* w2,
                    const uint16_t* ws2, uint16_t* y_perm, uint16_t* y_shared, void* ws, cudaStream_t st,
-                   bool gated = false) {
+                   bool gated = false, int early = 0) {
     const WsLayout L = ws_layout(s);
     WsHeader* hdr = at<WsHeader>(ws, 0);
     const long long R = (long long)s.tokens * s.top_k;
@@ -146,6 +147,7 @@ moe_status do_down(const moe_shape& s, const uint16_t* h, const int32_t* offsets
     g.out = y_perm; g.ldo = s.hidden; g.out_group_col = 0;
     g.max_group_rows = s.tokens;
     g.gated = gated;
+    g.early = early;
     moe_status r = launch_grouped_gemm(g, hdr, st);
     if (r != MOE_OK || s.shared == 0) return r;
     // all shared experts in one accumulation: K runs over (s, n), so their sum
@@ -169,7 +171,7 @@ size_t nvfp4_bscale_stride(int K) { return 16 * (size_t)((K + 255) / 256); }
 
 moe_status do_up_q(const moe_shape& s, const uint16_t* x_perm, const int32_t* offsets, const uint8_t* w13,
                    const uint8_t* b13, const float* s13, int wfmt, uint16_t* h, void* ws, cudaStream_t st,
-                   bool gated = false) {
+                   bool gated = false, int early = 0) {
     const long long R = (long long)s.tokens * s.top_k;
     GemmProblem g{};
     g.mode = s.act == MOE_ACT_SWIGLU ? kGemmSwiGLU : kGemmReLU2;
@@ -183,12 +185,13 @@ moe_status do_up_q(const moe_shape& s, const uint16_t* x_perm, const int32_t* of
     g.wfmt = wfmt; g.wscale = s13;
     g.bscale = b13; g.bscale_stride = (long long)nvfp4_bscale_stride(s.hidden);
     g.gated = gated;
+    g.early = early;
     return launch_grouped_gemm(g, at<WsHeader>(ws, 0), st);
 }
 
 moe_status do_down_q(const moe_shape& s, const uint16_t* h, const int32_t* offsets, const uint8_t* w2,
                      const uint8_t* b2, const float* s2, int wfmt, uint16_t* y_perm, void* ws, cudaStream_t st,
-                     bool gated = false) {
+                     bool gated = false, int early = 0) {
     const long long R = (long long)s.tokens * s.top_k;
     GemmProblem g{};
     g.mode = kGemmPlain;
@@ -202,6 +205,7 @@ moe_status do_down_q(const moe_shape& s, const uint16_t* h, const int32_t* offse
     g.wfmt = wfmt; g.wscale = s2;
     g.bscale = b2; g.bscale_stride = (long long)nvfp4_bscale_stride(s.inter);
     g.gated = gated;
+    g.early = early;
     return launch_grouped_gemm(g, at<WsHeader>(ws, 0), st);
 }
 
@@ -301,8 +305,12 @@ moe_status layer_q(const moe_shape* shape, const float* logits, const int32_t* i
                                 x_perm, ws, st)) != MOE_OK) {
         return r;
     }
-    if ((r = do_up_q(s, x_perm, offsets, w13, w13_bscale, w13_scale, wfmt, h, ws, st, true)) != MOE_OK) return r;
-    if ((r = do_down_q(s, h, offsets, w2, w2_bscale, w2_scale, wfmt, y_perm, ws, st, true)) != MOE_OK) return r;
+    // the up projection may start its weight loads once the fused dispatch has
+    // published the bucket bounds; the down projection at once (they are final)
+    if ((r = do_up_q(s, x_perm, offsets, w13, w13_bscale, w13_scale, wfmt, h, ws, st, true, small ? 2 : 0)) !=
+        MOE_OK)
+        return r;
+    if ((r = do_down_q(s, h, offsets, w2, w2_bscale, w2_scale, wfmt, y_perm, ws, st, true, 1)) != MOE_OK) return r;
     return do_combine(s, y_perm, dest, w, nullptr, residual, out, st, at<WsHeader>(ws, 0));
 }
 
@@ -477,8 +485,10 @@ moe_status moe_layer(const moe_shape* shape, const float* logits, const int32_t*
                                 x_perm, ws, st)) != MOE_OK) {
         return r;
     }
-    if ((r = do_up(s, x_perm, offsets, w13, x, ws13, h, ws, st, true)) != MOE_OK) return r;
-    if ((r = do_down(s, h, offsets, w2, ws2, y_perm, y_shared, ws, st, true)) != MOE_OK) return r;
+    // the up projection may start its weight loads once the fused dispatch has
+    // published the bucket bounds; the down projection at once (they are final)
+    if ((r = do_up(s, x_perm, offsets, w13, x, ws13, h, ws, st, true, small ? 2 : 0)) != MOE_OK) return r;
+    if ((r = do_down(s, h, offsets, w2, ws2, y_perm, y_shared, ws, st, true, 1)) != MOE_OK) return r;
     return do_combine(s, y_perm, dest, w, y_shared, residual, out, st, at<WsHeader>(ws, 0));
 }
 

@@ -32,7 +32,8 @@ struct WsHeader {
     // test controls (moe_workspace_set_wait); zero = normal operation
     unsigned long long lookback_wait_ns;   // look-back give-up time; 0 = kWaitLimitNs
     int count_tile_skip;                   // first tile id the count kernel hands out (0 or 1)
-    int pad_;
+    unsigned route_ready;                  // moe_layer, fused dispatch: 0 at its start, 1 once the
+                                           // bucket bounds and the capacity verdict are written
 };
 
 constexpr int kCountChunk = 1024;      // pairs per count tile (one 256-thread block)
@@ -76,6 +77,9 @@ inline WsLayout ws_layout(const moe_shape& s) {
 
 // Bounded waits give up after this long and raise MOE_ERR_TIMEOUT.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;   // 2 s
+// How long the up projection looks for the fused dispatch's published bucket
+// bounds before it falls back to the programmatic wait (not an error).
+constexpr unsigned long long kEarlyWaitNs = 200000ull;       // 200 us
 
 // Where a bounded wait gave up (WsHeader::timeout_site).
 enum TimeoutSite : int {
@@ -105,6 +109,14 @@ __device__ __forceinline__ void st_release_u64(unsigned long long* p, unsigned l
 __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
     unsigned long long v;
     asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_u32(unsigned* p, unsigned v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
 }
 
@@ -411,6 +423,10 @@ struct GemmProblem {
     long long bscale_stride;                              // NVFP4: bytes per B row of bscale
     int gated;                                            // 1: do nothing if this layer's dispatch
                                                           //    exceeded the capacity (hdr->cap_exceeded)
+    // Small-row kernel only (moe_layer): 1 = the bucket bounds are final when the
+    // kernel starts (the down projection); 2 = the fused dispatch publishes them
+    // in hdr->route_ready (the up projection after it); 0 = neither (any caller).
+    int early;
 };
 constexpr int kWeightBf16 = 0;
 constexpr int kWeightFp8E4M3 = 1;   // one E4M3 code per element (b_cols bytes per row)

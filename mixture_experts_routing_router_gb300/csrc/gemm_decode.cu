@@ -89,6 +89,13 @@ struct DParams {
     uint32_t a_col;             // TMEM column of the first converted-weight slot
     int conv_slots;             // converted-weight slots in TMEM (one chunk each)
     uint32_t s_off;             // NVFP4: first block-scale box within a stage
+    // When the bucket bounds are known (moe_layer): 0 = after the programmatic
+    // wait (any caller); 1 = at launch (the down projection: the dispatch that
+    // wrote them finished before the up projection passed its own wait); 2 =
+    // once the fused dispatch has published them (hdr->route_ready).  With 1
+    // or 2 the weight loads of the first ring stages go out before the wait;
+    // the activation loads, which read the predecessor's output, after it.
+    int early;
 };
 
 template <int MODE> struct OutOfD { using T = __nv_bfloat16; };
@@ -153,8 +160,8 @@ __device__ __forceinline__ void e2m1x8_to_bf16x8(uint32_t w, uint32_t m, uint32_
 }
 
 __device__ __forceinline__ void clamped_bounds(const DParams& p, int g, int& lo, int& hi) {
-    lo = p.offsets[g];
-    hi = p.offsets[g + 1];
+    lo = __ldcg(p.offsets + g);            // from L2: may be read before the programmatic wait
+    hi = __ldcg(p.offsets + g + 1);
     lo = lo < 0 ? 0 : (lo > p.a_rows ? p.a_rows : lo);
     hi = hi < lo ? lo : (hi > p.a_rows ? p.a_rows : hi);
 }
@@ -238,10 +245,25 @@ decode_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
         tmem_alloc(smem_u32(&ctl->tmem_base), p.tmem_cols);
         tmem_relinquish();
     }
-    pdl_wait();
-    pdl_trigger();
+    __shared__ int early_ok;
+    if (p.early == 2) {
+        // the fused dispatch publishes the bucket bounds before it copies rows;
+        // a bounded wait, after which the programmatic wait below is the fallback
+        if (tid == 0) {
+            const unsigned long long t0 = globaltimer_ns();
+            unsigned ready;
+            while ((ready = ld_acquire_u32(&p.hdr->route_ready)) == 0u && globaltimer_ns() - t0 < kEarlyWaitNs) { }
+            early_ok = ready != 0u;
+        }
+        __syncthreads();
+    }
+    const bool waited = p.early == 0 || (p.early == 2 && !early_ok);
+    if (waited) {
+        pdl_wait();
+        pdl_trigger();
+    }
     // after a capacity overflow in the same layer call no payload moved: no items
-    const bool skip = p.gated && p.hdr->cap_exceeded;
+    const bool skip = p.gated && __ldcg(&p.hdr->cap_exceeded);
 
     // ---- the non-empty groups (block-wide compaction of the offsets) --------
     if (skip) {
@@ -303,6 +325,49 @@ decode_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
     const uint32_t x_off = p.x_off, w_off = p.w_off;
     const uint32_t w_box = FP8W ? (uint32_t)W8_BYTES : (uint32_t)W_BYTES;
 
+    // The TMA loads of one ring stage: its weight boxes (with the NVFP4 block
+    // scales), and its activation boxes.
+    auto load_weights = [&](uint32_t sa, uint32_t full, int w_row, int seg, int kb) {
+        const int wcol = FP4W ? kb * (DBK4 / 2) : kb * kstep;     // code bytes
+#pragma unroll
+        for (int h = 0; h < NB8; ++h)   // FP8, 256-wide stage: two 128-byte code boxes
+            tma_load_2d(sa + w_off + (uint32_t)h * w_box, &tmW, full, wcol + h * DBK8, w_row + seg * p.b_seg_row);
+        if (MODE == kGemmSwiGLU)
+            tma_load_2d(sa + w_off + w_box, &tmW, full, wcol, w_row + p.up_off + seg * p.b_seg_row);
+        if (FP4W) {     // the rows' block scales of these 256 elements
+            tma_load_2d(sa + p.s_off, &tmS, full, kb * (DBK4 / 16), w_row);
+            if (MODE == kGemmSwiGLU)
+                tma_load_2d(sa + p.s_off + S4_BYTES, &tmS, full, kb * (DBK4 / 16), w_row + p.up_off);
+        }
+    };
+    auto load_acts = [&](uint32_t sa, uint32_t full, int xr, int seg, int kb) {
+        for (int xb = 0; xb < kstep / DBK; ++xb)   // 64-wide activation boxes
+            tma_load_2d(sa + x_off + (uint32_t)xb * xbox, &tmX, full, seg * p.a_seg_col + kb * kstep + xb * DBK, xr);
+    };
+
+    // Bucket bounds known before the programmatic wait: the producer arms the
+    // first ring stages and sends their weight loads (weights are never written
+    // by a kernel) while the predecessor finishes; every thread then waits, and
+    // the activation loads of those stages follow in the main loop.
+    int npre = 0;
+    if (!waited) {
+        if (warp == 0 && lane == 0) {
+            for (int it = blockIdx.x; it < items && npre < p.stages; it += gridDim.x) {
+                const int slot = it / ntn, nt = it - slot * ntn;
+                const int w_row = gid[slot] * p.b_group_rows + nt * DBM;
+                for (int xr = gst[slot]; xr < gst[slot] + gcnt[slot] && npre < p.stages; xr += nb)
+                    for (int i = 0; i < nk && npre < p.stages; ++i) {
+                        const uint32_t full = smem_u32(&ctl->full[npre]);
+                        mbar_arrive_expect_tx(full, (uint32_t)p.stage_bytes);
+                        load_weights(smem_base + (uint32_t)(npre * p.stage_bytes), full, w_row, i / nkb, i % nkb);
+                        ++npre;
+                    }
+            }
+        }
+        pdl_wait();
+        pdl_trigger();
+    }
+
     if (warp == 0) {
         // ---------------- TMA producer ----------------
         if (lane == 0) {
@@ -317,33 +382,25 @@ decode_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
                 for (int xr = row0; xr < row0 + rows && ok; xr += nb) {
                     for (int i = 0; i < nk; ++i) {
                         const int seg = i / nkb, kb = i - seg * nkb;
-                        if (!mbar_wait_bounded(smem_u32(&ctl->empty[stage]), ph ^ 1u, abort)) { ok = false; break; }
                         const uint32_t full = smem_u32(&ctl->full[stage]);
-                        mbar_arrive_expect_tx(full, (uint32_t)p.stage_bytes);
                         const uint32_t sa = smem_base + (uint32_t)(stage * p.stage_bytes);
-                        const int wcol = FP4W ? kb * (DBK4 / 2) : kb * kstep;     // code bytes
-#pragma unroll
-                        for (int h = 0; h < NB8; ++h)   // FP8, 256-wide stage: two 128-byte code boxes
-                            tma_load_2d(sa + w_off + (uint32_t)h * w_box, &tmW, full, wcol + h * DBK8,
-                                        w_row + seg * p.b_seg_row);
-                        if (MODE == kGemmSwiGLU)
-                            tma_load_2d(sa + w_off + w_box, &tmW, full, wcol, w_row + p.up_off + seg * p.b_seg_row);
-                        if (FP4W) {     // the rows' block scales of these 256 elements
-                            tma_load_2d(sa + p.s_off, &tmS, full, kb * (DBK4 / 16), w_row);
-                            if (MODE == kGemmSwiGLU)
-                                tma_load_2d(sa + p.s_off + S4_BYTES, &tmS, full, kb * (DBK4 / 16), w_row + p.up_off);
+                        if (armed >= npre) {      // else armed with its weights before the wait
+                            if (!mbar_wait_bounded(smem_u32(&ctl->empty[stage]), ph ^ 1u, abort)) { ok = false; break; }
+                            mbar_arrive_expect_tx(full, (uint32_t)p.stage_bytes);
+                            load_weights(sa, full, w_row, seg, kb);
                         }
-                        for (int xb = 0; xb < kstep / DBK; ++xb)   // 64-wide activation boxes
-                            tma_load_2d(sa + x_off + (uint32_t)xb * xbox, &tmX, full,
-                                        seg * p.a_seg_col + kb * kstep + xb * DBK, xr);
+                        load_acts(sa, full, xr, seg, kb);
                         ++armed;
                         if (++stage == p.stages) { stage = 0; ph ^= 1u; }
                     }
                 }
             }
             if (!ok) {
-                // let the copies already issued land before the CTA exits
-                if (!wait_armed_stages(smem_u32(&ctl->full[0]), p.stages, armed)) settle_delay();
+                // let the copies already issued land before the CTA exits (stages
+                // armed before the wait whose activations never went out cannot
+                // complete: their wait runs out and the fixed delay follows)
+                if (!wait_armed_stages(smem_u32(&ctl->full[0]), p.stages, armed > npre ? armed : npre))
+                    settle_delay();
                 raise_status(p.hdr, MOE_ERR_TIMEOUT);
                 p.hdr->timeout_site = kSiteGemmDecode;
             }
@@ -644,6 +701,7 @@ moe_status launch_decode_gemm(const GemmProblem& g, int nb, WsHeader* hdr, cudaS
     dp.nb = nb;
     dp.wscale = g.wscale;
     dp.s_off = 0;
+    dp.early = g.offsets ? g.early : 0;
     if (fp4) {
         // stage (K 256): [four activation boxes: nb rows x 128 B each][code box(es):
         // 128 rows x 128 B = 16 KiB each][block-scale box(es): 128 rows x 16 B]

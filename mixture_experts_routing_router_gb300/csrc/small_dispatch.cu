@@ -40,6 +40,13 @@ small_dispatch_kernel(int T, int E, int k, int capacity, const float* __restrict
                       int32_t* __restrict__ offsets, int32_t* __restrict__ dest, int32_t* __restrict__ sorted_pair,
                       uint4* __restrict__ x_perm, WsHeader* hdr) {
     pdl_wait();
+    // route_ready goes to 0 before any dependent kernel can start (they start
+    // once every CTA has triggered), and to 1 once the bucket bounds are out
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        hdr->route_ready = 0u;
+        __threadfence();
+    }
+    __syncthreads();
     pdl_trigger();
     extern __shared__ int sm[];
     const int R = T * k;
@@ -91,7 +98,10 @@ small_dispatch_kernel(int T, int E, int k, int capacity, const float* __restrict
         const int lrank = __popc(grp & sd_lanemask_lt());
         const bool leader = (lane == 31 - __clz(grp));
         int r = 0;
-        for (int w = 0; w < kSDThreads / 32; ++w) {
+        // warps in order; only the warps that hold pairs of this item
+        const int left = R - it * kSDThreads;
+        const int nw = left <= 0 ? 0 : (left >= kSDThreads ? kSDThreads / 32 : (left + 31) / 32);
+        for (int w = 0; w < nw; ++w) {
             if (warp == w) {
                 const int base = (e >= 0) ? hist[e] : 0;
                 __syncwarp();
@@ -142,6 +152,10 @@ small_dispatch_kernel(int T, int E, int k, int capacity, const float* __restrict
     if (lead && tid == 0) {
         hdr->cap_exceeded = any_over;
         if (any_over) raise_status(hdr, MOE_ERR_CAPACITY);
+        // ids, weights, counts, offsets and the verdict are written (the block
+        // barrier above orders the other threads' stores before this fence)
+        __threadfence();
+        st_release_u32(&hdr->route_ready, 1u);
     }
     if (any_over) return;                              // over capacity: no payload moves
 #pragma unroll
