@@ -80,6 +80,13 @@ moe_status from_cuda(cudaError_t e) {
 
 int up_rows(const moe_shape& s, int inter) { return (s.act == MOE_ACT_SWIGLU ? 2 : 1) * inter; }
 
+// A layer call that failed to launch a kernel after its fused dispatch never
+// reaches the combine that puts route_ready back to 0: do it here, so the next
+// call's up projection cannot take this call's published bucket bounds.
+void reset_route_ready(void* ws, cudaStream_t st) {
+    cudaMemsetAsync(&at<WsHeader>(ws, 0)->route_ready, 0, sizeof(unsigned), st);
+}
+
 // ---- the stage bodies (arguments already validated) --------------------------
 moe_status do_route(const moe_shape& s, const float* logits, int32_t* ids, float* w, void* ws, cudaStream_t st) {
     return from_cuda(launch_route(s, logits, ids, w, at<WsHeader>(ws, 0), st));
@@ -229,7 +236,7 @@ moe_status check_quant_shape(const moe_shape* s, int wfmt) {
 
 moe_status do_combine(const moe_shape& s, const uint16_t* y_perm, const int32_t* dest, const float* w,
                       const uint16_t* y_shared, const uint16_t* residual, uint16_t* out, cudaStream_t st,
-                      const WsHeader* gate = nullptr) {
+                      WsHeader* gate = nullptr) {
     return from_cuda(launch_combine(s, y_perm, dest, w, y_shared, residual, out, gate, st));
 }
 
@@ -307,11 +314,12 @@ moe_status layer_q(const moe_shape* shape, const float* logits, const int32_t* i
     }
     // the up projection may start its weight loads once the fused dispatch has
     // published the bucket bounds; the down projection at once (they are final)
-    if ((r = do_up_q(s, x_perm, offsets, w13, w13_bscale, w13_scale, wfmt, h, ws, st, true, small ? 2 : 0)) !=
-        MOE_OK)
-        return r;
-    if ((r = do_down_q(s, h, offsets, w2, w2_bscale, w2_scale, wfmt, y_perm, ws, st, true, 1)) != MOE_OK) return r;
-    return do_combine(s, y_perm, dest, w, nullptr, residual, out, st, at<WsHeader>(ws, 0));
+    if ((r = do_up_q(s, x_perm, offsets, w13, w13_bscale, w13_scale, wfmt, h, ws, st, true, small ? 2 : 0)) ==
+            MOE_OK &&
+        (r = do_down_q(s, h, offsets, w2, w2_bscale, w2_scale, wfmt, y_perm, ws, st, true, 1)) == MOE_OK)
+        r = do_combine(s, y_perm, dest, w, nullptr, residual, out, st, at<WsHeader>(ws, 0));
+    if (r != MOE_OK) reset_route_ready(ws, st);
+    return r;
 }
 
 }  // namespace
@@ -487,9 +495,11 @@ moe_status moe_layer(const moe_shape* shape, const float* logits, const int32_t*
     }
     // the up projection may start its weight loads once the fused dispatch has
     // published the bucket bounds; the down projection at once (they are final)
-    if ((r = do_up(s, x_perm, offsets, w13, x, ws13, h, ws, st, true, small ? 2 : 0)) != MOE_OK) return r;
-    if ((r = do_down(s, h, offsets, w2, ws2, y_perm, y_shared, ws, st, true, 1)) != MOE_OK) return r;
-    return do_combine(s, y_perm, dest, w, y_shared, residual, out, st, at<WsHeader>(ws, 0));
+    if ((r = do_up(s, x_perm, offsets, w13, x, ws13, h, ws, st, true, small ? 2 : 0)) == MOE_OK &&
+        (r = do_down(s, h, offsets, w2, ws2, y_perm, y_shared, ws, st, true, 1)) == MOE_OK)
+        r = do_combine(s, y_perm, dest, w, y_shared, residual, out, st, at<WsHeader>(ws, 0));
+    if (r != MOE_OK) reset_route_ready(ws, st);
+    return r;
 }
 
 moe_status moe_expert_up_fp8(const moe_shape* shape, const uint16_t* x_perm, const int32_t* offsets,

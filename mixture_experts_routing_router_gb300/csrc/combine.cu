@@ -31,10 +31,15 @@ __global__ void __launch_bounds__(256)
 combine_kernel(int T, int HV, int k, const uint4* __restrict__ y_perm, const int32_t* __restrict__ dest,
                const float* __restrict__ w, const uint4* __restrict__ y_shared, const uint4* residual,
                uint4* out,     // out may alias residual: each 16-byte group is read, then written, by one thread
-               const WsHeader* gate) {
+               WsHeader* gate) {
     pdl_wait();
     pdl_trigger();
-    if (gate && gate->cap_exceeded) return;     // over capacity in this layer call: out stays untouched
+    if (gate) {
+        // the layer's last kernel: the next layer call's fused dispatch will
+        // publish its bucket bounds afresh
+        if (blockIdx.x == 0 && threadIdx.x == 0) gate->route_ready = 0u;
+        if (gate->cap_exceeded) return;         // over capacity in this layer call: out stays untouched
+    }
     __shared__ int dsh[32];
     __shared__ float wsh[32];
     const long long R = (long long)T * k;
@@ -78,7 +83,7 @@ combine_kernel(int T, int HV, int k, const uint4* __restrict__ y_perm, const int
 }  // namespace
 
 cudaError_t launch_combine(const moe_shape& s, const uint16_t* y_perm, const int32_t* dest, const float* w,
-                           const uint16_t* y_shared, const uint16_t* residual, uint16_t* out, const WsHeader* gate,
+                           const uint16_t* y_shared, const uint16_t* residual, uint16_t* out, WsHeader* gate,
                            cudaStream_t st) {
     const int HV = s.hidden / 8;
     int threads = 32;

@@ -32,8 +32,8 @@ struct WsHeader {
     // test controls (moe_workspace_set_wait); zero = normal operation
     unsigned long long lookback_wait_ns;   // look-back give-up time; 0 = kWaitLimitNs
     int count_tile_skip;                   // first tile id the count kernel hands out (0 or 1)
-    unsigned route_ready;                  // moe_layer, fused dispatch: 0 at its start, 1 once the
-                                           // bucket bounds and the capacity verdict are written
+    unsigned route_ready;                  // moe_layer: 1 once the fused dispatch has written the bucket
+                                           // bounds and the capacity verdict; 0 again after the combine
 };
 
 constexpr int kCountChunk = 1024;      // pairs per count tile (one 256-thread block)
@@ -360,10 +360,11 @@ cudaError_t launch_small_dispatch(const moe_shape& s, const float* logits, const
                                   float* w_out, const uint16_t* x, int32_t* counts, int32_t* offsets, int32_t* dest,
                                   int32_t* sorted_pair, uint16_t* x_perm, WsHeader* hdr, cudaStream_t st);
 // gate: NULL, or (inside moe_layer) the workspace header whose capacity verdict,
-// when set, makes the kernel leave `out` untouched.
+// when set, makes the kernel leave `out` untouched; the kernel also puts the
+// header's route_ready back to 0 for the next layer call.
 cudaError_t launch_combine(const moe_shape& s, const uint16_t* y_perm, const int32_t* dest,
                            const float* w, const uint16_t* y_shared, const uint16_t* residual, uint16_t* out,
-                           const WsHeader* gate, cudaStream_t st);
+                           WsHeader* gate, cudaStream_t st);
 // The test controls of the look-back wait (moe_workspace_set_wait).
 cudaError_t launch_set_wait(WsHeader* hdr, unsigned long long lookback_wait_ns, int count_tile_skip,
                             cudaStream_t st);

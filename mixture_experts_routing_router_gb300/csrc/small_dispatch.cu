@@ -40,13 +40,6 @@ small_dispatch_kernel(int T, int E, int k, int capacity, const float* __restrict
                       int32_t* __restrict__ offsets, int32_t* __restrict__ dest, int32_t* __restrict__ sorted_pair,
                       uint4* __restrict__ x_perm, WsHeader* hdr) {
     pdl_wait();
-    // route_ready goes to 0 before any dependent kernel can start (they start
-    // once every CTA has triggered), and to 1 once the bucket bounds are out
-    if (blockIdx.x == 0 && threadIdx.x == 0) {
-        hdr->route_ready = 0u;
-        __threadfence();
-    }
-    __syncthreads();
     pdl_trigger();
     extern __shared__ int sm[];
     const int R = T * k;
@@ -153,7 +146,8 @@ small_dispatch_kernel(int T, int E, int k, int capacity, const float* __restrict
         hdr->cap_exceeded = any_over;
         if (any_over) raise_status(hdr, MOE_ERR_CAPACITY);
         // ids, weights, counts, offsets and the verdict are written (the block
-        // barrier above orders the other threads' stores before this fence)
+        // barrier above orders the other threads' stores before this fence);
+        // the layer's combine puts route_ready back to 0
         __threadfence();
         st_release_u32(&hdr->route_ready, 1u);
     }
