@@ -306,6 +306,40 @@ MOE_API moe_status moe_dispatch_noalloc(const moe_shape* shape, const uint16_t* 
                                         int32_t* counts, int32_t* offsets, int32_t* dest, int32_t* sorted_pair,
                                         uint16_t* x_perm, int32_t* device_status, void* stream);
 
+/* The plan of the expert-parallel count-first exchange (afdEP-comm count-first
+ * validation record, .change and .setup: with the experts split over the ranks
+ * of a node, the per-expert counts travel first -- E*G int32 in all -- so that
+ * before any payload row moves every rank knows where each of its rows lands
+ * in the owner's expert-contiguous receive buffer, and whether a receive
+ * buffer would overflow; the combine returns along the same segments).
+ * Host only: no device memory, nothing enqueued.
+ * The E experts are split over `world` ranks in contiguous balanced blocks:
+ * rank g owns experts [first(g), first(g+1)), first(g) = (g * E) / world, and
+ * el = first(rank+1) - first(rank) of them belong to `rank`.
+ *   counts_all   host i32 [world, E]  row s: rank s's per-expert counts (the
+ *                                     counts its moe_dispatch wrote)
+ *   send_offsets host i32 [E+1] out   where this rank's rows of expert e start
+ *                                     in its own x_perm (the exclusive scan of
+ *                                     its counts)
+ *   recv_offsets host i32 [el+1] out  the receive buffer's bucket bounds for
+ *                                     the el local experts (the offsets the
+ *                                     local expert FFN takes)
+ *   recv_slot    host i32 [world, el] out  first receive row of the rows that
+ *                                     source s sends for local expert j; inside a
+ *                                     bucket the sources come in rank order, each
+ *                                     in its own token order
+ *   peer_send, peer_recv host i32 [world] out  rows sent to / received from
+ *                                     each rank
+ * Rows for one (source, expert) pair travel as one segment, sender and
+ * receiver taking the segments of a peer in ascending expert order.
+ * Returns MOE_ERR_CAPACITY (with every output written) when some expert of some
+ * rank would receive more than `capacity` rows -- every rank reaches the same
+ * verdict from the same counts, so all skip the payload together -- and
+ * MOE_ERR_INVALID_ARG for bad sizes, null pointers or a negative count. */
+MOE_API moe_status moe_ep_plan(int32_t experts, int32_t world, int32_t rank, int32_t capacity,
+                               const int32_t* counts_all, int32_t* send_offsets, int32_t* recv_offsets,
+                               int32_t* recv_slot, int32_t* peer_send, int32_t* peer_recv);
+
 /* Synchronise `stream`, return in *device_status the largest status code raised
  * by kernels on this workspace since the last read, and clear it (together
  * with the timeout site below). */

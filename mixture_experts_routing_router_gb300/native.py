@@ -35,7 +35,7 @@ EXPORTS = ("moe_workspace_size", "moe_workspace_init", "moe_route", "moe_dispatc
            "moe_status_string", "moe_last_error_message", "moe_dispatch_noalloc", "moe_gate",
            "moe_route_sigmoid", "moe_expert_up_fp8", "moe_expert_down_fp8", "moe_layer_fp8",
            "moe_expert_up_nvfp4", "moe_expert_down_nvfp4", "moe_layer_nvfp4", "moe_workspace_set_wait",
-           "moe_timeout_site_read")
+           "moe_timeout_site_read", "moe_ep_plan")
 
 
 class MoEError(RuntimeError):
@@ -99,6 +99,7 @@ def lib():
                 "moe_layer_nvfp4": [SP, P, P, P, P, P, P, P, P, P, P, P, P, P, S, P],
                 "moe_workspace_set_wait": [P, S, ctypes.c_uint64, ctypes.c_int32, P],
                 "moe_timeout_site_read": [P, P, ctypes.POINTER(ctypes.c_int32)],
+                "moe_ep_plan": [ctypes.c_int32] * 4 + [P] * 6,
             }
             for name, args in sig.items():
                 fn = getattr(L, name)
@@ -288,3 +289,24 @@ def moe_timeout_site_read(ws, stream=None) -> int:
     site = ctypes.c_int32(0)
     _check(lib().moe_timeout_site_read(_ptr(ws), _stream(stream), ctypes.byref(site)), "moe_timeout_site_read")
     return site.value
+
+
+def moe_ep_plan(experts: int, world: int, rank: int, capacity: int, counts_all):
+    """Host-side plan of the expert-parallel exchange (numpy in, numpy out):
+    -> (status, dict(send_offsets [E+1], recv_offsets [el+1], recv_slot [world, el],
+    peer_send [world], peer_recv [world])).  The status is MOE_OK or
+    MOE_ERR_CAPACITY (the plan is written either way); other errors raise."""
+    import numpy as np
+    ca = np.ascontiguousarray(counts_all, dtype=np.int32)
+    if ca.shape != (world, experts):
+        raise ValueError(f"counts_all must be [{world}, {experts}], got {ca.shape}")
+    e0, e1 = rank * experts // world, (rank + 1) * experts // world
+    out = dict(send_offsets=np.zeros(experts + 1, np.int32), recv_offsets=np.zeros(e1 - e0 + 1, np.int32),
+               recv_slot=np.zeros((world, e1 - e0), np.int32), peer_send=np.zeros(world, np.int32),
+               peer_recv=np.zeros(world, np.int32))
+    p = lambda a: ctypes.c_void_p(a.ctypes.data)
+    st = lib().moe_ep_plan(experts, world, rank, capacity, p(ca), p(out["send_offsets"]), p(out["recv_offsets"]),
+                           p(out["recv_slot"]), p(out["peer_send"]), p(out["peer_recv"]))
+    if st not in (MOE_OK, MOE_ERR_CAPACITY):
+        raise MoEError(st, "moe_ep_plan")
+    return st, out
