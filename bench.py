@@ -136,7 +136,7 @@ class ClockSampler:
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -207,29 +207,111 @@ def barrier(world):
 # ---------------------------------------------------------------------------
 # CPU oracle timing (baseline leg and the reference arm)
 # ---------------------------------------------------------------------------
-def oracle_sample(wl, g_logits_host, x_host, tokens, weight_device, seed=0):
+def host_description():
+    """The host the oracle runs on: logical CPUs and the CPU model."""
+    model = ""
+    try:
+        with open("/proc/cpuinfo") as f:
+            info = f.read()
+        for key in ("model name", "Model", "cpu model"):
+            for ln in info.splitlines():
+                if ln.lower().startswith(key.lower()) and ":" in ln:
+                    model = ln.split(":", 1)[1].strip()
+                    break
+            if model:
+                break
+        if not model:       # Arm: implementer / part numbers
+            parts = {ln.split(":", 1)[1].strip() for ln in info.splitlines() if ln.startswith("CPU part")}
+            impl = {ln.split(":", 1)[1].strip() for ln in info.splitlines() if ln.startswith("CPU implementer")}
+            if parts:
+                model = f"Arm CPU implementer {'/'.join(sorted(impl))} part {'/'.join(sorted(parts))}"
+    except OSError:
+        pass
+    return {"nproc": os.cpu_count(), "cpu_model": model or "unknown"}
+
+
+def oracle_macs_per_token(wl):
+    """Multiply-adds of the oracle per token: k routed rows plus the shared experts."""
+    H, I, up = wl.hidden, wl.inter, wl.up
+    return wl.top_k * (H * up + I * H) + wl.shared * (H * wl.shared_up + wl.shared_inter * H)
+
+
+def oracle_sample(wl, g_logits_host, x_host, tokens, weight_device, seed=0, threads=1):
     """Time the oracle on `tokens` tokens of the workload: routing of those
     tokens, their k expert rows (up projection, activation, down projection)
-    and the combine.  Weights of the touched experts are regenerated from
-    their seeded streams.  Returns (seconds, tokens)."""
+    and the combine, the rows on a pool of `threads` host threads (the C++
+    oracle releases the interpreter lock).  Expert weights are regenerated
+    from their seeded streams one expert at a time, outside the timed part.
+    Returns (seconds, tokens)."""
+    import concurrent.futures as cf
+
     import oracle
     from mixture_experts_routing_router_gb300.synth import bf16_bits, expert_weights
-    _, ids, w = oracle.route(g_logits_host[tokens], wl.top_k)
-    need = sorted(set(ids.reshape(-1).tolist()))
-    wts = {}
-    for e in need:
-        a, b = expert_weights(wl, e, seed, weight_device)
-        wts[e] = (bf16_bits(a), bf16_bits(b))
     t0 = time.perf_counter()
     _, ids, w = oracle.route(g_logits_host[tokens], wl.top_k)
-    for i, t in enumerate(tokens):
-        ys = []
+    timed = time.perf_counter() - t0
+    by_e = {}
+    for i in range(len(tokens)):
         for j in range(wl.top_k):
-            e = int(ids[i, j])
-            _, y = oracle.expert_row(x_host[t], wts[e][0], wts[e][1], wl.act)
-            ys.append(y)
-        oracle.combine_row(np.stack(ys), np.arange(wl.top_k, dtype=np.int32), w[i])
-    return time.perf_counter() - t0, len(tokens)
+            by_e.setdefault(int(ids[i, j]), []).append((i, j))
+    ys = {}
+    with cf.ThreadPoolExecutor(threads) as ex:
+        for e, rows in sorted(by_e.items()):
+            a, b = expert_weights(wl, e, seed, weight_device)
+            w13e, w2e = bf16_bits(a), bf16_bits(b)
+            t0 = time.perf_counter()
+            res = list(ex.map(lambda ij: oracle.expert_row(x_host[tokens[ij[0]]], w13e, w2e, wl.act)[1], rows))
+            timed += time.perf_counter() - t0
+            for ij, y in zip(rows, res):
+                ys[ij] = y
+    t0 = time.perf_counter()
+    for i in range(len(tokens)):
+        oracle.combine_row(np.stack([ys[(i, j)] for j in range(wl.top_k)]), np.arange(wl.top_k, dtype=np.int32), w[i])
+    timed += time.perf_counter() - t0
+    return timed, len(tokens)
+
+
+def oracle_full(wl, g):
+    """Time the whole oracle layer, single-threaded, on the workload's batch."""
+    import oracle
+    kw = dict(ws13=synth.bf16_bits(g["ws13"]), ws2=synth.bf16_bits(g["ws2"])) if wl.shared else {}
+    x, w13, w2 = synth.bf16_bits(g["x"]), synth.bf16_bits(g["w13"]), synth.bf16_bits(g["w2"])
+    lg = g["logits"].cpu().numpy()
+    t0 = time.perf_counter()
+    ref = oracle.layer(x, w13, w2, wl.act, wl.top_k, wl.cap, logits=lg, **kw)
+    secs = time.perf_counter() - t0
+    assert ref["status"] == 0
+    return secs
+
+
+# The oracle's rate, roughly (FP64 multiply-adds per second per core): sizes the
+# bounded sample so the CPU baseline stays at about 20 core-seconds.
+ORACLE_MACS_PER_CORE_S = 1.0e9
+CPU_BUDGET_CORE_S = 20.0
+
+
+def cpu_baseline(wl, g, dev, seed):
+    """The oracle on the machine's host cores.  Workloads whose whole oracle layer
+    fits the budget run it in full, single-threaded (the oracle as it stands);
+    larger ones time a seeded sample of tokens with the rows spread over every
+    host core, the thread count stated."""
+    host = host_description()
+    T = wl.tokens
+    per_tok = oracle_macs_per_token(wl)
+    if T * per_tok <= CPU_BUDGET_CORE_S * ORACLE_MACS_PER_CORE_S and g.get("w13") is not None:
+        secs = oracle_full(wl, g)
+        return {"value": T / secs, "unit": "tokens/s", "cores": 1, "kind": "oracle", **host,
+                "sample": f"the whole {T}-token layer (routing, dispatch, expert FFN with FP64 sums, combine), "
+                          f"single-threaded, {secs:.1f} s"}
+    threads = max(1, os.cpu_count() or 1)
+    n = int(min(T, max(8, CPU_BUDGET_CORE_S * ORACLE_MACS_PER_CORE_S // per_tok)))
+    rng = np.random.default_rng(0)
+    toks = sorted(rng.choice(T, n, replace=False).tolist())
+    secs, n = oracle_sample(wl, g["logits"].cpu().numpy(), synth.bf16_bits(g["x"]), toks, dev, seed=seed,
+                            threads=threads)
+    return {"value": n / secs, "unit": "tokens/s", "cores": threads, "kind": "oracle", **host,
+            "sample": f"{n} seeded random tokens of the {T}-token batch: their routing, top-{wl.top_k} expert rows "
+                      f"(FP64 sums, rows spread over {threads} host threads) and combine; {secs:.1f} s wall"}
 
 
 def run_reference(args, wl, world, rank):
@@ -241,23 +323,26 @@ def run_reference(args, wl, world, rank):
     logits = synth.make_logits(wl, 0, dev).cpu().numpy()
     x = synth.bf16_bits(synth.normal((wl.tokens, wl.hidden), 1.0, 0, "x", dev))
     rng = np.random.default_rng(0)
-    per_step = 1
+    threads = max(1, os.cpu_count() or 1)
+    # each step a bounded sample: as many tokens as there are host threads
+    per_step = min(wl.tokens, threads)
     times, toks = [], 0
     for step in range(args.warmup + args.steps):
         tokens = sorted(rng.choice(wl.tokens, per_step, replace=False).tolist())
-        s, n = oracle_sample(wl, logits, x, tokens, dev)
+        s, n = oracle_sample(wl, logits, x, tokens, dev, threads=threads)
         if step >= args.warmup:
             times.append(s)
             toks += n
     total = sum(times)
     value = toks / total
-    sample = (f"{per_step} random token(s) per step of the {wl.tokens}-token batch: routing, the top-{wl.top_k} "
-              f"expert rows (FP64 sums) and the combine; single-threaded")
+    sample = (f"{per_step} seeded random token(s) per step of the {wl.tokens}-token batch: routing, the top-{wl.top_k} "
+              f"expert rows (FP64 sums, spread over {threads} host threads) and the combine")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": describe(wl), "tokens_per_step": per_step},
-            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                             **host_description(), "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -363,28 +448,37 @@ def run_native(args, wl, world, rank, local):
     torch.cuda.synchronize(dev)
     with ClockSampler(local) as clk:
         with torch.cuda.stream(stream):
-            if not flush:
-                ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                ev0.record(stream)
-                for _ in range(args.steps):
-                    layer_graph.replay()
-                ev1.record(stream)
-                pairs = [(ev0, ev1)]
-            else:
-                pairs = []
-                for i in range(args.steps):
+            # one event per step boundary: back to back when no flush is needed
+            # (the steps' total is first start to last end), else around each step
+            pairs = []
+            prev = None
+            for i in range(args.steps):
+                if flush:
                     flush_l2(i)
-                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    prev = None
+                a = prev if prev is not None else torch.cuda.Event(enable_timing=True)
+                if prev is None:
                     a.record(stream)
-                    layer_graph.replay()
-                    b.record(stream)
-                    pairs.append((a, b))
+                b = torch.cuda.Event(enable_timing=True)
+                layer_graph.replay()
+                b.record(stream)
+                pairs.append((a, b))
+                prev = None if flush else b
         stream.synchronize()
     torch.cuda.synchronize(dev)
     barrier(world)
-    elapsed = sum(a.elapsed_time(b) for a, b in pairs) / 1e3
+    step_ms = [a.elapsed_time(b) for a, b in pairs]
+    elapsed = sum(step_ms) / 1e3
     elapsed = max_over_ranks(elapsed, world, dev)
     tokens_per_s = world * T * args.steps / elapsed
+    # spread of the steps: median, p95, and the drift between the first and
+    # the last tenth of the run (flagged above 2 %)
+    tenth = max(1, len(step_ms) // 10)
+    first, last = statistics.mean(step_ms[:tenth]), statistics.mean(step_ms[-tenth:])
+    step_stats = {"median_ms": statistics.median(step_ms),
+                  "p95_ms": float(np.percentile(step_ms, 95)),
+                  "drift_first_to_last": (last - first) / first,
+                  "unstable": abs(last - first) / first > 0.02}
 
     # ---- per-stage times (same stream, events between the stage calls) --------
     ids = torch.empty(T, k, dtype=torch.int32, device=dev)
@@ -472,6 +566,8 @@ def run_native(args, wl, world, rank, local):
     # after another.
     x_host = g["x"].cpu().pin_memory()
     lg_host = g["logits"].cpu().pin_memory()
+    e2e_clk = ClockSampler(local)
+    e2e_clk.__enter__()
     # as many steps as the headline, so both run in the same (power-capped) state
     e2e_steps = max(3, args.steps)
 
@@ -532,12 +628,13 @@ def run_native(args, wl, world, rank, local):
             stream.synchronize()
         e2e_s = max_over_ranks(sum(a.elapsed_time(b) for a, b in e2e_pairs) / 1e3 / e2e_steps, world, dev)
         e2e_mode = "sequential: input copy, layer, output copy per step, L2 flushed before each"
+    e2e_clk.__exit__(None, None, None)
     st = N.moe_status_read(ws, stream)
     if st != N.MOE_OK:
         raise RuntimeError(f"device status {st} after the end-to-end steps")
     e2e = {"value": world * T / e2e_s, "unit": "tokens/s",
            "h2d_bytes_per_step": x_host.numel() * 2 + lg_host.numel() * 4,
-           "d2h_bytes_per_step": T * H * 2, "mode": e2e_mode}
+           "d2h_bytes_per_step": T * H * 2, "mode": e2e_mode, "clocks": e2e_clk.summary()}
 
     peaks = load_peaks()
     up_s = stage_ms["expert_up"] / 1e3
@@ -553,6 +650,19 @@ def run_native(args, wl, world, rank, local):
                 "peak_source": f"{peaks['source']} hbm_gbs"}
     roof["frac"] = roof["achieved"] / roof["peak"]
     achieved = alg["up_flops"] / up_s / 1e12
+    # per clock: the up projection against the tensor pipe's own rate at the
+    # median SM clock of the timed region (152 SMs x 8192 BF16 flop per cycle:
+    # M128 N256 K16 per 128 cycles, measured), so box-to-box clock spread does
+    # not hide the kernel's trend
+    clocks = clk.summary()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    per_clock = None
+    if clocks.get("sm_mhz"):
+        rate = sms * 8192 * clocks["sm_mhz"] * 1e6 / 1e12
+        per_clock = {"sm_mhz": clocks["sm_mhz"], "tensor_rate_at_clock_tflops": rate,
+                     "expert_up_frac_of_rate": achieved / rate,
+                     "gemm_frac_of_rate": (alg["up_flops"] + alg["down_flops"]) /
+                     ((stage_ms["expert_up"] + stage_ms["expert_down"]) / 1e3) / 1e12 / rate}
     dc_s = (stage_ms["dispatch"] + stage_ms["combine"]) / 1e3
     dc_gbs = (alg["dispatch_bytes"] + alg["combine_bytes"]) / dc_s / 1e9
     gemm_tflops = (alg["up_flops"] + alg["down_flops"]) / ((stage_ms["expert_up"] + stage_ms["expert_down"]) / 1e3) / 1e12
@@ -561,12 +671,7 @@ def run_native(args, wl, world, rank, local):
     if rank == 0 and not args.no_cpu_baseline and not quant:   # the oracle sample is the BF16 layer
         import oracle
         oracle.build()
-        rng = np.random.default_rng(0)
-        toks = sorted(rng.choice(T, min(args.cpu_tokens, T), replace=False).tolist())
-        secs, n = oracle_sample(wl, g["logits"].cpu().numpy(), synth.bf16_bits(g["x"]), toks, dev, seed=rank)
-        cpu = {"value": n / secs, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-               "sample": f"{n} random tokens of the {T}-token batch: routing, their top-{k} expert rows with FP64 "
-                         f"sums, and the combine ({secs:.1f} s single-threaded)"}
+        cpu = cpu_baseline(wl, g, dev, seed=rank)
 
     if rank == 0:
         line = {
@@ -587,9 +692,10 @@ def run_native(args, wl, world, rank, local):
             "expert_up_tflops": achieved,
             "dispatch_combine_gbs": dc_gbs, "dispatch_combine_hbm_frac": dc_gbs / peaks["hbm_gbs"],
             "gemm_tflops": gemm_tflops, "gemm_frac": gemm_tflops / peak,
+            "per_clock": per_clock, "steps_ms": step_stats,
             "stages_ms": stage_ms, "algorithmic": alg, "router_front": router_front,
             "e2e": e2e, "gpu_launches": kernels_per_layer * args.steps,
-            "clocks": clk.summary(), "cpu_baseline": cpu,
+            "clocks": clocks, "cpu_baseline": cpu,
             "kernel_source_sha": kernel_source_sha(),
         }
         print(json.dumps(line), flush=True)
@@ -603,7 +709,6 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(synth.WORKLOADS))
-    ap.add_argument("--cpu-tokens", type=int, default=24)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--weights", default="bf16", choices=["bf16", "fp8", "nvfp4"],
                     help="expert weight format (fp8: E4M3 codes with a scale per row, moe_layer_fp8; nvfp4: E2M1 "
