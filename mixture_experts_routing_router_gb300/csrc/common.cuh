@@ -339,6 +339,51 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
          | ((uint32_t)(M >> 4) << 24);             // M >> 4
 }
 
+// ---- weight decoders (FP8 E4M3, NVFP4 E2M1) to BF16 ---------------------------
+// Four E4M3 codes (bytes 0..3 of w) -> four BF16 values, exact, in integer and
+// one BF16 multiply per pair: prmt spreads two codes into 16-bit halves with
+// the sign byte replicated above each ([S|b]); shifting left 4 and masking
+// with 0x87F0 per half leaves the sign at bit 15 and the code's 7 exponent and
+// mantissa bits at bits 4..10 -- a BF16 whose exponent field is the E4M3
+// exponent field (bias 127 instead of 7) -- and multiplying by 2^120 rebiases
+// it.  An E4M3 subnormal (exponent field 0) is then a BF16 subnormal m*2^-129,
+// and the same multiply gives m*2^-9 exactly.  Out: lo = (b0, b1), hi = (b2, b3),
+// low half first.  The E4M3 NaN codes (S.1111.111) are not valid weights; they
+// decode to +-480 here.
+__device__ __forceinline__ void e4m3x4_to_bf16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    constexpr uint32_t kTwo120 = 0x7B807B80u;                 // (2^120, 2^120) in BF16
+    uint32_t t0, t1;
+    asm("prmt.b32 %0, %1, 0, 0x9180;" : "=r"(t0) : "r"(w));  // [S1 b1 S0 b0]
+    asm("prmt.b32 %0, %1, 0, 0xB3A2;" : "=r"(t1) : "r"(w));  // [S3 b3 S2 b2]
+    t0 = (t0 << 4) & 0x87F087F0u;
+    t1 = (t1 << 4) & 0x87F087F0u;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(lo) : "r"(t0), "r"(kTwo120));
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(hi) : "r"(t1), "r"(kTwo120));
+}
+
+// Eight E2M1 codes (the nibbles of w, element 0 in the low nibble) times a
+// block scale -> four BF16 pairs (elements 2j, 2j+1 in out[j], low half
+// first), exact.  The codes are split into even and odd elements, one per
+// byte; prmt places element 2j in the low and 2j+1 in the high 16-bit half
+// (zero bytes from the sign-replicate selector on a byte below 0x80), and the
+// multiply by 0x1040 adds the copies shifted by 6 and by 12 (disjoint bits),
+// so the mask keeps the code's exponent and mantissa bits at bits 6..8 and
+// its sign at bit 15 of each half: the BF16 number e2m1 * 2^-126 (subnormal
+// for exponent field 0, where E2M1 is 0 or 0.5, exactly as E2M1 defines it).
+// m = (s, s) with s = block scale * 2^126 * 2^-8 finishes the value in one
+// BF16 multiply: at most 2 + 4 significant bits, within the normal range.
+__device__ __forceinline__ void e2m1x8_to_bf16x8(uint32_t w, uint32_t m, uint32_t* out) {
+    const uint32_t ev = w & 0x0F0F0F0Fu;                      // elements 0, 2, 4, 6
+    const uint32_t od = (w >> 4) & 0x0F0F0F0Fu;               // elements 1, 3, 5, 7
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        uint32_t t;
+        asm("prmt.b32 %0, %1, %2, %3;" : "=r"(t) : "r"(ev), "r"(od), "r"(0x8480u + 0x0101u * (uint32_t)j));
+        t = (t * 0x1040u) & 0x81C081C0u;
+        asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(out[j]) : "r"(t), "r"(m));
+    }
+}
+
 // ---------------------------------------------------------------------------
 // Host-side launchers (one per translation unit); all return cudaError_t of the launch.
 // ---------------------------------------------------------------------------

@@ -807,6 +807,396 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
     }
 }
 
+// ---------------------------------------------------------------------------
+// Quantized expert weights at prefill sizes (ONNX Runtime PR #33963: weight-only
+// quantized FC1/FC2 with BF16 activations; here FP8 E4M3 with a scale per weight
+// row, or NVFP4 with an E4M3 scale per 16 elements and a scale per row).
+// The single-CTA tile of the BF16 kernel -- 128 activation rows (A) by 256
+// weight rows (B) per tile, tcgen05.mma M128 N256 K16 into TMEM -- with B read
+// as codes: the TMA ring carries the A box and two 128-row code boxes per 64-wide
+// K step (16 or 8 KiB of codes instead of 32 KiB of BF16), and eight converter
+// warps decode each step's codes exactly to BF16 (the decoders of the small-row
+// kernel) into a separate ring of swizzled B tiles, which the MMA reads from
+// shared memory.  Each weight tile is converted once per 128-row activation tile,
+// however many rows the group holds.  The row scales multiply the accumulator in
+// the epilogue (NVFP4 tiles are converted at 2^-8 of their value and undone there).
+// A ring stage is released by the converters (codes read) and the MMA (A read).
+// ---------------------------------------------------------------------------
+constexpr int Q_STAGES = 4;
+constexpr int Q_CSLOTS = 2;
+constexpr int Q_CONV_WARPS = 8;
+constexpr int Q_THREADS = 192 + 32 * Q_CONV_WARPS;       // producer, MMA, 4 epilogue, 8 converter warps
+constexpr int Q_SLOT_BYTES = B_BYTES;                     // 256 rows x 64 BF16, 128-byte swizzled
+
+template <int WF>
+struct QCfg {
+    static constexpr int CODE_ROW = WF == kWeightNvfp4 ? 32 : 64;   // code bytes per weight row per K step
+    static constexpr int CODE_BOX = 128 * CODE_ROW;                 // one 128-row code box
+    static constexpr int STAGE_BYTES = A_BYTES + 2 * CODE_BOX;      // 32 KiB (FP8) / 24 KiB (NVFP4)
+};
+
+struct QParams {
+    KParams k;
+    const float* wscale;        // FP32 scale per weight row
+    const uint8_t* bscale;      // NVFP4: E4M3 block scales, bscale_stride bytes per weight row
+    long long bscale_stride;
+    int b_rows;                 // weight rows in all (the block-scale reads stay below it)
+};
+
+struct QCtl {
+    float scl[4][256];          // per epilogue warp: the weight-row scales of its tile's 256 B rows
+    unsigned long long full[Q_STAGES];
+    unsigned long long empty[Q_STAGES];
+    unsigned long long cfull[Q_CSLOTS];
+    unsigned long long cempty[Q_CSLOTS];
+    unsigned long long tfull[2];
+    unsigned long long tempty[2];
+    unsigned long long drain;
+    uint32_t tmem_base;
+    int abort;
+    int total_tiles;
+};
+
+// The epilogue chunk with the weight rows' scales: output column col0 + c of the
+// tile takes scale sg[c] (and su[c] for the matching up row), from shared memory.
+template <int MODE>
+__device__ __forceinline__ void epilogue_chunk_q(uint32_t tg, uint32_t tu, bool row_ok, __nv_bfloat16* orow,
+                                                 int col0, int N, const float* sg, const float* su) {
+    uint32_t gv[32], uv[32];
+    tmem_ld_32cols(tg, gv);
+    if (MODE == kGemmSwiGLU) tmem_ld_32cols(tu, uv);
+    tmem_ld_wait();
+    if (!row_ok) return;
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+        const int c0 = col0 + v * 8;
+        if (c0 < N) {                       // N is a multiple of 8: the whole group of 8 is inside
+            uint32_t o[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                float a[2];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int j = v * 8 + 2 * i + h;
+                    const float x = __uint_as_float(gv[j]) * sg[j];
+                    if (MODE == kGemmSwiGLU) {
+                        const float u = __uint_as_float(uv[j]) * su[j];
+                        a[h] = x / (1.0f + __expf(-x)) * u;
+                    } else if (MODE == kGemmReLU2) {
+                        a[h] = x > 0.f ? x * x : 0.f;
+                    } else {
+                        a[h] = x;
+                    }
+                }
+                o[i] = pack2(a[0], a[1]);
+            }
+            *reinterpret_cast<uint4*>(orow + c0) = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+    }
+}
+
+template <int MODE, int WF>
+__global__ void __launch_bounds__(Q_THREADS, 1)
+grouped_gemm_q_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                      const QParams qp) {
+    using QC = QCfg<WF>;
+    constexpr bool FP4W = WF == kWeightNvfp4;
+    constexpr int BN_OUT = (MODE == kGemmSwiGLU) ? 128 : 256;
+    constexpr int BMT = BM;                                  // 128 activation rows per tile
+    const KParams& p = qp.k;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_u32 = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + ((1024u - (raw_u32 & 1023u)) & 1023u);
+    uint8_t* slots = smem + Q_STAGES * QC::STAGE_BYTES;     // converted B tiles
+    QCtl* ctl = reinterpret_cast<QCtl*>(slots + Q_CSLOTS * Q_SLOT_BYTES);
+    int* prefix = reinterpret_cast<int*>(ctl + 1);
+    int* rstart = prefix + (p.groups + 1);
+    int* rcount = rstart + p.groups;
+    const uint32_t smem_base = smem_u32(smem);
+    const uint32_t slot_base = smem_u32(slots);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int ntn = (p.N + BN_OUT - 1) / BN_OUT;
+
+    if (tid == 0) {
+        for (int s = 0; s < Q_STAGES; ++s) {
+            mbar_init(smem_u32(&ctl->full[s]), 1);
+            mbar_init(smem_u32(&ctl->empty[s]), 1 + Q_CONV_WARPS);      // MMA commit + converter warps
+        }
+        for (int c = 0; c < Q_CSLOTS; ++c) {
+            mbar_init(smem_u32(&ctl->cfull[c]), Q_CONV_WARPS);
+            mbar_init(smem_u32(&ctl->cempty[c]), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(smem_u32(&ctl->tfull[a]), 1);
+            mbar_init(smem_u32(&ctl->tempty[a]), 4);
+        }
+        mbar_init(smem_u32(&ctl->drain), 1);
+        ctl->abort = 0;
+        fence_mbar_init();
+        fence_proxy_async_smem();
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&ctl->tmem_base), TMEM_COLS);
+        tmem_relinquish();
+    }
+    pdl_wait();
+    pdl_trigger();
+    // after a capacity overflow in the same layer call no payload moved: no tiles
+    const bool skip = p.gated && p.hdr->cap_exceeded;
+    for (int g = tid; g < p.groups; g += Q_THREADS) {
+        if (skip) {
+            rstart[g] = 0;
+            rcount[g] = 0;
+        } else if (p.offsets) {
+            int lo = p.offsets[g], hi = p.offsets[g + 1];
+            lo = lo < 0 ? 0 : (lo > p.a_rows ? p.a_rows : lo);
+            hi = hi < lo ? lo : (hi > p.a_rows ? p.a_rows : hi);
+            rstart[g] = lo;
+            rcount[g] = hi - lo;
+        } else {
+            rstart[g] = 0;
+            rcount[g] = p.rows_all;
+        }
+    }
+    __syncthreads();
+    if (tid == 0) {             // exclusive scan of tiles per group (at most 1024 groups)
+        int run = 0;
+        for (int g = 0; g < p.groups; ++g) {
+            prefix[g] = run;
+            run += ((rcount[g] + BMT - 1) / BMT) * ntn;
+        }
+        prefix[p.groups] = run;
+        ctl->total_tiles = run;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = ctl->tmem_base;
+    const int total = ctl->total_tiles;
+    volatile int* abort = &ctl->abort;
+    const int nk = (p.K + BK - 1) / BK;
+
+    if (warp == 0) {
+        // ---------------- TMA producer: A box + two code boxes per K step ----------------
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            long long armed = 0;
+            for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+                const Tile t = decode_tile<MODE == kGemmSwiGLU || MODE == kGemmReLU2>(tile, prefix, rstart, rcount, p,
+                                                                                     ntn, BMT);
+                const int a_row = t.row0 + t.mt * BMT;
+                const int b_lo = t.g * p.b_group_rows + t.nt * BN_OUT;
+                const int b_hi = (MODE == kGemmSwiGLU) ? b_lo + p.up_off : b_lo + 128;
+                for (int i = 0; i < nk; ++i) {
+                    if (!mbar_wait_bounded(smem_u32(&ctl->empty[stage]), ph ^ 1u, abort)) { ok = false; break; }
+                    const uint32_t full = smem_u32(&ctl->full[stage]);
+                    const uint32_t sa = smem_base + stage * QC::STAGE_BYTES;
+                    mbar_arrive_expect_tx(full, QC::STAGE_BYTES);
+                    tma_load_2d(sa, &tmA, full, i * BK, a_row);
+                    tma_load_2d(sa + A_BYTES, &tmB, full, i * QC::CODE_ROW, b_lo);
+                    tma_load_2d(sa + A_BYTES + QC::CODE_BOX, &tmB, full, i * QC::CODE_ROW, b_hi);
+                    ++armed;
+                    if (++stage == Q_STAGES) { stage = 0; ph ^= 1u; }
+                }
+            }
+            if (!ok) {
+                // let the copies already issued land before the CTA exits
+                if (!wait_armed_stages(smem_u32(&ctl->full[0]), Q_STAGES, armed)) settle_delay();
+                raise_status(p.hdr, MOE_ERR_TIMEOUT);
+                p.hdr->timeout_site = kSiteGemmProducer;
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer: A from the ring, B from the converted tiles ----------------
+        if (lane == 0) {
+            int stage = 0, acc = 0, cs = 0;
+            uint32_t ph = 0, aph = 0, cph = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+                const Tile t = decode_tile<MODE == kGemmSwiGLU || MODE == kGemmReLU2>(tile, prefix, rstart, rcount, p,
+                                                                                     ntn, BMT);
+                const int rows0 = t.mrows - t.mt * BMT;
+                const uint32_t idesc = rows0 <= kTailRows ? IDESC64 : IDESC;
+                if (!mbar_wait_bounded(smem_u32(&ctl->tempty[acc]), aph ^ 1u, abort)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t d0 = tmem_base + (uint32_t)(acc * BN_MMA);
+                for (int i = 0; i < nk; ++i) {
+                    if (!mbar_wait_bounded(smem_u32(&ctl->full[stage]), ph, abort) ||
+                        !mbar_wait_bounded(smem_u32(&ctl->cfull[cs]), cph, abort)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint64_t ad = sdesc_k_sw128(smem_base + stage * QC::STAGE_BYTES);
+                    const uint64_t bd = sdesc_k_sw128(slot_base + cs * Q_SLOT_BYTES);
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk)
+                        tc_mma_bf16(d0, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc,
+                                    (i > 0 || kk > 0) ? 1u : 0u);
+                    tc_commit(smem_u32(&ctl->empty[stage]));
+                    tc_commit(smem_u32(&ctl->cempty[cs]));
+                    if (++stage == Q_STAGES) { stage = 0; ph ^= 1u; }
+                    if (++cs == Q_CSLOTS) { cs = 0; cph ^= 1u; }
+                }
+                if (!ok) break;
+                tc_commit(smem_u32(&ctl->tfull[acc]));
+                if (++acc == 2) { acc = 0; aph ^= 1u; }
+            }
+            tc_commit(smem_u32(&ctl->drain));
+            volatile int never = 0;
+            const bool drained = mbar_wait_bounded(smem_u32(&ctl->drain), 0, &never);
+            if (!ok || !drained) {
+                raise_status(p.hdr, MOE_ERR_TIMEOUT);
+                p.hdr->timeout_site = kSiteGemmMma;
+                *abort = 1;
+            }
+        }
+    } else if (warp >= 6) {
+        // ---------------- converters (warps 6..13): codes -> swizzled BF16 B tile ----------------
+        // Thread ct takes, in four passes, weight row r = 64*pass + ct/4 of the
+        // 256-row tile and its 16-element quarter qd = ct%4 of the 64-wide K step:
+        // reads 16 codes (FP8: 16 bytes; NVFP4: 8 bytes and the block's scale),
+        // writes 16 BF16 as two 16-byte chunks of the row at chunk (2qd + h) ^ (r%8).
+        const int ct = tid - 192;
+        const int qd = ct & 3;
+        int stage = 0, cs = 0;
+        uint32_t ph = 0, cph = 0;
+        bool ok = true;
+        // NVFP4: this quarter's block scale of each pass, for 64-wide step i
+        // (read from global memory one step ahead, never past K or the weight rows)
+        auto block_scales = [&](int b_lo, int b_hi, int i, uint32_t (&s4)[4]) {
+#pragma unroll
+            for (int pass = 0; pass < 4; ++pass) {
+                const int r = pass * 64 + (ct >> 2);
+                const int wrow = ((r >> 7) ? b_hi : b_lo) + (r & 127);
+                const int k0 = i * BK + qd * 16;
+                s4[pass] = (k0 < p.K && wrow < qp.b_rows)
+                               ? (uint32_t)__ldg(qp.bscale + (long long)wrow * qp.bscale_stride + (k0 >> 4)) : 0x100u;
+            }
+        };
+        for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+            const Tile t = decode_tile<MODE == kGemmSwiGLU || MODE == kGemmReLU2>(tile, prefix, rstart, rcount, p,
+                                                                                 ntn, BMT);
+            const int b_lo = t.g * p.b_group_rows + t.nt * BN_OUT;
+            const int b_hi = (MODE == kGemmSwiGLU) ? b_lo + p.up_off : b_lo + 128;
+            uint32_t s_next[4] = {0u, 0u, 0u, 0u};
+            if (FP4W) block_scales(b_lo, b_hi, 0, s_next);
+            for (int i = 0; i < nk; ++i) {
+                uint32_t s_cur[4];
+#pragma unroll
+                for (int pass = 0; pass < 4; ++pass) s_cur[pass] = s_next[pass];
+                if (FP4W && i + 1 < nk) block_scales(b_lo, b_hi, i + 1, s_next);
+                if (!mbar_wait_bounded(smem_u32(&ctl->full[stage]), ph, abort) ||
+                    !mbar_wait_bounded(smem_u32(&ctl->cempty[cs]), cph ^ 1u, abort)) { ok = false; break; }
+                const uint8_t* codes = smem + stage * QC::STAGE_BYTES + A_BYTES;
+                uint8_t* dst = slots + cs * Q_SLOT_BYTES;
+#pragma unroll
+                for (int pass = 0; pass < 4; ++pass) {
+                    const int r = pass * 64 + (ct >> 2);
+                    const uint8_t* src = codes + (r >> 7) * QC::CODE_BOX + (r & 127) * QC::CODE_ROW;
+                    uint32_t v[8];
+                    if constexpr (FP4W) {
+                        // this quarter is one 16-element block: its E4M3 scale, at 2^-8
+                        // (0x100 marks a block past K or the weight rows: zeros)
+                        uint32_t m = 0u;
+                        if (s_cur[pass] != 0x100u) {
+                            constexpr uint32_t kTwo118 = 0x7A807A80u;       // (2^118, 2^118) in BF16
+                            uint32_t lo, hi;
+                            e4m3x4_to_bf16x4(s_cur[pass], lo, hi);
+                            asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(lo) : "r"(lo), "r"(kTwo118));
+                            asm("prmt.b32 %0, %1, 0, 0x1010;" : "=r"(m) : "r"(lo));
+                        }
+                        const uint2 w = *reinterpret_cast<const uint2*>(src + qd * 8);
+                        e2m1x8_to_bf16x8(w.x, m, &v[0]);
+                        e2m1x8_to_bf16x8(w.y, m, &v[4]);
+                    } else {
+                        const uint4 w = *reinterpret_cast<const uint4*>(src + qd * 16);
+                        e4m3x4_to_bf16x4(w.x, v[0], v[1]);
+                        e4m3x4_to_bf16x4(w.y, v[2], v[3]);
+                        e4m3x4_to_bf16x4(w.z, v[4], v[5]);
+                        e4m3x4_to_bf16x4(w.w, v[6], v[7]);
+                    }
+                    uint8_t* drow = dst + r * 128;
+                    *reinterpret_cast<uint4*>(drow + (((2 * qd) ^ (r & 7)) << 4)) = make_uint4(v[0], v[1], v[2], v[3]);
+                    *reinterpret_cast<uint4*>(drow + (((2 * qd + 1) ^ (r & 7)) << 4)) =
+                        make_uint4(v[4], v[5], v[6], v[7]);
+                }
+                // the BF16 tile is read by the tensor core (async proxy); the codes
+                // have been read: release both
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(smem_u32(&ctl->cfull[cs]));
+                    mbar_arrive(smem_u32(&ctl->empty[stage]));
+                }
+                if (++stage == Q_STAGES) { stage = 0; ph ^= 1u; }
+                if (++cs == Q_CSLOTS) { cs = 0; cph ^= 1u; }
+            }
+        }
+    } else {
+        // ---------------- epilogue (warps 2..5): scales, activation, BF16 stores ----------------
+        const int q = warp & 3;
+        const float undo = FP4W ? 256.f : 1.f;
+        int acc = 0;
+        uint32_t aph = 0;
+        for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+            const Tile t = decode_tile<MODE == kGemmSwiGLU || MODE == kGemmReLU2>(tile, prefix, rstart, rcount, p,
+                                                                                 ntn, BMT);
+            const int n0 = t.nt * BN_OUT;
+            // the tile's 256 weight-row scales into this warp's shared slice while
+            // the accumulator fills (SwiGLU: 128 gate rows, then the 128 up rows);
+            // warp-local, so a warp that gives up leaves no other warp waiting
+            float* scl = ctl->scl[q];
+#pragma unroll
+            for (int j = lane; j < 256; j += 32) {
+                const int col = n0 + (MODE == kGemmSwiGLU ? (j & 127) : j);
+                const long long row = (long long)t.g * p.b_group_rows + col +
+                                      ((MODE == kGemmSwiGLU && j >= 128) ? p.up_off : 0);
+                scl[j] = col < p.N ? __ldg(qp.wscale + row) * undo : 0.f;
+            }
+            __syncwarp();
+            if (!mbar_wait_bounded(smem_u32(&ctl->tfull[acc]), aph, abort)) {
+                if (lane == 0) {
+                    raise_status(p.hdr, MOE_ERR_TIMEOUT);
+                    p.hdr->timeout_site = kSiteGemmEpilogue;
+                }
+                break;
+            }
+            tc_fence_after();
+            const int hrow0 = t.mt * BMT;
+            const bool m64 = t.mrows - hrow0 <= kTailRows;
+            const int r = m64 ? hrow0 + q * 16 + lane : hrow0 + q * 32 + lane;
+            const bool row_ok = (!m64 || lane < 16) && r < t.mrows;
+            __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(out_row<MODE>(p, t.row0 + (row_ok ? r : 0), t.g));
+            const uint32_t tbase = tmem_base + (uint32_t)(acc * BN_MMA) + ((uint32_t)(q * 32) << 16);
+            if (MODE == kGemmSwiGLU) {
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c)
+                    epilogue_chunk_q<MODE>(tbase + c * 32, tbase + 128 + c * 32, row_ok, orow, n0 + c * 32, p.N,
+                                           scl + c * 32, scl + 128 + c * 32);
+            } else {
+#pragma unroll 1
+                for (int c = 0; c < 8; ++c)
+                    epilogue_chunk_q<MODE>(tbase + c * 32, 0, row_ok, orow, n0 + c * 32, p.N, scl + c * 32,
+                                           scl + c * 32);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[acc]));
+            if (++acc == 2) { acc = 0; aph ^= 1u; }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
 // ---- host side ---------------------------------------------------------------
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -882,6 +1272,31 @@ cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const KPar
     return e;
 }
 
+template <int MODE, int WF>
+cudaError_t launch_q(const CUtensorMap& ma, const CUtensorMap& mb, const QParams& qp, size_t smem,
+                     cudaStream_t st) {
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [] {
+        attr_err = cudaFuncSetAttribute(grouped_gemm_q_kernel<MODE, WF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        MAX_DYN_SMEM);
+    });
+    if (attr_err != cudaSuccess) {
+        set_error("cudaFuncSetAttribute(max dynamic smem %d): %s", MAX_DYN_SMEM, cudaGetErrorString(attr_err));
+        return attr_err;
+    }
+    const cudaError_t e = launch_kernel(grouped_gemm_q_kernel<MODE, WF>, dim3((unsigned)device_sm_count()),
+                                        dim3(Q_THREADS), smem, st, 1, kUsePdl, ma, mb, qp);
+    if (e != cudaSuccess) set_error("quantized grouped GEMM launch (smem %zu): %s", smem, cudaGetErrorString(e));
+    return e;
+}
+
+template <int WF>
+size_t q_smem_bytes(int groups) {
+    return 1024 + (size_t)Q_STAGES * QCfg<WF>::STAGE_BYTES + (size_t)Q_CSLOTS * Q_SLOT_BYTES + sizeof(QCtl) +
+           3 * (size_t)(groups + 1) * 4;
+}
+
 size_t pair_smem_bytes(int groups) {
     return 1024 + (size_t)P_STAGES * P_STAGE_BYTES + sizeof(PairCtl) + 3 * (size_t)(groups + 1) * 4 +
            (size_t)P_XG_FLOATS * 4;
@@ -935,14 +1350,76 @@ moe_status launch_grouped_gemm(const GemmProblem& g, WsHeader* hdr, cudaStream_t
     // stream a few percent better (measured at 1 to 16 tokens over 240 experts).
     const long long row_bound = g.offsets ? (g.max_group_rows > 0 ? g.max_group_rows : g.a_rows) : g.rows_all;
     if (g.wfmt != kWeightBf16) {
-        // FP8 and NVFP4 weights are decoded by the small-row kernel at any size
-        // (groups of more than 64 rows are taken in 64-row chunks)
         if (g.nseg != 1) {
             set_error("grouped GEMM: quantized weights take one K segment");
             return MOE_ERR_UNSUPPORTED;
         }
-        const int nb = row_bound >= kDecodeRows ? kDecodeRows : (row_bound < 16 ? 16 : (int)((row_bound + 15) / 16 * 16));
-        return launch_decode_gemm(g, nb, hdr, st);
+        // Groups of up to 64 rows (decode): the small-row kernel, weights on the
+        // MMA's M side, converted into tensor memory.  Larger groups (prefill):
+        // the tile kernel with converted B tiles, each weight tile converted once
+        // per 128 activation rows instead of re-streamed per 64-row chunk.
+        if (row_bound <= kDecodeRows || g.mode == kGemmF32) {
+            const int nb = row_bound >= kDecodeRows ? kDecodeRows
+                                                    : (row_bound < 16 ? 16 : (int)((row_bound + 15) / 16 * 16));
+            return launch_decode_gemm(g, nb, hdr, st);
+        }
+        const bool fp4 = g.wfmt == kWeightNvfp4;
+        if (fp4 && (!g.bscale || g.K % 32 != 0 || g.bscale_stride * 16 < g.K)) {
+            set_error("grouped GEMM: NVFP4 weights need K %% 32 == 0 and block-scale rows covering K");
+            return MOE_ERR_UNSUPPORTED;
+        }
+        if (!g.wscale) {
+            set_error("grouped GEMM: quantized weights need a scale per weight row");
+            return MOE_ERR_UNSUPPORTED;
+        }
+        const size_t smem = fp4 ? q_smem_bytes<kWeightNvfp4>(g.groups) : q_smem_bytes<kWeightFp8E4M3>(g.groups);
+        if (smem > (size_t)MAX_DYN_SMEM) {
+            set_error("quantized grouped GEMM needs %zu bytes of shared memory", smem);
+            return MOE_ERR_UNSUPPORTED;
+        }
+        CUtensorMap ma, mb;
+        if (!make_map(&ma, g.a, g.a_rows, g.a_cols)) return MOE_ERR_CUDA;
+        const long long code_cols = fp4 ? g.b_cols / 2 : g.b_cols;
+        if (!make_tensor_map_u8_rows(&mb, g.b, g.b_rows, code_cols, code_cols,
+                                     (unsigned)(fp4 ? QCfg<kWeightNvfp4>::CODE_ROW : QCfg<kWeightFp8E4M3>::CODE_ROW),
+                                     128u))
+            return MOE_ERR_CUDA;
+        QParams qp;
+        qp.k.offsets = g.offsets;
+        qp.k.groups = g.groups;
+        qp.k.rows_all = g.rows_all;
+        qp.k.a_rows = (int)g.a_rows;
+        qp.k.K = g.K;
+        qp.k.nseg = 1;
+        qp.k.a_seg_col = 0;
+        qp.k.b_seg_row = 0;
+        qp.k.N = g.N;
+        qp.k.b_group_rows = g.b_group_rows;
+        qp.k.up_off = g.up_off;
+        qp.k.out = g.out;
+        qp.k.ldo = g.ldo;
+        qp.k.out_group_col = g.out_group_col;
+        qp.k.hdr = hdr;
+        qp.k.gated = g.gated;
+        qp.wscale = g.wscale;
+        qp.bscale = g.bscale;
+        qp.bscale_stride = g.bscale_stride;
+        qp.b_rows = (int)g.b_rows;
+        cudaError_t e;
+        if (fp4) {
+            switch (g.mode) {
+                case kGemmSwiGLU: e = launch_q<kGemmSwiGLU, kWeightNvfp4>(ma, mb, qp, smem, st); break;
+                case kGemmReLU2: e = launch_q<kGemmReLU2, kWeightNvfp4>(ma, mb, qp, smem, st); break;
+                default: e = launch_q<kGemmPlain, kWeightNvfp4>(ma, mb, qp, smem, st); break;
+            }
+        } else {
+            switch (g.mode) {
+                case kGemmSwiGLU: e = launch_q<kGemmSwiGLU, kWeightFp8E4M3>(ma, mb, qp, smem, st); break;
+                case kGemmReLU2: e = launch_q<kGemmReLU2, kWeightFp8E4M3>(ma, mb, qp, smem, st); break;
+                default: e = launch_q<kGemmPlain, kWeightFp8E4M3>(ma, mb, qp, smem, st); break;
+            }
+        }
+        return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
     }
     if (row_bound <= kDecodeRows) {
         const long long slots = g.offsets ? (g.a_rows < g.groups ? g.a_rows : g.groups) : g.groups;

@@ -17,7 +17,8 @@ Workloads (shapes and value laws of the pages' workloads):
                 (ONNX Runtime PR #33963, "Measured CUDA kernel latency")
   deepseek      1024 tokens, H 2048, E 64, top-6, I 1408, SwiGLU, plus two
                 always-on shared experts of intermediate 1408
-                (DeepSeek fleet megakernel REPORT.md, model shape)
+                (DeepSeek fleet megakernel REPORT.md, model shape);
+                deepseek_routed is the same without the shared experts
   large         16384 tokens, H 7168, E 256, top-8, I 2048, SwiGLU, logits
                 N(0,1) plus a Zipf(1.2) expert bias (hot experts)
 Router logits are N(0,1) unless stated; x ~ N(0,1) and W ~ N(0, 0.02) where a
@@ -79,6 +80,9 @@ WORKLOADS = {
     "count_first": Workload("count_first", 2048, 2048, 128, 8, 768, capacity=2048),
     "deepseek": Workload("deepseek", 1024, 2048, 64, 6, 1408, shared=2, shared_inter=1408),
     "large": Workload("large", 16384, 7168, 256, 8, 2048, logits="zipf"),
+    # the DeepSeek shape without its shared experts (the quantized entry points
+    # take routed experts only)
+    "deepseek_routed": Workload("deepseek_routed", 1024, 2048, 64, 6, 1408),
     # profiling case of the large layer's kernels: same hidden / intermediate /
     # top-k, 32 experts and 4096 tokens (about 3 GB on the device)
     "large_e32": Workload("large_e32", 4096, 7168, 32, 8, 2048, logits="zipf"),
