@@ -634,10 +634,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
                     const uint32_t s_rows = swap ? sa + A_BYTES : sa;
                     const uint32_t s_w = swap ? sa : sa + A_BYTES;
                     tma_load_2d_pair(s_rows, &tmA, full_leader, seg * p.a_seg_col + kb * BK, a_row);
-                    if (MODE == kGemmSwiGLU) {   // two 64-row boxes: gate, then up
-                        tma_load_2d_pair(s_w, &tmB, full_leader, kb * BK, b_row + seg * p.b_seg_row);
-                        tma_load_2d_pair(s_w + B_HALF_BYTES / 2, &tmB, full_leader, kb * BK,
-                                         b_row + p.up_off + seg * p.b_seg_row);
+                    if (MODE == kGemmSwiGLU) {   // 64 gate rows, then the 64 up rows: one 4-D box
+                        tma_load_4d_pair(s_w, &tmB, full_leader, kb * BK, n0 + (int)rank * 64, 0, t.g);
                     } else {
                         tma_load_2d_pair(s_w, &tmB, full_leader, kb * BK, b_row + seg * p.b_seg_row);
                     }
@@ -1234,6 +1232,37 @@ bool make_map(CUtensorMap* m, const void* base, long long rows, long long cols, 
     return true;
 }
 
+// SwiGLU weights [groups x (gate rows | up rows), cols] BF16 seen as 4-D
+// (cols, row in half, half, group): one box brings box_rows gate rows and the
+// up rows of the same output columns, gate first -- in shared memory exactly
+// the two box_rows-row boxes of the 2-D map, one after the other, in one copy
+// instead of two.  Rows past the half's end read zeros.
+bool make_map_glu(CUtensorMap* m, const void* base, long long rows, long long cols, long long half_rows,
+                  long long group_rows, unsigned box_rows) {
+    auto enc = encode_fn();
+    if (!enc) {
+        set_error("cuTensorMapEncodeTiled is not available from the driver");
+        return false;
+    }
+    if (half_rows < 1 || group_rows != 2 * half_rows || rows % group_rows != 0) {
+        set_error("SwiGLU weight map: %lld rows in groups of %lld, half %lld", rows, group_rows, half_rows);
+        return false;
+    }
+    cuuint64_t dims[4] = {(cuuint64_t)cols, (cuuint64_t)half_rows, 2u, (cuuint64_t)(rows / group_rows)};
+    cuuint64_t strides[3] = {(cuuint64_t)cols * 2, (cuuint64_t)(half_rows * cols * 2), (cuuint64_t)(group_rows * cols * 2)};
+    cuuint32_t box[4] = {(cuuint32_t)BK, (cuuint32_t)box_rows, 2u, 1u};
+    cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
+                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        set_error("cuTensorMapEncodeTiled failed (CUresult %d) for SwiGLU weights [%lld, %lld] at %p", (int)r, rows,
+                  cols, base);
+        return false;
+    }
+    return true;
+}
+
 template <int MODE, int HALVES>
 cudaError_t launch_mode(const CUtensorMap& ma, const CUtensorMap& mb, const KParams& kp, size_t smem,
                         cudaStream_t st) {
@@ -1430,9 +1459,16 @@ moe_status launch_grouped_gemm(const GemmProblem& g, WsHeader* hdr, cudaStream_t
     const bool pairs = avg_rows >= kPairRows && device_sm_count() >= 2;
     CUtensorMap ma, mb;
     if (!make_map(&ma, g.a, g.a_rows, g.a_cols)) return MOE_ERR_CUDA;
-    // the pair kernel loads a SwiGLU B half as 64 gate rows + 64 up rows
-    if (!make_map(&mb, g.b, g.b_rows, g.b_cols, (pairs && g.mode == kGemmSwiGLU) ? 64u : 128u))
+    // the pair kernel loads a SwiGLU B half as 64 gate rows + 64 up rows (one 4-D box)
+    if (pairs && g.mode == kGemmSwiGLU) {
+        if (g.nseg != 1) {
+            set_error("grouped GEMM: SwiGLU over %d K segments", g.nseg);
+            return MOE_ERR_UNSUPPORTED;
+        }
+        if (!make_map_glu(&mb, g.b, g.b_rows, g.b_cols, g.up_off, g.b_group_rows, 64u)) return MOE_ERR_CUDA;
+    } else if (!make_map(&mb, g.b, g.b_rows, g.b_cols, 128u)) {
         return MOE_ERR_CUDA;
+    }
     KParams kp;
     kp.offsets = g.offsets;
     kp.groups = g.groups;
