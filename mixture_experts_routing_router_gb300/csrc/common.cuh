@@ -203,6 +203,21 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, uint
         " [%0], [%1, {%3, %4}], [%2];"
         :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y) : "memory");
 }
+// 3-D / 5-D tiled loads: coordinates innermost first.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, uint32_t bar, int x, int y, int z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];"
+        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y), "r"(z) : "memory");
+}
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const void* tmap, uint32_t bar, int x, int y, int z, int w,
+                                            int v) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];"
+        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w), "r"(v)
+        : "memory");
+}
 // 4-D tiled load: coordinates (x, y, z, w), innermost first.
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* tmap, uint32_t bar, int x, int y, int z, int w) {
     asm volatile(
@@ -506,6 +521,17 @@ moe_status launch_decode_gemm(const GemmProblem& p, int nb, WsHeader* hdr, cudaS
 // Tensor map of a row-major [rows, cols] BF16 matrix, 128-byte swizzle, boxes
 // of 64 columns x box_rows rows (records the failure for moe_last_error_message).
 bool make_tensor_map_bf16(CUtensorMap* m, const void* base, long long rows, long long cols, unsigned box_rows);
+// [rows, cols] BF16 with cols a multiple of 64, as (column in chunk, row, chunk):
+// a box of `chunks` 64-column chunks of box_rows rows lands as that many
+// 128-byte swizzled [box_rows x 64] tiles, one after the other; chunks past the
+// last read zeros.
+bool make_tensor_map_bf16_chunks(CUtensorMap* m, const void* base, long long rows, long long cols, unsigned box_rows,
+                                 unsigned chunks);
+// SwiGLU weights [groups x (half_rows gate | half_rows up), cols] as (column in
+// chunk, row in half, half, group, chunk): per chunk a box lands as box_rows
+// gate rows, then the up rows of the same output columns.
+bool make_tensor_map_glu_chunks(CUtensorMap* m, const void* base, long long rows, long long cols, long long half_rows,
+                                long long group_rows, unsigned box_rows, unsigned chunks);
 // Tensor map of a [rows, cols] byte matrix with row stride `stride` bytes (a
 // multiple of 16; FP8 / NVFP4 codes, NVFP4 block scales), boxes of box_cols
 // bytes x box_rows rows; 128-byte boxes are 128-byte swizzled, others not.

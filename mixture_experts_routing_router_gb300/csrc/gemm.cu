@@ -1339,6 +1339,61 @@ size_t smem_bytes(int groups) {
 
 }  // namespace
 
+bool make_tensor_map_bf16_chunks(CUtensorMap* m, const void* base, long long rows, long long cols, unsigned box_rows,
+                                 unsigned chunks) {
+    auto enc = encode_fn();
+    if (!enc) {
+        set_error("cuTensorMapEncodeTiled is not available from the driver");
+        return false;
+    }
+    if (cols % BK != 0) {
+        set_error("chunked tensor map: %lld columns are not whole 64-column chunks", cols);
+        return false;
+    }
+    cuuint64_t dims[3] = {(cuuint64_t)BK, (cuuint64_t)rows, (cuuint64_t)(cols / BK)};
+    cuuint64_t strides[2] = {(cuuint64_t)cols * 2, (cuuint64_t)BK * 2};
+    cuuint32_t box[3] = {(cuuint32_t)BK, (cuuint32_t)box_rows, (cuuint32_t)chunks};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        set_error("cuTensorMapEncodeTiled failed (CUresult %d) for a chunked [%lld, %lld] bf16 tensor at %p", (int)r,
+                  rows, cols, base);
+        return false;
+    }
+    return true;
+}
+
+bool make_tensor_map_glu_chunks(CUtensorMap* m, const void* base, long long rows, long long cols, long long half_rows,
+                                long long group_rows, unsigned box_rows, unsigned chunks) {
+    auto enc = encode_fn();
+    if (!enc) {
+        set_error("cuTensorMapEncodeTiled is not available from the driver");
+        return false;
+    }
+    if (cols % BK != 0 || half_rows < 1 || group_rows != 2 * half_rows || rows % group_rows != 0) {
+        set_error("chunked SwiGLU weight map: [%lld, %lld] in groups of %lld, half %lld", rows, cols, group_rows,
+                  half_rows);
+        return false;
+    }
+    cuuint64_t dims[5] = {(cuuint64_t)BK, (cuuint64_t)half_rows, 2u, (cuuint64_t)(rows / group_rows),
+                          (cuuint64_t)(cols / BK)};
+    cuuint64_t strides[4] = {(cuuint64_t)cols * 2, (cuuint64_t)(half_rows * cols * 2),
+                             (cuuint64_t)(group_rows * cols * 2), (cuuint64_t)BK * 2};
+    cuuint32_t box[5] = {(cuuint32_t)BK, (cuuint32_t)box_rows, 2u, 1u, (cuuint32_t)chunks};
+    cuuint32_t estr[5] = {1u, 1u, 1u, 1u, 1u};
+    const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box,
+                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        set_error("cuTensorMapEncodeTiled failed (CUresult %d) for chunked SwiGLU weights [%lld, %lld] at %p",
+                  (int)r, rows, cols, base);
+        return false;
+    }
+    return true;
+}
+
 bool make_tensor_map_bf16(CUtensorMap* m, const void* base, long long rows, long long cols, unsigned box_rows) {
     return make_map(m, base, rows, cols, box_rows);
 }

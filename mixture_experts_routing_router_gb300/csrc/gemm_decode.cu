@@ -12,12 +12,19 @@
 // picks NB from a bound on the rows per group).
 //
 // Persistent CTAs (at most one per SM) take items round-robin.  Roles: warp 0
-// lane 0 issues the TMA loads of a ring of stages (weights: one 128-row box,
-// SwiGLU two -- the gate rows and the matching up rows; activations: one
-// NB-row box); warp 1 lane 0 issues tcgen05.mma into one of two accumulators;
+// lane 0 issues the TMA loads of a ring of stages; warp 1 lane 0 issues
+// tcgen05.mma into one of two accumulators;
 // warps 2..5 run the epilogue (warp w owns TMEM lanes 32(w%4)..+31, i.e. the
 // output columns n0 + 32(w%4) + lane) while the next item streams.  The list
 // of non-empty groups is built once per CTA from the offsets.
+//
+// BF16 stages: the TMA unit of an SM takes about the same time per stage for
+// 16 as for 64 KiB (a streaming microbenchmark: ~45 GB/s per SM from DRAM with
+// one 16 KiB box per stage, ~150 GB/s with 64 KiB stages), so a stage carries
+// up to four 64-column chunks of K: the 128 weight rows of each chunk (SwiGLU:
+// gate rows then the matching up rows) in one box of a (column in chunk, row,
+// chunk) view, the NB activation rows of each chunk in one more.  K that is not
+// a whole number of chunks takes one chunk per stage through 2-D maps.
 //
 // The epilogue arithmetic is the tile kernels': SwiGLU silu(g)*u, ReLU^2,
 // plain, or the FP32 accumulator.  Every wait is bounded (MOE_ERR_TIMEOUT,
@@ -66,7 +73,7 @@ constexpr int DBK4 = 256;                  // NVFP4 stage: 256 codes (128 B) of 
 constexpr int S4_BYTES = DBM * 16;         // NVFP4: the 16 block scales of 128 weight rows
 constexpr int MAX_CSLOTS = 4;
 constexpr int MAX_DSTAGES = 16;
-constexpr int MAX_DSMEM = 212 * 1024;
+constexpr int MAX_DSMEM = 222 * 1024;
 
 struct DParams {
     const int32_t* offsets;
@@ -96,6 +103,10 @@ struct DParams {
     // or 2 the weight loads of the first ring stages go out before the wait;
     // the activation loads, which read the predecessor's output, after it.
     int early;
+    // BF16 weights: 64-column K chunks per stage, loaded as one box per operand
+    // through (column in chunk, row, chunk) tensor maps; 0 = one chunk per stage
+    // through plain 2-D maps (K not a whole number of chunks).
+    int kc;
 };
 
 template <int MODE> struct OutOfD { using T = __nv_bfloat16; };
@@ -271,8 +282,11 @@ decode_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
     volatile int* abort = &ctl->abort;
     const int ntn = (p.N + DBM - 1) / DBM;
     const int items = ctl->ng * ntn;
-    // the MMA takes a stage in 64-wide activation boxes
-    const int kstep = KSTEP;
+    // the MMA takes a stage in 64-wide activation boxes; BF16 stages hold kcs
+    // chunks of K (a TMA stage costs an SM about the same time for 16 as for
+    // 64 KiB, so wide stages stream weights faster)
+    const int kcs = (!FP8W && p.kc > 0) ? p.kc : 1;
+    const int kstep = FP8W ? KSTEP : DBK * kcs;
     const int nkb = (p.K + kstep - 1) / kstep;
     const int nk = nkb * p.nseg;
     const uint32_t xbox = (uint32_t)(p.nb * DBK * 2);        // one activation box (nb rows x 64)
@@ -284,6 +298,16 @@ decode_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
     // The TMA loads of one ring stage: its weight boxes (with the NVFP4 block
     // scales), and its activation boxes.
     auto load_weights = [&](uint32_t sa, uint32_t full, int w_row, int seg, int kb) {
+        if constexpr (!FP8W) {
+            if (p.kc > 0) {      // kcs chunks of the weight rows in one box
+                if (MODE == kGemmSwiGLU)   // gate rows, then up rows, per chunk
+                    tma_load_5d(sa + w_off, &tmW, full, 0, w_row % p.b_group_rows, 0, w_row / p.b_group_rows,
+                                kb * kcs);
+                else
+                    tma_load_3d(sa + w_off, &tmW, full, 0, w_row + seg * p.b_seg_row, kb * kcs);
+                return;
+            }
+        }
         const int wcol = FP4W ? kb * (DBK4 / 2) : kb * kstep;     // code bytes
 #pragma unroll
         for (int h = 0; h < NB8; ++h)   // FP8, 256-wide stage: two 128-byte code boxes
@@ -297,6 +321,10 @@ decode_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
         }
     };
     auto load_acts = [&](uint32_t sa, uint32_t full, int xr, int seg, int kb) {
+        if (!FP8W && p.kc > 0) {
+            tma_load_3d(sa + x_off, &tmX, full, 0, xr, seg * (p.a_seg_col / DBK) + kb * kcs);
+            return;
+        }
         for (int xb = 0; xb < kstep / DBK; ++xb)   // 64-wide activation boxes
             tma_load_2d(sa + x_off + (uint32_t)xb * xbox, &tmX, full, seg * p.a_seg_col + kb * kstep + xb * DBK, xr);
     };
@@ -304,13 +332,15 @@ decode_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
     // Bucket bounds known before the programmatic wait: the producer arms the
     // first ring stages and sends their weight loads (weights are never written
     // by a kernel) while the predecessor finishes; every thread then waits, and
-    // the activation loads of those stages follow in the main loop.  Only a few
-    // stages: the TMA unit takes the requests in order, and a CTA that starts
-    // late would otherwise queue its first activation loads behind a ring of
-    // weight loads (measured: 4 stages beat a full ring by about 1 us per layer
-    // at decode).
+    // the activation loads of those stages follow in the main loop.  Only about
+    // 64 KiB of weights (four one-chunk stages, one four-chunk stage): the TMA
+    // unit takes the requests in order, and a CTA that starts late would
+    // otherwise queue its first activation loads behind a ring of weight loads
+    // (measured at decode: four narrow stages beat a full ring by about 1 us per
+    // layer, one wide stage beats three by about 0.7 us).
     constexpr int kPreStages = 4;
-    const int npre_max = p.stages < kPreStages ? p.stages : kPreStages;
+    const int npre_lim = (kPreStages + kcs - 1) / kcs;        // about 64 KiB of weights
+    const int npre_max = p.stages < npre_lim ? p.stages : npre_lim;
     int npre = 0;
     if (!waited) {
         if (warp == 0 && lane == 0) {
@@ -412,16 +442,25 @@ decode_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
                             if (!ok) break;
                         } else {
                             tc_fence_after();
-                            const uint64_t wd = sdesc_k_sw128(sa + w_off);
-                            const uint64_t xd = sdesc_k_sw128(sa + x_off);
+                            // chunk c of the stage: weights at w_off + c * NW * 16 KiB (SwiGLU:
+                            // gate, then up), activations at x_off + c * xbox; chunks past
+                            // this segment's K (the last stage) are not multiplied
+                            const int kb0 = (i - (i / nkb) * nkb) * kcs;
+                            const int nch = p.K / DBK - kb0 < kcs ? p.K / DBK - kb0 : kcs;
+                            for (int c = 0; c < kcs; ++c) {
+                                if (c > 0 && c >= nch) break;
+                                const uint64_t wd = sdesc_k_sw128(sa + w_off + (uint32_t)(c * NW * W_BYTES));
+                                const uint64_t xd = sdesc_k_sw128(sa + x_off + (uint32_t)c * xbox);
 #pragma unroll
-                            for (int kk = 0; kk < DBK / 16; ++kk) {
-                                const uint32_t accum = (i > 0 || kk > 0) ? 1u : 0u;
-                                tc_mma_bf16(d, wd + (uint64_t)(kk * 2), xd + (uint64_t)(kk * 2), idesc, accum);
-                                if (MODE == kGemmSwiGLU)
-                                    tc_mma_bf16(d + (uint32_t)nb,
-                                                sdesc_k_sw128(sa + w_off + W_BYTES) + (uint64_t)(kk * 2),
-                                                xd + (uint64_t)(kk * 2), idesc, accum);
+                                for (int kk = 0; kk < DBK / 16; ++kk) {
+                                    const uint32_t accum = (i > 0 || c > 0 || kk > 0) ? 1u : 0u;
+                                    tc_mma_bf16(d, wd + (uint64_t)(kk * 2), xd + (uint64_t)(kk * 2), idesc, accum);
+                                    if (MODE == kGemmSwiGLU)
+                                        tc_mma_bf16(d + (uint32_t)nb,
+                                                    sdesc_k_sw128(sa + w_off + (uint32_t)(c * NW * W_BYTES) + W_BYTES) +
+                                                        (uint64_t)(kk * 2),
+                                                    xd + (uint64_t)(kk * 2), idesc, accum);
+                                }
                             }
                         }
                         tc_commit(smem_u32(&ctl->empty[stage]));
@@ -664,6 +703,7 @@ moe_status launch_decode_gemm(const GemmProblem& g, int nb, WsHeader* hdr, cudaS
     dp.wscale = g.wscale;
     dp.s_off = 0;
     dp.early = g.offsets ? g.early : 0;
+    dp.kc = 0;
     if (fp4) {
         // stage (K 256): [four activation boxes: nb rows x 128 B each][code box(es):
         // 128 rows x 128 B = 16 KiB each][block-scale box(es): 128 rows x 16 B]
@@ -688,10 +728,20 @@ moe_status launch_decode_gemm(const GemmProblem& g, int nb, WsHeader* hdr, cudaS
         dp.a_col = nw == 1 ? 128 : 256;
         dp.conv_slots = nw == 1 ? 3 : 2;
     } else {
-        // stage: [BF16 weight box(es): 16 KiB each][activation box]
-        dp.x_off = (uint32_t)(nw * W_BYTES);
+        // stage: [kc chunks of the weight rows: nw x 16 KiB each][kc activation
+        // boxes: nb rows x 128 B each], kc as large as leaves three stages (at
+        // most four chunks); one chunk through 2-D maps when K is ragged
+        const size_t fixed0 = 1024 + sizeof(DCtl) + (size_t)3 * g.groups * sizeof(int);
+        const bool chunked = g.K % DBK == 0 && g.a_cols % DBK == 0 && g.b_cols % DBK == 0 && g.a_seg_col % DBK == 0 &&
+                             (g.mode != kGemmSwiGLU || (g.nseg == 1 && g.b_group_rows == 2 * g.up_off));
+        int kc = 1;
+        if (chunked)
+            for (kc = 4; kc > 1; --kc)
+                if (fixed0 + 3 * (size_t)kc * (nw * W_BYTES + nb * DBK * 2) <= (size_t)MAX_DSMEM) break;
+        dp.kc = chunked ? kc : 0;
         dp.w_off = 0;
-        dp.stage_bytes = nw * W_BYTES + nb * DBK * 2;
+        dp.x_off = (uint32_t)(kc * nw * W_BYTES);
+        dp.stage_bytes = kc * (nw * W_BYTES + nb * DBK * 2);
         dp.conv_slots = 0;
         dp.a_col = 0;
     }
@@ -707,7 +757,7 @@ moe_status launch_decode_gemm(const GemmProblem& g, int nb, WsHeader* hdr, cudaS
     if (grid > sms) grid = sms;
     if (grid < 1) grid = 1;
     const size_t fixed = 1024 + sizeof(DCtl) + (size_t)3 * g.groups * sizeof(int);
-    const int kstep = fp4 ? DBK4 : (fp8 ? (nw == 1 ? 256 : DBK8) : DBK);
+    const int kstep = fp4 ? DBK4 : (fp8 ? (nw == 1 ? 256 : DBK8) : DBK * (dp.kc > 0 ? dp.kc : 1));
     const int nk = ((g.K + kstep - 1) / kstep) * g.nseg;
     long long stages = ((long long)MAX_DSMEM - (long long)fixed) / dp.stage_bytes;
     if (stages > MAX_DSTAGES) stages = MAX_DSTAGES;
@@ -722,11 +772,20 @@ moe_status launch_decode_gemm(const GemmProblem& g, int nb, WsHeader* hdr, cudaS
         return MOE_ERR_UNSUPPORTED;
     }
     CUtensorMap mx, mw, ms;
-    if (!make_tensor_map_bf16(&mx, g.a, g.a_rows, g.a_cols, (unsigned)nb)) return MOE_ERR_CUDA;
+    if (dp.kc > 0) {
+        if (!make_tensor_map_bf16_chunks(&mx, g.a, g.a_rows, g.a_cols, (unsigned)nb, (unsigned)dp.kc) ||
+            (g.mode == kGemmSwiGLU
+                 ? !make_tensor_map_glu_chunks(&mw, g.b, g.b_rows, g.b_cols, g.up_off, g.b_group_rows,
+                                               (unsigned)DBM, (unsigned)dp.kc)
+                 : !make_tensor_map_bf16_chunks(&mw, g.b, g.b_rows, g.b_cols, (unsigned)DBM, (unsigned)dp.kc)))
+            return MOE_ERR_CUDA;
+    } else if (!make_tensor_map_bf16(&mx, g.a, g.a_rows, g.a_cols, (unsigned)nb)) {
+        return MOE_ERR_CUDA;
+    }
     // code rows: K bytes (FP8) or K/2 bytes (NVFP4, two codes per byte)
     const long long code_cols = fp4 ? g.b_cols / 2 : g.b_cols;
     if (fp8 ? !make_tensor_map_u8_rows(&mw, g.b, g.b_rows, code_cols, code_cols, (unsigned)DBK8, (unsigned)DBM)
-            : !make_tensor_map_bf16(&mw, g.b, g.b_rows, g.b_cols, (unsigned)DBM))
+            : (dp.kc == 0 && !make_tensor_map_bf16(&mw, g.b, g.b_rows, g.b_cols, (unsigned)DBM)))
         return MOE_ERR_CUDA;
     if (fp4) {
         // block scales: K/16 bytes of each padded row, 16 per stage

@@ -44,6 +44,9 @@ SMALL = {
     "pair_relu2": synth.Workload("pair_relu2", 600, 200, 3, 2, 264, act=synth.ACT_RELU2),
     "pair_shared": synth.Workload("pair_shared", 300, 128, 2, 2, 64, shared=2, shared_inter=72),
     "pair_longk": synth.Workload("pair_longk", 300, 4096, 2, 2, 136),
+    # the pair kernel with K of an odd number of 64-column chunks, and two shared
+    # experts summed over K segments (their down projection) on the pair path
+    "pair_oddk": synth.Workload("pair_oddk", 600, 320, 2, 1, 192, shared=2, shared_inter=192),
 }
 for _n in DECODE:
     SMALL[_n] = W[_n]
