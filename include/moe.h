@@ -369,7 +369,8 @@ MOE_API moe_status moe_workspace_set_wait(void* ws, size_t ws_bytes, uint64_t lo
 /* Synchronise `stream` and return in *site where the last bounded wait that
  * ran out on this workspace gave up: 0 none, 1 the count kernel's look-back,
  * 2 a GEMM TMA producer, 3 a GEMM MMA issuer, 4 a GEMM epilogue, 5 the
- * small-row GEMM.  Read it before moe_status_read, which clears it. */
+ * small-row GEMM, 6 moe_layer's fused decode FFN.  Read it before
+ * moe_status_read, which clears it. */
 MOE_API moe_status moe_timeout_site_read(void* ws, void* stream, int32_t* site);
 
 /* A static, human-readable name for a status code. */

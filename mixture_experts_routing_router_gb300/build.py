@@ -20,7 +20,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmoe.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 SOURCES = ["api.cu", "route.cu", "dispatch.cu", "small_dispatch.cu", "combine.cu", "gemm.cu", "gemm_decode.cu",
-           "ep_plan.cu"]
+           "ep_plan.cu", "decode_ffn.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden",
                 "-I", INCLUDE, "--expt-relaxed-constexpr"]

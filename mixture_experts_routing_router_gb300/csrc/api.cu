@@ -305,7 +305,8 @@ moe_status layer_q(const moe_shape* shape, const float* logits, const int32_t* i
     if (small) {
         if ((r = from_cuda(launch_small_dispatch(s, logits, ids_in, at<int32_t>(ws, L.ids), at<float>(ws, L.w), x,
                                                  at<int32_t>(ws, L.counts), offsets, dest,
-                                                 at<int32_t>(ws, L.sorted_pair), x_perm, at<WsHeader>(ws, 0), st))) !=
+                                                 at<int32_t>(ws, L.sorted_pair), x_perm, at<WsHeader>(ws, 0),
+                                                 nullptr, 0, st))) !=
             MOE_OK)
             return r;
     } else if ((r = do_dispatch(s, x, ids, at<int32_t>(ws, L.counts), offsets, dest, at<int32_t>(ws, L.sorted_pair),
@@ -483,12 +484,22 @@ moe_status moe_layer(const moe_shape* shape, const float* logits, const int32_t*
     uint16_t* h = at<uint16_t>(ws, L.h);
     uint16_t* y_perm = at<uint16_t>(ws, L.y_perm);
     uint16_t* y_shared = s.shared > 0 ? at<uint16_t>(ws, L.y_shared) : nullptr;
+    // decode: the expert FFN and the combine in one launch after the fused dispatch
+    const bool fused = small && decode_ffn_fits(s);
+    unsigned* sync = at<unsigned>(ws, L.sync);
     if (small) {
         if ((r = from_cuda(launch_small_dispatch(s, logits, ids_in, at<int32_t>(ws, L.ids), at<float>(ws, L.w), x,
                                                  at<int32_t>(ws, L.counts), offsets, dest,
-                                                 at<int32_t>(ws, L.sorted_pair), x_perm, at<WsHeader>(ws, 0), st))) !=
+                                                 at<int32_t>(ws, L.sorted_pair), x_perm, at<WsHeader>(ws, 0),
+                                                 fused ? sync : nullptr, (int)decode_ffn_sync_words(s), st))) !=
             MOE_OK)
             return r;
+        if (fused) {
+            r = launch_decode_ffn(s, x_perm, offsets, w13, w2, h, y_perm, dest, w, residual, out, sync,
+                                  at<WsHeader>(ws, 0), st);
+            if (r != MOE_OK) reset_route_ready(ws, st);
+            return r;
+        }
     } else if ((r = do_dispatch(s, x, ids, at<int32_t>(ws, L.counts), offsets, dest, at<int32_t>(ws, L.sorted_pair),
                                 x_perm, ws, st)) != MOE_OK) {
         return r;

@@ -46,6 +46,7 @@ struct WsLayout {
     size_t hdr, flags, rank, h_shared;        // stage regions
     size_t stage_end;                         // bytes the stage calls need
     size_t counts, offsets, ids, w, dest, sorted_pair, x_perm, h, y_perm, y_shared;
+    size_t sync;                              // moe_layer's fused decode FFN: its counters
     size_t total;                             // bytes moe_layer needs
     int count_tiles;
 };
@@ -71,6 +72,7 @@ inline WsLayout ws_layout(const moe_shape& s) {
     L.h = o;            o = align_up(o + R * I * 2, kAlign);
     L.y_perm = o;       o = align_up(o + R * H * 2, kAlign);
     L.y_shared = o;     o = align_up(o + (s.shared > 0 ? T * H * 2 : 0), kAlign);
+    L.sync = o;         o = align_up(o + (E + 4 * ((H + 127) / 128) + 1) * 4, kAlign);
     L.total = o;
     return L;
 }
@@ -84,7 +86,7 @@ constexpr unsigned long long kEarlyWaitNs = 200000ull;       // 200 us
 // Where a bounded wait gave up (WsHeader::timeout_site).
 enum TimeoutSite : int {
     kSiteNone = 0, kSiteLookback = 1, kSiteGemmProducer = 2, kSiteGemmMma = 3, kSiteGemmEpilogue = 4,
-    kSiteGemmDecode = 5,
+    kSiteGemmDecode = 5, kSiteDecodeFfn = 6,
 };
 
 // ---------------------------------------------------------------------------
@@ -429,11 +431,24 @@ cudaError_t launch_scatter(const moe_shape& s, const uint16_t* x, const int32_t*
                            int32_t* sorted_pair, uint16_t* x_perm, WsHeader* hdr, cudaStream_t st);
 // Route (when logits is not null; else take ids_in), count and scatter in one
 // kernel for batches of at most kSmallDispatchTokens tokens; results bitwise
-// those of launch_route + launch_count + launch_scatter.
+// those of launch_route + launch_count + launch_scatter.  `sync` (nsync
+// words, or null): counters of the fused decode FFN that follows, zeroed
+// before the bucket bounds are published.
 constexpr int kSmallDispatchTokens = 16;
 cudaError_t launch_small_dispatch(const moe_shape& s, const float* logits, const int32_t* ids_in, int32_t* ids_out,
                                   float* w_out, const uint16_t* x, int32_t* counts, int32_t* offsets, int32_t* dest,
-                                  int32_t* sorted_pair, uint16_t* x_perm, WsHeader* hdr, cudaStream_t st);
+                                  int32_t* sorted_pair, uint16_t* x_perm, WsHeader* hdr, unsigned* sync, int nsync,
+                                  cudaStream_t st);
+// moe_layer at decode: the expert FFN (up, down) and the weighted combine in
+// one persistent launch after the fused dispatch (decode_ffn.cu), for shapes
+// decode_ffn_fits accepts; `sync` is the workspace's counter region
+// (decode_ffn_sync_words words), zeroed by that dispatch.
+bool decode_ffn_fits(const moe_shape& s);
+size_t decode_ffn_sync_words(const moe_shape& s);
+moe_status launch_decode_ffn(const moe_shape& s, const uint16_t* x_perm, const int32_t* offsets,
+                             const uint16_t* w13, const uint16_t* w2, uint16_t* h, uint16_t* y_perm,
+                             const int32_t* dest, const float* topk_w, const uint16_t* residual, uint16_t* out,
+                             unsigned* sync, WsHeader* hdr, cudaStream_t st);
 // gate: NULL, or (inside moe_layer) the workspace header whose capacity verdict,
 // when set, makes the kernel leave `out` untouched; the kernel also puts the
 // header's route_ready back to 0 for the next layer call.

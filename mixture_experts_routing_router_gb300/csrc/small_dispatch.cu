@@ -38,7 +38,7 @@ small_dispatch_kernel(int T, int E, int k, int capacity, const float* __restrict
                       const int32_t* __restrict__ ids_in, int32_t* __restrict__ ids_out, float* __restrict__ w_out,
                       const uint4* __restrict__ x, int HV, int32_t* __restrict__ counts,
                       int32_t* __restrict__ offsets, int32_t* __restrict__ dest, int32_t* __restrict__ sorted_pair,
-                      uint4* __restrict__ x_perm, WsHeader* hdr) {
+                      uint4* __restrict__ x_perm, WsHeader* hdr, unsigned* __restrict__ sync, int nsync) {
     pdl_wait();
     pdl_trigger();
     extern __shared__ int sm[];
@@ -141,13 +141,15 @@ small_dispatch_kernel(int T, int E, int k, int capacity, const float* __restrict
         offs[E] = run;
         if (lead) offsets[E] = run;
     }
+    if (lead && sync)   // the fused decode FFN's counters start from zero
+        for (int i = tid; i < nsync; i += kSDThreads) sync[i] = 0u;
     const int any_over = __syncthreads_or(over);
     if (lead && tid == 0) {
         hdr->cap_exceeded = any_over;
         if (any_over) raise_status(hdr, MOE_ERR_CAPACITY);
-        // ids, weights, counts, offsets and the verdict are written (the block
-        // barrier above orders the other threads' stores before this fence);
-        // the layer's combine puts route_ready back to 0
+        // ids, weights, counts, offsets, the counters and the verdict are
+        // written (the block barrier above orders the other threads' stores
+        // before this fence); the layer's last kernel puts route_ready back to 0
         __threadfence();
         st_release_u32(&hdr->route_ready, 1u);
     }
@@ -179,25 +181,26 @@ small_dispatch_kernel(int T, int E, int k, int capacity, const float* __restrict
 template <int EPL>
 cudaError_t launch_sd(const moe_shape& s, const float* logits, const int32_t* ids_in, int32_t* ids_out, float* w_out,
                       const uint16_t* x, int32_t* counts, int32_t* offsets, int32_t* dest, int32_t* sorted_pair,
-                      uint16_t* x_perm, WsHeader* hdr, cudaStream_t st) {
+                      uint16_t* x_perm, WsHeader* hdr, unsigned* sync, int nsync, cudaStream_t st) {
     const int R = s.tokens * s.top_k;
     const size_t smem = (size_t)(2 * R + 2 * s.experts + 1) * sizeof(int);
     const int grid = s.tokens < device_sm_count() ? s.tokens : device_sm_count();
     return launch_kernel(small_dispatch_kernel<EPL>, dim3((unsigned)grid), dim3(kSDThreads), smem, st, 1, kUsePdl,
                          s.tokens, s.experts, s.top_k, s.capacity, logits, ids_in, ids_out, w_out,
                          reinterpret_cast<const uint4*>(x), s.hidden / 8, counts, offsets, dest, sorted_pair,
-                         reinterpret_cast<uint4*>(x_perm), hdr);
+                         reinterpret_cast<uint4*>(x_perm), hdr, sync, nsync);
 }
 
 }  // namespace
 
 cudaError_t launch_small_dispatch(const moe_shape& s, const float* logits, const int32_t* ids_in, int32_t* ids_out,
                                   float* w_out, const uint16_t* x, int32_t* counts, int32_t* offsets, int32_t* dest,
-                                  int32_t* sorted_pair, uint16_t* x_perm, WsHeader* hdr, cudaStream_t st) {
+                                  int32_t* sorted_pair, uint16_t* x_perm, WsHeader* hdr, unsigned* sync, int nsync,
+                                  cudaStream_t st) {
     if (s.tokens > kSmallDispatchTokens) return cudaErrorInvalidValue;
     auto go = [&](auto epl) {
         return launch_sd<decltype(epl)::value>(s, logits, ids_in, ids_out, w_out, x, counts, offsets, dest,
-                                               sorted_pair, x_perm, hdr, st);
+                                               sorted_pair, x_perm, hdr, sync, nsync, st);
     };
     const int E = s.experts;
     if (E <= 32) return go(std::integral_constant<int, 1>{});

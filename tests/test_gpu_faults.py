@@ -151,3 +151,25 @@ def test_layer_over_capacity_leaves_out_and_residual_untouched(tokens):
                        ids_in=ids.cpu().numpy(), w_in=w.cpu().numpy(), ws13=bits(g["ws13"]), ws2=bits(g["ws2"]),
                        residual=bits(keep))
     assert_close(bits(out), ref["out"], "layer within capacity")
+
+
+def test_fused_decode_layer_over_capacity_leaves_out_and_residual_untouched():
+    """The same at 8 tokens without shared experts, where the expert FFN and
+    the combine run as one kernel after the fused dispatch."""
+    wl = synth.Workload("cap_fused", 8, 128, 8, 2, 64)
+    g = inputs(wl, unit_scale=True, seed=14)
+    ids = torch.zeros(8, 2, dtype=torch.int32, device=dev())
+    ids[:, 1] = 1
+    w = torch.full((8, 2), 0.5, device=dev())
+    shape = N.shape_of(wl)
+    shape.capacity = 4
+    ws = N.workspace(shape, dev())
+    res = synth.normal((8, wl.hidden), 1.0, 14, "residual", dev())
+    keep = res.clone()
+    N.moe_layer(shape, None, ids, w, g["x"], g["w13"], g["w2"], None, None, res, ws, residual=res)
+    assert N.moe_status_read(ws) == N.MOE_ERR_CAPACITY
+    assert torch.equal(res.view(torch.int16), keep.view(torch.int16))
+    # and the workspace runs a valid call afterwards
+    shape.capacity = 8
+    N.moe_layer(shape, None, ids, w, g["x"], g["w13"], g["w2"], None, None, res, ws, residual=res)
+    assert N.moe_status_read(ws) == N.MOE_OK

@@ -165,6 +165,10 @@ EDGE = {
     "max_e": synth.Workload("max_e", 300, 64, 1024, 32, 32),
     "t1": synth.Workload("t1", 1, 256, 16, 4, 128),
     "small_fused": synth.Workload("small_fused", 16, 200, 240, 9, 264, act=synth.ACT_RELU2),
+    # the fused decode FFN (2..16 tokens, whole 64-column chunks): ragged 128-row
+    # blocks of W13 and W2, both activations
+    "decode_ffn_relu2": synth.Workload("decode_ffn_relu2", 7, 320, 20, 5, 192, act=synth.ACT_RELU2),
+    "decode_ffn_swiglu": synth.Workload("decode_ffn_swiglu", 12, 192, 24, 6, 320),
     "shared_ragged": synth.Workload("shared_ragged", 45, 136, 12, 2, 72, shared=2, shared_inter=40),
     "pair_ragged": synth.Workload("pair_ragged", 600, 200, 3, 2, 264, act=synth.ACT_RELU2),
 }

@@ -10,7 +10,7 @@ import oracle
 from mixture_experts_routing_router_gb300 import native as N
 from mixture_experts_routing_router_gb300 import synth
 
-from gpu_util import assert_close, bits, dev, inputs, run_layer
+from gpu_util import alloc_stage_outputs, assert_close, bits, dev, inputs, run_layer
 from test_gpu_stages import SMALL, oracle_stages
 
 pytestmark = pytest.mark.gpu
@@ -207,3 +207,74 @@ def test_layer_random_shapes(wl):
                 residual=res)
     assert N.moe_status_read(ws) == N.MOE_OK
     assert_close(bits(out), ref["out"], f"{wl.name} layer")
+
+
+# Decode-sized layers (2 to 16 tokens) run the expert FFN and the combine as
+# one persistent kernel after the fused dispatch; the separate calls (route, dispatch, expert
+# FFN, combine) run the small-row GEMM and the combine kernel.  Same MMA
+# order, same epilogue and combine arithmetic: equal bit for bit.
+FUSED = {
+    "decode_2_shared": W["decode_1_shared"].with_(tokens=2, name="decode_2_shared"),
+    "decode_16_distinct": W["decode_16_distinct"],
+    "swiglu_t16": synth.Workload("swiglu_t16", 16, 512, 8, 2, 384),              # a partial last down stage
+    "swiglu_t2_e64": synth.Workload("swiglu_t2_e64", 2, 256, 64, 8, 192),        # ragged 128-row blocks
+    "relu2_t5_h320": synth.Workload("relu2_t5_h320", 5, 320, 12, 3, 64, act=synth.ACT_RELU2),
+}
+
+
+def staged_layer(wl, g, residual=None, preselected=None):
+    shape = N.shape_of(wl)
+    ws = N.workspace(shape, dev())
+    o = alloc_stage_outputs(wl)
+    if preselected is None:
+        N.moe_route(shape, g["logits"], o["ids"], o["w"], ws)
+        ids, w = o["ids"], o["w"]
+    else:
+        ids, w = preselected
+    N.moe_dispatch(shape, g["x"], ids, o["counts"], o["offsets"], o["dest"], o["sorted_pair"], o["x_perm"], ws)
+    N.moe_expert_ffn(shape, o["x_perm"], o["offsets"], g["w13"], g["w2"], None, None, None, o["h"], o["y_perm"], None,
+                     ws)
+    N.moe_combine(shape, o["y_perm"], o["dest"], w, None, o["out"], ws, residual=residual)
+    return o["out"], N.moe_status_read(ws)
+
+
+@pytest.mark.parametrize("name", sorted(FUSED))
+def test_decode_fused_layer_equals_separate_kernels(name):
+    wl = FUSED[name]
+    g = inputs(wl, unit_scale=True, seed=41)
+    a, sa = run_layer(wl, g)
+    b, sb = staged_layer(wl, g)
+    assert sa == sb == N.MOE_OK
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    ref = oracle_stages(wl, g)
+    assert_close(bits(a), ref["out"], f"{name} fused out")
+    # in place on the residual, twice on one workspace (the counters start afresh)
+    res = synth.normal((wl.tokens, wl.hidden), 1.0, 41, "residual", dev())
+    want, st = staged_layer(wl, g, residual=res)
+    assert st == N.MOE_OK
+    shape = N.shape_of(wl)
+    ws = N.workspace(shape, dev())
+    for _ in range(2):
+        buf = res.clone()
+        N.moe_layer(shape, g["logits"], None, None, g["x"], g["w13"], g["w2"], None, None, buf, ws, residual=buf)
+        assert N.moe_status_read(ws) == N.MOE_OK
+        assert torch.equal(buf.view(torch.int16), want.view(torch.int16))
+
+
+def test_decode_fused_layer_all_routes_invalid():
+    """No routed row at all: the output is the residual (invalid pairs add
+    nothing), as from the separate combine."""
+    wl = FUSED["relu2_t5_h320"]
+    g = inputs(wl, unit_scale=True, seed=42)
+    ids = torch.full((wl.tokens, wl.top_k), -1, dtype=torch.int32, device=dev())
+    w = torch.full((wl.tokens, wl.top_k), 0.25, device=dev())
+    res = synth.normal((wl.tokens, wl.hidden), 1.0, 42, "residual", dev())
+    shape = N.shape_of(wl)
+    ws = N.workspace(shape, dev())
+    out = torch.empty(wl.tokens, wl.hidden, dtype=torch.bfloat16, device=dev())
+    N.moe_layer(shape, None, ids, w, g["x"], g["w13"], g["w2"], None, None, out, ws, residual=res)
+    assert N.moe_status_read(ws) == N.MOE_ERR_INVALID_ROUTE
+    want, st = staged_layer(wl, g, residual=res, preselected=(ids, w))
+    assert st == N.MOE_ERR_INVALID_ROUTE
+    assert torch.equal(out.view(torch.int16), want.view(torch.int16))
+    assert torch.equal(out.view(torch.int16), res.view(torch.int16))
