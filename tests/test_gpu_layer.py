@@ -278,3 +278,40 @@ def test_decode_fused_layer_all_routes_invalid():
     assert st == N.MOE_ERR_INVALID_ROUTE
     assert torch.equal(out.view(torch.int16), want.view(torch.int16))
     assert torch.equal(out.view(torch.int16), res.view(torch.int16))
+
+
+def test_decode_fused_layer_graph_replays_and_alternates():
+    """The fused decode FFN's counters are zeroed by each call's dispatch and
+    route_ready is put back by the last CTA out: captured in a graph and
+    replayed, and interleaved with a one-token layer (three separate kernels)
+    on the same stream, every output stays bit for bit the eager one."""
+    wl8 = FUSED["decode_2_shared"].with_(tokens=8, name="decode_8_fused")
+    wl1 = FUSED["decode_2_shared"].with_(tokens=1, name="decode_1_sep")
+    s = torch.cuda.Stream()
+    runs = []
+    for wl in (wl8, wl1):
+        g = inputs(wl, unit_scale=True, seed=43)
+        shape = N.shape_of(wl)
+        ws = N.workspace(shape, dev())
+        out = torch.empty(wl.tokens, wl.hidden, dtype=torch.bfloat16, device=dev())
+        with torch.cuda.stream(s):
+            N.moe_layer(shape, g["logits"], None, None, g["x"], g["w13"], g["w2"], None, None, out, ws, s)
+        s.synchronize()
+        assert N.moe_status_read(ws) == N.MOE_OK
+        runs.append((wl, g, shape, ws, out, out.clone()))
+    graphs = []
+    for wl, g, shape, ws, out, _ in runs:
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=s):
+            N.moe_layer(shape, g["logits"], None, None, g["x"], g["w13"], g["w2"], None, None, out, ws, s)
+        graphs.append(gr)
+    for _ in range(5):
+        with torch.cuda.stream(s):
+            for (wl, g, shape, ws, out, eager), gr in zip(runs, graphs):
+                out.zero_()
+                gr.replay()
+        s.synchronize()
+        for wl, g, shape, ws, out, eager in runs:
+            assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
+    for wl, g, shape, ws, out, eager in runs:
+        assert N.moe_status_read(ws) == N.MOE_OK
