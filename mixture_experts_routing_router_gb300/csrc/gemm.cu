@@ -820,10 +820,9 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
 // the epilogue (NVFP4 tiles are converted at 2^-8 of their value and undone there).
 // A ring stage is released by the converters (codes read) and the MMA (A read).
 // ---------------------------------------------------------------------------
-constexpr int Q_STAGES = 4;
+constexpr int Q_STAGES = 4;                               // the most any geometry uses
 constexpr int Q_CSLOTS = 2;
 constexpr int Q_CONV_WARPS = 8;
-constexpr int Q_THREADS = 192 + 32 * Q_CONV_WARPS;       // producer, MMA, 4 epilogue, 8 converter warps
 constexpr int Q_SLOT_BYTES = B_BYTES;                     // 256 rows x 64 BF16, 128-byte swizzled
 
 template <int WF>
@@ -831,6 +830,21 @@ struct QCfg {
     static constexpr int CODE_ROW = WF == kWeightNvfp4 ? 32 : 64;   // code bytes per weight row per K step
     static constexpr int CODE_BOX = 128 * CODE_ROW;                 // one 128-row code box
     static constexpr int STAGE_BYTES = A_BYTES + 2 * CODE_BOX;      // 32 KiB (FP8) / 24 KiB (NVFP4)
+};
+// Tile geometry: HALVES = 1, 128 activation rows per tile, double-buffered
+// accumulators; HALVES = 2, 256 rows as two 128-row halves that share each
+// converted B tile (each weight tile is converted once per 256 rows: groups of
+// 129..256 rows convert it once instead of twice), one accumulator pair of
+// 2 x 256 columns, eight epilogue warps.
+template <int WF, int HALVES>
+struct QGeo {
+    static constexpr int A_PART = HALVES * A_BYTES;                       // activation boxes of a stage
+    static constexpr int STAGE_BYTES = A_PART + 2 * QCfg<WF>::CODE_BOX;
+    static constexpr int STAGES = HALVES == 2 ? 3 : 4;
+    static constexpr int EPI_WARPS = 4 * HALVES;
+    static constexpr int CONV_W0 = 2 + EPI_WARPS;                         // first converter warp
+    static constexpr int THREADS = 64 + 32 * EPI_WARPS + 32 * Q_CONV_WARPS;
+    static constexpr int NUM_ACC = HALVES == 2 ? 1 : 2;
 };
 
 struct QParams {
@@ -842,7 +856,7 @@ struct QParams {
 };
 
 struct QCtl {
-    float scl[4][256];          // per epilogue warp: the weight-row scales of its tile's 256 B rows
+    float scl[8][256];          // per epilogue warp: the weight-row scales of its tile's 256 B rows
     unsigned long long full[Q_STAGES];
     unsigned long long empty[Q_STAGES];
     unsigned long long cfull[Q_CSLOTS];
@@ -893,19 +907,20 @@ __device__ __forceinline__ void epilogue_chunk_q(uint32_t tg, uint32_t tu, bool 
     }
 }
 
-template <int MODE, int WF>
-__global__ void __launch_bounds__(Q_THREADS, 1)
+template <int MODE, int WF, int HALVES>
+__global__ void __launch_bounds__(QGeo<WF, HALVES>::THREADS, 1)
 grouped_gemm_q_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const QParams qp) {
     using QC = QCfg<WF>;
+    using QG = QGeo<WF, HALVES>;
     constexpr bool FP4W = WF == kWeightNvfp4;
     constexpr int BN_OUT = (MODE == kGemmSwiGLU) ? 128 : 256;
-    constexpr int BMT = BM;                                  // 128 activation rows per tile
+    constexpr int BMT = BM * HALVES;                         // activation rows per tile
     const KParams& p = qp.k;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + ((1024u - (raw_u32 & 1023u)) & 1023u);
-    uint8_t* slots = smem + Q_STAGES * QC::STAGE_BYTES;     // converted B tiles
+    uint8_t* slots = smem + QG::STAGES * QG::STAGE_BYTES;   // converted B tiles
     QCtl* ctl = reinterpret_cast<QCtl*>(slots + Q_CSLOTS * Q_SLOT_BYTES);
     int* prefix = reinterpret_cast<int*>(ctl + 1);
     int* rstart = prefix + (p.groups + 1);
@@ -916,7 +931,7 @@ grouped_gemm_q_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
     const int ntn = (p.N + BN_OUT - 1) / BN_OUT;
 
     if (tid == 0) {
-        for (int s = 0; s < Q_STAGES; ++s) {
+        for (int s = 0; s < QG::STAGES; ++s) {
             mbar_init(smem_u32(&ctl->full[s]), 1);
             mbar_init(smem_u32(&ctl->empty[s]), 1 + Q_CONV_WARPS);      // MMA commit + converter warps
         }
@@ -926,7 +941,7 @@ grouped_gemm_q_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(smem_u32(&ctl->tfull[a]), 1);
-            mbar_init(smem_u32(&ctl->tempty[a]), 4);
+            mbar_init(smem_u32(&ctl->tempty[a]), QG::EPI_WARPS);
         }
         mbar_init(smem_u32(&ctl->drain), 1);
         ctl->abort = 0;
@@ -943,7 +958,7 @@ grouped_gemm_q_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
     pdl_trigger();
     // after a capacity overflow in the same layer call no payload moved: no tiles
     const bool skip = p.gated && p.hdr->cap_exceeded;
-    for (int g = tid; g < p.groups; g += Q_THREADS) {
+    for (int g = tid; g < p.groups; g += QG::THREADS) {
         if (skip) {
             rstart[g] = 0;
             rcount[g] = 0;
@@ -987,23 +1002,27 @@ grouped_gemm_q_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                 const Tile t = decode_tile<MODE == kGemmSwiGLU || MODE == kGemmReLU2>(tile, prefix, rstart, rcount, p,
                                                                                      ntn, BMT);
                 const int a_row = t.row0 + t.mt * BMT;
+                // the tile's second 128-row half, when it has rows
+                const bool second = HALVES == 2 && t.mt * BMT + BM < t.mrows;
+                const uint32_t bytes = (second ? 2u : 1u) * A_BYTES + 2u * QC::CODE_BOX;
                 const int b_lo = t.g * p.b_group_rows + t.nt * BN_OUT;
                 const int b_hi = (MODE == kGemmSwiGLU) ? b_lo + p.up_off : b_lo + 128;
                 for (int i = 0; i < nk; ++i) {
                     if (!mbar_wait_bounded(smem_u32(&ctl->empty[stage]), ph ^ 1u, abort)) { ok = false; break; }
                     const uint32_t full = smem_u32(&ctl->full[stage]);
-                    const uint32_t sa = smem_base + stage * QC::STAGE_BYTES;
-                    mbar_arrive_expect_tx(full, QC::STAGE_BYTES);
+                    const uint32_t sa = smem_base + stage * QG::STAGE_BYTES;
+                    mbar_arrive_expect_tx(full, bytes);
                     tma_load_2d(sa, &tmA, full, i * BK, a_row);
-                    tma_load_2d(sa + A_BYTES, &tmB, full, i * QC::CODE_ROW, b_lo);
-                    tma_load_2d(sa + A_BYTES + QC::CODE_BOX, &tmB, full, i * QC::CODE_ROW, b_hi);
+                    if (second) tma_load_2d(sa + A_BYTES, &tmA, full, i * BK, a_row + BM);
+                    tma_load_2d(sa + QG::A_PART, &tmB, full, i * QC::CODE_ROW, b_lo);
+                    tma_load_2d(sa + QG::A_PART + QC::CODE_BOX, &tmB, full, i * QC::CODE_ROW, b_hi);
                     ++armed;
-                    if (++stage == Q_STAGES) { stage = 0; ph ^= 1u; }
+                    if (++stage == QG::STAGES) { stage = 0; ph ^= 1u; }
                 }
             }
             if (!ok) {
                 // let the copies already issued land before the CTA exits
-                if (!wait_armed_stages(smem_u32(&ctl->full[0]), Q_STAGES, armed)) settle_delay();
+                if (!wait_armed_stages(smem_u32(&ctl->full[0]), QG::STAGES, armed)) settle_delay();
                 raise_status(p.hdr, MOE_ERR_TIMEOUT);
                 p.hdr->timeout_site = kSiteGemmProducer;
             }
@@ -1017,29 +1036,36 @@ grouped_gemm_q_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
                 const Tile t = decode_tile<MODE == kGemmSwiGLU || MODE == kGemmReLU2>(tile, prefix, rstart, rcount, p,
                                                                                      ntn, BMT);
-                const int rows0 = t.mrows - t.mt * BMT;
+                const int rows0 = t.mrows - t.mt * BMT;                   // rows from the first half on
+                const bool second = HALVES == 2 && rows0 > BM;
                 const uint32_t idesc = rows0 <= kTailRows ? IDESC64 : IDESC;
+                const uint32_t idesc1 = rows0 - BM <= kTailRows ? IDESC64 : IDESC;
                 if (!mbar_wait_bounded(smem_u32(&ctl->tempty[acc]), aph ^ 1u, abort)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t d0 = tmem_base + (uint32_t)(acc * BN_MMA);
+                const uint32_t d0 = tmem_base + (uint32_t)(acc * BN_MMA);   // half 1: the next 256 columns
                 for (int i = 0; i < nk; ++i) {
                     if (!mbar_wait_bounded(smem_u32(&ctl->full[stage]), ph, abort) ||
                         !mbar_wait_bounded(smem_u32(&ctl->cfull[cs]), cph, abort)) { ok = false; break; }
                     tc_fence_after();
-                    const uint64_t ad = sdesc_k_sw128(smem_base + stage * QC::STAGE_BYTES);
+                    const uint64_t ad = sdesc_k_sw128(smem_base + stage * QG::STAGE_BYTES);
+                    const uint64_t ad1 = sdesc_k_sw128(smem_base + stage * QG::STAGE_BYTES + A_BYTES);
                     const uint64_t bd = sdesc_k_sw128(slot_base + cs * Q_SLOT_BYTES);
 #pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk)
+                    for (int kk = 0; kk < BK / 16; ++kk) {
                         tc_mma_bf16(d0, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc,
                                     (i > 0 || kk > 0) ? 1u : 0u);
+                        if (second)   // the same converted B tile for the second 128 rows
+                            tc_mma_bf16(d0 + (uint32_t)BN_MMA, ad1 + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2),
+                                        idesc1, (i > 0 || kk > 0) ? 1u : 0u);
+                    }
                     tc_commit(smem_u32(&ctl->empty[stage]));
                     tc_commit(smem_u32(&ctl->cempty[cs]));
-                    if (++stage == Q_STAGES) { stage = 0; ph ^= 1u; }
+                    if (++stage == QG::STAGES) { stage = 0; ph ^= 1u; }
                     if (++cs == Q_CSLOTS) { cs = 0; cph ^= 1u; }
                 }
                 if (!ok) break;
                 tc_commit(smem_u32(&ctl->tfull[acc]));
-                if (++acc == 2) { acc = 0; aph ^= 1u; }
+                if (++acc == QG::NUM_ACC) { acc = 0; aph ^= 1u; }
             }
             tc_commit(smem_u32(&ctl->drain));
             volatile int never = 0;
@@ -1050,13 +1076,13 @@ grouped_gemm_q_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                 *abort = 1;
             }
         }
-    } else if (warp >= 6) {
-        // ---------------- converters (warps 6..13): codes -> swizzled BF16 B tile ----------------
+    } else if (warp >= QG::CONV_W0) {
+        // ---------------- converters (the last 8 warps): codes -> swizzled BF16 B tile ----------------
         // Thread ct takes, in four passes, weight row r = 64*pass + ct/4 of the
         // 256-row tile and its 16-element quarter qd = ct%4 of the 64-wide K step:
         // reads 16 codes (FP8: 16 bytes; NVFP4: 8 bytes and the block's scale),
         // writes 16 BF16 as two 16-byte chunks of the row at chunk (2qd + h) ^ (r%8).
-        const int ct = tid - 192;
+        const int ct = tid - 32 * QG::CONV_W0;
         const int qd = ct & 3;
         int stage = 0, cs = 0;
         uint32_t ph = 0, cph = 0;
@@ -1087,7 +1113,7 @@ grouped_gemm_q_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                 if (FP4W && i + 1 < nk) block_scales(b_lo, b_hi, i + 1, s_next);
                 if (!mbar_wait_bounded(smem_u32(&ctl->full[stage]), ph, abort) ||
                     !mbar_wait_bounded(smem_u32(&ctl->cempty[cs]), cph ^ 1u, abort)) { ok = false; break; }
-                const uint8_t* codes = smem + stage * QC::STAGE_BYTES + A_BYTES;
+                const uint8_t* codes = smem + stage * QG::STAGE_BYTES + QG::A_PART;
                 uint8_t* dst = slots + cs * Q_SLOT_BYTES;
 #pragma unroll
                 for (int pass = 0; pass < 4; ++pass) {
@@ -1128,13 +1154,15 @@ grouped_gemm_q_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                     mbar_arrive(smem_u32(&ctl->cfull[cs]));
                     mbar_arrive(smem_u32(&ctl->empty[stage]));
                 }
-                if (++stage == Q_STAGES) { stage = 0; ph ^= 1u; }
+                if (++stage == QG::STAGES) { stage = 0; ph ^= 1u; }
                 if (++cs == Q_CSLOTS) { cs = 0; cph ^= 1u; }
             }
         }
     } else {
-        // ---------------- epilogue (warps 2..5): scales, activation, BF16 stores ----------------
+        // ---------------- epilogue (warps 2..2+EPI_WARPS-1): scales, activation, BF16 stores ----------------
+        // warp w: TMEM lane quarter w % 4 (the warps a warp may read), half (w - 2) / 4
         const int q = warp & 3;
+        const int hf = (warp - 2) >> 2;
         const float undo = FP4W ? 256.f : 1.f;
         int acc = 0;
         uint32_t aph = 0;
@@ -1145,7 +1173,7 @@ grouped_gemm_q_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
             // the tile's 256 weight-row scales into this warp's shared slice while
             // the accumulator fills (SwiGLU: 128 gate rows, then the 128 up rows);
             // warp-local, so a warp that gives up leaves no other warp waiting
-            float* scl = ctl->scl[q];
+            float* scl = ctl->scl[warp - 2];
 #pragma unroll
             for (int j = lane; j < 256; j += 32) {
                 const int col = n0 + (MODE == kGemmSwiGLU ? (j & 127) : j);
@@ -1162,12 +1190,13 @@ grouped_gemm_q_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                 break;
             }
             tc_fence_after();
-            const int hrow0 = t.mt * BMT;
+            const int hrow0 = t.mt * BMT + hf * BM;                    // this half's first row
             const bool m64 = t.mrows - hrow0 <= kTailRows;
             const int r = m64 ? hrow0 + q * 16 + lane : hrow0 + q * 32 + lane;
-            const bool row_ok = (!m64 || lane < 16) && r < t.mrows;
+            // an empty second half had no MMAs: its (stale) columns are loaded, not stored
+            const bool row_ok = hrow0 < t.mrows && (!m64 || lane < 16) && r < t.mrows;
             __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(out_row<MODE>(p, t.row0 + (row_ok ? r : 0), t.g));
-            const uint32_t tbase = tmem_base + (uint32_t)(acc * BN_MMA) + ((uint32_t)(q * 32) << 16);
+            const uint32_t tbase = tmem_base + (uint32_t)((acc + hf) * BN_MMA) + ((uint32_t)(q * 32) << 16);
             if (MODE == kGemmSwiGLU) {
 #pragma unroll 1
                 for (int c = 0; c < 4; ++c)
@@ -1182,7 +1211,7 @@ grouped_gemm_q_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[acc]));
-            if (++acc == 2) { acc = 0; aph ^= 1u; }
+            if (++acc == QG::NUM_ACC) { acc = 0; aph ^= 1u; }
         }
     }
 
@@ -1301,28 +1330,29 @@ cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const KPar
     return e;
 }
 
-template <int MODE, int WF>
+template <int MODE, int WF, int HALVES>
 cudaError_t launch_q(const CUtensorMap& ma, const CUtensorMap& mb, const QParams& qp, size_t smem,
                      cudaStream_t st) {
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(grouped_gemm_q_kernel<MODE, WF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        MAX_DYN_SMEM);
+        attr_err = cudaFuncSetAttribute(grouped_gemm_q_kernel<MODE, WF, HALVES>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, MAX_DYN_SMEM);
     });
     if (attr_err != cudaSuccess) {
         set_error("cudaFuncSetAttribute(max dynamic smem %d): %s", MAX_DYN_SMEM, cudaGetErrorString(attr_err));
         return attr_err;
     }
-    const cudaError_t e = launch_kernel(grouped_gemm_q_kernel<MODE, WF>, dim3((unsigned)device_sm_count()),
-                                        dim3(Q_THREADS), smem, st, 1, kUsePdl, ma, mb, qp);
+    const cudaError_t e = launch_kernel(grouped_gemm_q_kernel<MODE, WF, HALVES>, dim3((unsigned)device_sm_count()),
+                                        dim3(QGeo<WF, HALVES>::THREADS), smem, st, 1, kUsePdl, ma, mb, qp);
     if (e != cudaSuccess) set_error("quantized grouped GEMM launch (smem %zu): %s", smem, cudaGetErrorString(e));
     return e;
 }
 
-template <int WF>
+template <int WF, int HALVES>
 size_t q_smem_bytes(int groups) {
-    return 1024 + (size_t)Q_STAGES * QCfg<WF>::STAGE_BYTES + (size_t)Q_CSLOTS * Q_SLOT_BYTES + sizeof(QCtl) +
+    return 1024 + (size_t)QGeo<WF, HALVES>::STAGES * QGeo<WF, HALVES>::STAGE_BYTES + (size_t)Q_CSLOTS * Q_SLOT_BYTES +
+           sizeof(QCtl) +
            3 * (size_t)(groups + 1) * 4;
 }
 
@@ -1456,7 +1486,13 @@ moe_status launch_grouped_gemm(const GemmProblem& g, WsHeader* hdr, cudaStream_t
             set_error("grouped GEMM: quantized weights need a scale per weight row");
             return MOE_ERR_UNSUPPORTED;
         }
-        const size_t smem = fp4 ? q_smem_bytes<kWeightNvfp4>(g.groups) : q_smem_bytes<kWeightFp8E4M3>(g.groups);
+        // NVFP4 groups of more than 96 rows on average: 256-row tiles (its converter
+        // is the dearer one, and groups of 129..256 rows then convert each weight
+        // tile once instead of twice)
+        const long long avg_rows = g.offsets ? g.a_rows / g.groups : g.rows_all;
+        const bool two = fp4 && avg_rows > 96;
+        const size_t smem = fp4 ? (two ? q_smem_bytes<kWeightNvfp4, 2>(g.groups) : q_smem_bytes<kWeightNvfp4, 1>(g.groups))
+                                : q_smem_bytes<kWeightFp8E4M3, 1>(g.groups);
         if (smem > (size_t)MAX_DYN_SMEM) {
             set_error("quantized grouped GEMM needs %zu bytes of shared memory", smem);
             return MOE_ERR_UNSUPPORTED;
@@ -1490,17 +1526,23 @@ moe_status launch_grouped_gemm(const GemmProblem& g, WsHeader* hdr, cudaStream_t
         qp.bscale_stride = g.bscale_stride;
         qp.b_rows = (int)g.b_rows;
         cudaError_t e;
-        if (fp4) {
+        if (fp4 && two) {
             switch (g.mode) {
-                case kGemmSwiGLU: e = launch_q<kGemmSwiGLU, kWeightNvfp4>(ma, mb, qp, smem, st); break;
-                case kGemmReLU2: e = launch_q<kGemmReLU2, kWeightNvfp4>(ma, mb, qp, smem, st); break;
-                default: e = launch_q<kGemmPlain, kWeightNvfp4>(ma, mb, qp, smem, st); break;
+                case kGemmSwiGLU: e = launch_q<kGemmSwiGLU, kWeightNvfp4, 2>(ma, mb, qp, smem, st); break;
+                case kGemmReLU2: e = launch_q<kGemmReLU2, kWeightNvfp4, 2>(ma, mb, qp, smem, st); break;
+                default: e = launch_q<kGemmPlain, kWeightNvfp4, 2>(ma, mb, qp, smem, st); break;
+            }
+        } else if (fp4) {
+            switch (g.mode) {
+                case kGemmSwiGLU: e = launch_q<kGemmSwiGLU, kWeightNvfp4, 1>(ma, mb, qp, smem, st); break;
+                case kGemmReLU2: e = launch_q<kGemmReLU2, kWeightNvfp4, 1>(ma, mb, qp, smem, st); break;
+                default: e = launch_q<kGemmPlain, kWeightNvfp4, 1>(ma, mb, qp, smem, st); break;
             }
         } else {
             switch (g.mode) {
-                case kGemmSwiGLU: e = launch_q<kGemmSwiGLU, kWeightFp8E4M3>(ma, mb, qp, smem, st); break;
-                case kGemmReLU2: e = launch_q<kGemmReLU2, kWeightFp8E4M3>(ma, mb, qp, smem, st); break;
-                default: e = launch_q<kGemmPlain, kWeightFp8E4M3>(ma, mb, qp, smem, st); break;
+                case kGemmSwiGLU: e = launch_q<kGemmSwiGLU, kWeightFp8E4M3, 1>(ma, mb, qp, smem, st); break;
+                case kGemmReLU2: e = launch_q<kGemmReLU2, kWeightFp8E4M3, 1>(ma, mb, qp, smem, st); break;
+                default: e = launch_q<kGemmPlain, kWeightFp8E4M3, 1>(ma, mb, qp, smem, st); break;
             }
         }
         return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
