@@ -218,24 +218,23 @@ decode_ffn_kernel(const __grid_constant__ CUtensorMap tmX,     // x_perm: 16-row
     const bool skip = __ldcg(&p.hdr->cap_exceeded) != 0;   // over capacity: no payload moved
 
     // ---- the non-empty experts (block-wide compaction of the bounds) ---------
+    // each thread's experts g0 .. g0+per-1 (per <= 6: at most 1024 experts over
+    // 192 threads): their per+1 bounds read once, together, through L2
     {
+        constexpr int kMaxPer = 8;
         const int per = (p.E + F_THREADS - 1) / F_THREADS;
         const int g0 = tid * per;
-        auto bounds = [&](int g, int& lo, int& hi) {
-            lo = __ldcg(p.offsets + g);
-            hi = __ldcg(p.offsets + g + 1);
-            lo = lo < 0 ? 0 : (lo > p.R ? p.R : lo);
-            hi = hi < lo ? lo : (hi > p.R ? p.R : hi);
-        };
-        int cnt = 0;
-        for (int i = 0; i < per && !skip; ++i) {
+        int bnd[kMaxPer + 1];
+#pragma unroll
+        for (int i = 0; i <= kMaxPer; ++i) {
             const int g = g0 + i;
-            if (g < p.E) {
-                int lo, hi;
-                bounds(g, lo, hi);
-                cnt += hi > lo;
-            }
+            const int v = (!skip && i <= per && g <= p.E) ? __ldcg(p.offsets + g) : 0;
+            bnd[i] = v < 0 ? 0 : (v > p.R ? p.R : v);
         }
+        int cnt = 0;
+#pragma unroll
+        for (int i = 0; i < kMaxPer; ++i)
+            if (i < per && g0 + i < p.E) cnt += bnd[i + 1] > bnd[i];
         int inc = cnt;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
@@ -247,12 +246,14 @@ decode_ffn_kernel(const __grid_constant__ CUtensorMap tmX,     // x_perm: 16-row
         int kk = inc - cnt;
         for (int w = 0; w < warp; ++w) kk += ctl->wsum[w];
         if (tid == F_THREADS - 1) ctl->ng = kk + cnt;
-        for (int i = 0; i < per && !skip; ++i) {
+#pragma unroll
+        for (int i = 0; i < kMaxPer; ++i) {
             const int g = g0 + i;
-            if (g < p.E) {
-                int lo, hi;
-                bounds(g, lo, hi);
-                if (hi > lo) { gid[kk] = g; gst[kk] = lo; gcnt[kk] = hi - lo; ++kk; }
+            if (i < per && g < p.E && bnd[i + 1] > bnd[i]) {
+                gid[kk] = g;
+                gst[kk] = bnd[i];
+                gcnt[kk] = bnd[i + 1] - bnd[i];
+                ++kk;
             }
         }
     }

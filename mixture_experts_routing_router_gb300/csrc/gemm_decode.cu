@@ -126,12 +126,6 @@ struct DCtl {
     int wsum[DTHREADS_FP8 / 32];
 };
 
-__device__ __forceinline__ void clamped_bounds(const DParams& p, int g, int& lo, int& hi) {
-    lo = __ldcg(p.offsets + g);            // from L2: may be read before the programmatic wait
-    hi = __ldcg(p.offsets + g + 1);
-    lo = lo < 0 ? 0 : (lo > p.a_rows ? p.a_rows : lo);
-    hi = hi < lo ? lo : (hi > p.a_rows ? p.a_rows : hi);
-}
 
 // D[tmem] (+)= A[tmem] * B[smem]^T: A (M x K, BF16) in TMEM, one row per lane
 // and two consecutive K elements per 32-bit column (lower K in the low half).
@@ -236,17 +230,23 @@ decode_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
     if (skip) {
         if (tid == 0) ctl->ng = 0;
     } else if (p.offsets) {
+        // each thread's groups g0 .. g0+per-1 (per <= 6: at most 1024 groups over
+        // at least 192 threads): their per+1 bounds are read once, together, and
+        // kept in registers for both passes
+        constexpr int kMaxPer = 8;
         const int per = (p.groups + NTH - 1) / NTH;
         const int g0 = tid * per;
-        int cnt = 0;
-        for (int i = 0; i < per; ++i) {
+        int bnd[kMaxPer + 1];
+#pragma unroll
+        for (int i = 0; i <= kMaxPer; ++i) {
             const int g = g0 + i;
-            if (g < p.groups) {
-                int lo, hi;
-                clamped_bounds(p, g, lo, hi);
-                cnt += hi > lo;
-            }
+            int v = (i <= per && g <= p.groups) ? __ldcg(p.offsets + g) : 0;   // from L2: before the wait too
+            bnd[i] = v < 0 ? 0 : (v > p.a_rows ? p.a_rows : v);
         }
+        int cnt = 0;
+#pragma unroll
+        for (int i = 0; i < kMaxPer; ++i)
+            if (i < per && g0 + i < p.groups) cnt += bnd[i + 1] > bnd[i];
         int inc = cnt;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
@@ -258,12 +258,14 @@ decode_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
         int k = inc - cnt;
         for (int w = 0; w < warp; ++w) k += ctl->wsum[w];
         if (tid == NTH - 1) ctl->ng = k + cnt;
-        for (int i = 0; i < per; ++i) {
+#pragma unroll
+        for (int i = 0; i < kMaxPer; ++i) {
             const int g = g0 + i;
-            if (g < p.groups) {
-                int lo, hi;
-                clamped_bounds(p, g, lo, hi);
-                if (hi > lo) { gid[k] = g; gst[k] = lo; gcnt[k] = hi - lo; ++k; }
+            if (i < per && g < p.groups && bnd[i + 1] > bnd[i]) {
+                gid[k] = g;
+                gst[k] = bnd[i];
+                gcnt[k] = bnd[i + 1] - bnd[i];
+                ++k;
             }
         }
     } else {
@@ -667,6 +669,10 @@ cudaError_t launch_d(const CUtensorMap& mx, const CUtensorMap& mw, const CUtenso
 }  // namespace
 
 moe_status launch_decode_gemm(const GemmProblem& g, int nb, WsHeader* hdr, cudaStream_t st) {
+    if (g.groups > 192 * 8) {       // the kernel's group list: at most 8 groups per thread
+        set_error("decode GEMM: %d groups", g.groups);
+        return MOE_ERR_UNSUPPORTED;
+    }
     if (nb < 16 || nb > kDecodeRows || nb % 16 != 0) {
         set_error("decode GEMM: %d rows per chunk is not a multiple of 16 in [16, %d]", nb, kDecodeRows);
         return MOE_ERR_INTERNAL;
