@@ -264,6 +264,38 @@ def test_expert_ffn_buckets_above_the_row_bound(act):
     assert_close(bits(o["y_perm"]), y_ref, "chunked y_perm")
 
 
+# one full 256-row tile plus a tail of every padded size class per group (16
+# to 256 rows, 8 to 128 per CTA of the pair), and exact multiples of 256
+PAIR_TAILS = [0, 1, 8, 9, 16, 17, 31, 32, 33, 63, 64, 65, 127, 128, 129, 200, 255]
+
+
+@pytest.mark.parametrize("act,hidden", [(synth.ACT_SWIGLU, 320), (synth.ACT_RELU2, 576)])
+def test_expert_ffn_pair_kernel_partial_tiles(act, hidden):
+    """Caller-made offsets whose groups (two of them empty) hold 256 + t rows
+    for every tail size t above: the CTA-pair kernel computes each group's
+    full tile, then its tail with the operands swapped (weights on M, the
+    tail's rows padded to 16 on N); K of 5 and 9 chunks of 64, and the down
+    projection's 3."""
+    sizes = [256 + t for t in PAIR_TAILS]
+    sizes[3:3] = [0]
+    sizes[10:10] = [0]
+    E, R = len(sizes), sum(sizes)
+    wl = synth.Workload("pair_tails", R, hidden, E, 1, 192, act=act)
+    g = inputs(wl, unit_scale=True, seed=13)
+    x_perm = synth.normal((R, hidden), 1.0, 13, "x_perm", dev())
+    offsets = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    h_ref, y_ref, _, _ = oracle.expert_ffn(bits(x_perm), offsets, bits(g["w13"]), bits(g["w2"]), wl.act)
+    shape = N.shape_of(wl)
+    ws = N.workspace(shape, dev())
+    o = alloc_stage_outputs(wl)
+    N.moe_expert_up(shape, x_perm, i32_dev(offsets), g["w13"], g["x"], None, o["h"], ws)
+    assert N.moe_status_read(ws) == N.MOE_OK
+    assert_close(bits(o["h"]), h_ref, "pair tails h")
+    N.moe_expert_down(shape, to_bf16_dev(h_ref), i32_dev(offsets), g["w2"], None, o["y_perm"], None, ws)
+    assert N.moe_status_read(ws) == N.MOE_OK
+    assert_close(bits(o["y_perm"]), y_ref, "pair tails y_perm")
+
+
 # ---------------------------------------------------------------------------
 # combine
 # ---------------------------------------------------------------------------
