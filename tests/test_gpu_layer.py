@@ -219,6 +219,11 @@ FUSED = {
     "swiglu_t16": synth.Workload("swiglu_t16", 16, 512, 8, 2, 384),              # a partial last down stage
     "swiglu_t2_e64": synth.Workload("swiglu_t2_e64", 2, 256, 64, 8, 192),        # ragged 128-row blocks
     "relu2_t5_h320": synth.Workload("relu2_t5_h320", 5, 320, 12, 3, 64, act=synth.ACT_RELU2),
+    # the ABI's largest expert count and top-k: up to 512 non-empty experts in the
+    # group list, six bucket bounds per thread
+    "max_e_t16": synth.Workload("max_e_t16", 16, 128, 1024, 32, 64),
+    # a DeepSeek-sized hidden dimension: 112 K chunks, one-chunk-wide down stages
+    "relu2_t16_h7168": synth.Workload("relu2_t16_h7168", 16, 7168, 16, 2, 256, act=synth.ACT_RELU2),
 }
 
 
