@@ -829,7 +829,9 @@ template <int WF>
 struct QCfg {
     static constexpr int CODE_ROW = WF == kWeightNvfp4 ? 32 : 64;   // code bytes per weight row per K step
     static constexpr int CODE_BOX = 128 * CODE_ROW;                 // one 128-row code box
-    static constexpr int STAGE_BYTES = A_BYTES + 2 * CODE_BOX;      // 32 KiB (FP8) / 24 KiB (NVFP4)
+    // NVFP4: 16 bytes of block scales per weight row (the 16-byte group holding this
+    // K step's four), one box per 128 rows
+    static constexpr int SCALE_BOX = WF == kWeightNvfp4 ? 128 * 16 : 0;
 };
 // Tile geometry: HALVES = 1, 128 activation rows per tile, double-buffered
 // accumulators; HALVES = 2, 256 rows as two 128-row halves that share each
@@ -839,7 +841,8 @@ struct QCfg {
 template <int WF, int HALVES>
 struct QGeo {
     static constexpr int A_PART = HALVES * A_BYTES;                       // activation boxes of a stage
-    static constexpr int STAGE_BYTES = A_PART + 2 * QCfg<WF>::CODE_BOX;
+    static constexpr int S_PART = A_PART + 2 * QCfg<WF>::CODE_BOX;         // NVFP4 block-scale boxes
+    static constexpr int STAGE_BYTES = S_PART + 2 * QCfg<WF>::SCALE_BOX;
     static constexpr int STAGES = HALVES == 2 ? 3 : 4;
     static constexpr int EPI_WARPS = 4 * HALVES;
     static constexpr int CONV_W0 = 2 + EPI_WARPS;                         // first converter warp
@@ -850,9 +853,6 @@ struct QGeo {
 struct QParams {
     KParams k;
     const float* wscale;        // FP32 scale per weight row
-    const uint8_t* bscale;      // NVFP4: E4M3 block scales, bscale_stride bytes per weight row
-    long long bscale_stride;
-    int b_rows;                 // weight rows in all (the block-scale reads stay below it)
 };
 
 struct QCtl {
@@ -910,7 +910,7 @@ __device__ __forceinline__ void epilogue_chunk_q(uint32_t tg, uint32_t tu, bool 
 template <int MODE, int WF, int HALVES>
 __global__ void __launch_bounds__(QGeo<WF, HALVES>::THREADS, 1)
 grouped_gemm_q_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                      const QParams qp) {
+                      const __grid_constant__ CUtensorMap tmS, const QParams qp) {
     using QC = QCfg<WF>;
     using QG = QGeo<WF, HALVES>;
     constexpr bool FP4W = WF == kWeightNvfp4;
@@ -949,6 +949,7 @@ grouped_gemm_q_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
         fence_proxy_async_smem();
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
+        if (FP4W) tma_prefetch_desc(&tmS);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(&ctl->tmem_base), TMEM_COLS);
@@ -1004,7 +1005,7 @@ grouped_gemm_q_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                 const int a_row = t.row0 + t.mt * BMT;
                 // the tile's second 128-row half, when it has rows
                 const bool second = HALVES == 2 && t.mt * BMT + BM < t.mrows;
-                const uint32_t bytes = (second ? 2u : 1u) * A_BYTES + 2u * QC::CODE_BOX;
+                const uint32_t bytes = (second ? 2u : 1u) * A_BYTES + 2u * QC::CODE_BOX + 2u * QC::SCALE_BOX;
                 const int b_lo = t.g * p.b_group_rows + t.nt * BN_OUT;
                 const int b_hi = (MODE == kGemmSwiGLU) ? b_lo + p.up_off : b_lo + 128;
                 for (int i = 0; i < nk; ++i) {
@@ -1016,6 +1017,10 @@ grouped_gemm_q_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                     if (second) tma_load_2d(sa + A_BYTES, &tmA, full, i * BK, a_row + BM);
                     tma_load_2d(sa + QG::A_PART, &tmB, full, i * QC::CODE_ROW, b_lo);
                     tma_load_2d(sa + QG::A_PART + QC::CODE_BOX, &tmB, full, i * QC::CODE_ROW, b_hi);
+                    if (FP4W) {     // the 16-byte group of block scales holding step i's four
+                        tma_load_2d(sa + QG::S_PART, &tmS, full, (i * (BK / 16)) & ~15, b_lo);
+                        tma_load_2d(sa + QG::S_PART + QC::SCALE_BOX, &tmS, full, (i * (BK / 16)) & ~15, b_hi);
+                    }
                     ++armed;
                     if (++stage == QG::STAGES) { stage = 0; ph ^= 1u; }
                 }
@@ -1087,33 +1092,23 @@ grouped_gemm_q_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
         int stage = 0, cs = 0;
         uint32_t ph = 0, cph = 0;
         bool ok = true;
-        // NVFP4: this quarter's block scale of each pass, for 64-wide step i
-        // (read from global memory one step ahead, never past K or the weight rows)
-        auto block_scales = [&](int b_lo, int b_hi, int i, uint32_t (&s4)[4]) {
-#pragma unroll
-            for (int pass = 0; pass < 4; ++pass) {
-                const int r = pass * 64 + (ct >> 2);
-                const int wrow = ((r >> 7) ? b_hi : b_lo) + (r & 127);
-                const int k0 = i * BK + qd * 16;
-                s4[pass] = (k0 < p.K && wrow < qp.b_rows)
-                               ? (uint32_t)__ldg(qp.bscale + (long long)wrow * qp.bscale_stride + (k0 >> 4)) : 0x100u;
-            }
-        };
         for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-            const Tile t = decode_tile<MODE == kGemmSwiGLU || MODE == kGemmReLU2>(tile, prefix, rstart, rcount, p,
-                                                                                 ntn, BMT);
-            const int b_lo = t.g * p.b_group_rows + t.nt * BN_OUT;
-            const int b_hi = (MODE == kGemmSwiGLU) ? b_lo + p.up_off : b_lo + 128;
-            uint32_t s_next[4] = {0u, 0u, 0u, 0u};
-            if (FP4W) block_scales(b_lo, b_hi, 0, s_next);
             for (int i = 0; i < nk; ++i) {
-                uint32_t s_cur[4];
-#pragma unroll
-                for (int pass = 0; pass < 4; ++pass) s_cur[pass] = s_next[pass];
-                if (FP4W && i + 1 < nk) block_scales(b_lo, b_hi, i + 1, s_next);
                 if (!mbar_wait_bounded(smem_u32(&ctl->full[stage]), ph, abort) ||
                     !mbar_wait_bounded(smem_u32(&ctl->cempty[cs]), cph ^ 1u, abort)) { ok = false; break; }
                 const uint8_t* codes = smem + stage * QG::STAGE_BYTES + QG::A_PART;
+                // NVFP4: this quarter's block scale of each pass, from the stage (0x100
+                // marks a block past K: zeros; rows past the weights arrive as scale 0)
+                uint32_t s_cur[4] = {0u, 0u, 0u, 0u};
+                if (FP4W) {
+                    const uint8_t* sc = smem + stage * QG::STAGE_BYTES + QG::S_PART + (i & 3) * 4 + qd;
+                    const bool in_k = i * BK + qd * 16 < p.K;
+#pragma unroll
+                    for (int pass = 0; pass < 4; ++pass) {
+                        const int r = pass * 64 + (ct >> 2);
+                        s_cur[pass] = in_k ? (uint32_t)sc[(r >> 7) * QC::SCALE_BOX + (r & 127) * 16] : 0x100u;
+                    }
+                }
                 uint8_t* dst = slots + cs * Q_SLOT_BYTES;
 #pragma unroll
                 for (int pass = 0; pass < 4; ++pass) {
@@ -1122,7 +1117,7 @@ grouped_gemm_q_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                     uint32_t v[8];
                     if constexpr (FP4W) {
                         // this quarter is one 16-element block: its E4M3 scale, at 2^-8
-                        // (0x100 marks a block past K or the weight rows: zeros)
+                        // (0x100 marks a block past K: zeros)
                         uint32_t m = 0u;
                         if (s_cur[pass] != 0x100u) {
                             constexpr uint32_t kTwo118 = 0x7A807A80u;       // (2^118, 2^118) in BF16
@@ -1331,8 +1326,8 @@ cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const KPar
 }
 
 template <int MODE, int WF, int HALVES>
-cudaError_t launch_q(const CUtensorMap& ma, const CUtensorMap& mb, const QParams& qp, size_t smem,
-                     cudaStream_t st) {
+cudaError_t launch_q(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& ms, const QParams& qp,
+                     size_t smem, cudaStream_t st) {
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
@@ -1344,7 +1339,7 @@ cudaError_t launch_q(const CUtensorMap& ma, const CUtensorMap& mb, const QParams
         return attr_err;
     }
     const cudaError_t e = launch_kernel(grouped_gemm_q_kernel<MODE, WF, HALVES>, dim3((unsigned)device_sm_count()),
-                                        dim3(QGeo<WF, HALVES>::THREADS), smem, st, 1, kUsePdl, ma, mb, qp);
+                                        dim3(QGeo<WF, HALVES>::THREADS), smem, st, 1, kUsePdl, ma, mb, ms, qp);
     if (e != cudaSuccess) set_error("quantized grouped GEMM launch (smem %zu): %s", smem, cudaGetErrorString(e));
     return e;
 }
@@ -1478,8 +1473,8 @@ moe_status launch_grouped_gemm(const GemmProblem& g, WsHeader* hdr, cudaStream_t
             return launch_decode_gemm(g, nb, hdr, st);
         }
         const bool fp4 = g.wfmt == kWeightNvfp4;
-        if (fp4 && (!g.bscale || g.K % 32 != 0 || g.bscale_stride * 16 < g.K)) {
-            set_error("grouped GEMM: NVFP4 weights need K %% 32 == 0 and block-scale rows covering K");
+        if (fp4 && (!g.bscale || g.K % 32 != 0 || g.bscale_stride % 16 != 0 || g.bscale_stride * 16 < g.K)) {
+            set_error("grouped GEMM: NVFP4 weights need K %% 32 == 0 and 16-byte block-scale rows covering K");
             return MOE_ERR_UNSUPPORTED;
         }
         if (!g.wscale) {
@@ -1490,7 +1485,7 @@ moe_status launch_grouped_gemm(const GemmProblem& g, WsHeader* hdr, cudaStream_t
         // is the dearer one, and groups of 129..256 rows then convert each weight
         // tile once instead of twice)
         const long long avg_rows = g.offsets ? g.a_rows / g.groups : g.rows_all;
-        const bool two = fp4 && avg_rows > 96;
+        const bool two = fp4 && avg_rows > 96 && q_smem_bytes<kWeightNvfp4, 2>(g.groups) <= (size_t)MAX_DYN_SMEM;
         const size_t smem = fp4 ? (two ? q_smem_bytes<kWeightNvfp4, 2>(g.groups) : q_smem_bytes<kWeightNvfp4, 1>(g.groups))
                                 : q_smem_bytes<kWeightFp8E4M3, 1>(g.groups);
         if (smem > (size_t)MAX_DYN_SMEM) {
@@ -1503,6 +1498,10 @@ moe_status launch_grouped_gemm(const GemmProblem& g, WsHeader* hdr, cudaStream_t
         if (!make_tensor_map_u8_rows(&mb, g.b, g.b_rows, code_cols, code_cols,
                                      (unsigned)(fp4 ? QCfg<kWeightNvfp4>::CODE_ROW : QCfg<kWeightFp8E4M3>::CODE_ROW),
                                      128u))
+            return MOE_ERR_CUDA;
+        // NVFP4 block scales: 16-byte groups of 128 weight rows
+        CUtensorMap ms = mb;
+        if (fp4 && !make_tensor_map_u8_rows(&ms, g.bscale, g.b_rows, g.bscale_stride, g.bscale_stride, 16u, 128u))
             return MOE_ERR_CUDA;
         QParams qp;
         qp.k.offsets = g.offsets;
@@ -1522,27 +1521,24 @@ moe_status launch_grouped_gemm(const GemmProblem& g, WsHeader* hdr, cudaStream_t
         qp.k.hdr = hdr;
         qp.k.gated = g.gated;
         qp.wscale = g.wscale;
-        qp.bscale = g.bscale;
-        qp.bscale_stride = g.bscale_stride;
-        qp.b_rows = (int)g.b_rows;
         cudaError_t e;
         if (fp4 && two) {
             switch (g.mode) {
-                case kGemmSwiGLU: e = launch_q<kGemmSwiGLU, kWeightNvfp4, 2>(ma, mb, qp, smem, st); break;
-                case kGemmReLU2: e = launch_q<kGemmReLU2, kWeightNvfp4, 2>(ma, mb, qp, smem, st); break;
-                default: e = launch_q<kGemmPlain, kWeightNvfp4, 2>(ma, mb, qp, smem, st); break;
+                case kGemmSwiGLU: e = launch_q<kGemmSwiGLU, kWeightNvfp4, 2>(ma, mb, ms, qp, smem, st); break;
+                case kGemmReLU2: e = launch_q<kGemmReLU2, kWeightNvfp4, 2>(ma, mb, ms, qp, smem, st); break;
+                default: e = launch_q<kGemmPlain, kWeightNvfp4, 2>(ma, mb, ms, qp, smem, st); break;
             }
         } else if (fp4) {
             switch (g.mode) {
-                case kGemmSwiGLU: e = launch_q<kGemmSwiGLU, kWeightNvfp4, 1>(ma, mb, qp, smem, st); break;
-                case kGemmReLU2: e = launch_q<kGemmReLU2, kWeightNvfp4, 1>(ma, mb, qp, smem, st); break;
-                default: e = launch_q<kGemmPlain, kWeightNvfp4, 1>(ma, mb, qp, smem, st); break;
+                case kGemmSwiGLU: e = launch_q<kGemmSwiGLU, kWeightNvfp4, 1>(ma, mb, ms, qp, smem, st); break;
+                case kGemmReLU2: e = launch_q<kGemmReLU2, kWeightNvfp4, 1>(ma, mb, ms, qp, smem, st); break;
+                default: e = launch_q<kGemmPlain, kWeightNvfp4, 1>(ma, mb, ms, qp, smem, st); break;
             }
         } else {
             switch (g.mode) {
-                case kGemmSwiGLU: e = launch_q<kGemmSwiGLU, kWeightFp8E4M3, 1>(ma, mb, qp, smem, st); break;
-                case kGemmReLU2: e = launch_q<kGemmReLU2, kWeightFp8E4M3, 1>(ma, mb, qp, smem, st); break;
-                default: e = launch_q<kGemmPlain, kWeightFp8E4M3, 1>(ma, mb, qp, smem, st); break;
+                case kGemmSwiGLU: e = launch_q<kGemmSwiGLU, kWeightFp8E4M3, 1>(ma, mb, ms, qp, smem, st); break;
+                case kGemmReLU2: e = launch_q<kGemmReLU2, kWeightFp8E4M3, 1>(ma, mb, ms, qp, smem, st); break;
+                default: e = launch_q<kGemmPlain, kWeightFp8E4M3, 1>(ma, mb, ms, qp, smem, st); break;
             }
         }
         return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
