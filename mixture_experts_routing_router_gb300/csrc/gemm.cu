@@ -833,21 +833,16 @@ struct QCfg {
     // K step's four), one box per 128 rows
     static constexpr int SCALE_BOX = WF == kWeightNvfp4 ? 128 * 16 : 0;
 };
-// Tile geometry: HALVES = 1, 128 activation rows per tile, double-buffered
-// accumulators; HALVES = 2, 256 rows as two 128-row halves that share each
-// converted B tile (each weight tile is converted once per 256 rows: groups of
-// 129..256 rows convert it once instead of twice), one accumulator pair of
-// 2 x 256 columns, eight epilogue warps.
-template <int WF, int HALVES>
+// Tile geometry: 128 activation rows per tile, four TMA stages, two converted B
+// tiles, double-buffered accumulators; warps: producer, MMA, four epilogue
+// warps, eight converter warps.
+template <int WF>
 struct QGeo {
-    static constexpr int A_PART = HALVES * A_BYTES;                       // activation boxes of a stage
-    static constexpr int S_PART = A_PART + 2 * QCfg<WF>::CODE_BOX;         // NVFP4 block-scale boxes
+    static constexpr int S_PART = A_BYTES + 2 * QCfg<WF>::CODE_BOX;        // NVFP4 block-scale boxes
     static constexpr int STAGE_BYTES = S_PART + 2 * QCfg<WF>::SCALE_BOX;
-    static constexpr int STAGES = HALVES == 2 ? 3 : 4;
-    static constexpr int EPI_WARPS = 4 * HALVES;
-    static constexpr int CONV_W0 = 2 + EPI_WARPS;                         // first converter warp
-    static constexpr int THREADS = 64 + 32 * EPI_WARPS + 32 * Q_CONV_WARPS;
-    static constexpr int NUM_ACC = HALVES == 2 ? 1 : 2;
+    static constexpr int STAGES = 4;
+    static constexpr int CONV_W0 = 6;                                     // first converter warp
+    static constexpr int THREADS = 32 * CONV_W0 + 32 * Q_CONV_WARPS;
 };
 
 struct QParams {
@@ -856,7 +851,7 @@ struct QParams {
 };
 
 struct QCtl {
-    float scl[8][256];          // per epilogue warp: the weight-row scales of its tile's 256 B rows
+    float scl[4][256];          // per epilogue warp: the weight-row scales of its tile's 256 B rows
     unsigned long long full[Q_STAGES];
     unsigned long long empty[Q_STAGES];
     unsigned long long cfull[Q_CSLOTS];
@@ -907,15 +902,14 @@ __device__ __forceinline__ void epilogue_chunk_q(uint32_t tg, uint32_t tu, bool 
     }
 }
 
-template <int MODE, int WF, int HALVES>
-__global__ void __launch_bounds__(QGeo<WF, HALVES>::THREADS, 1)
+template <int MODE, int WF>
+__global__ void __launch_bounds__(QGeo<WF>::THREADS, 1)
 grouped_gemm_q_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const __grid_constant__ CUtensorMap tmS, const QParams qp) {
     using QC = QCfg<WF>;
-    using QG = QGeo<WF, HALVES>;
+    using QG = QGeo<WF>;
     constexpr bool FP4W = WF == kWeightNvfp4;
     constexpr int BN_OUT = (MODE == kGemmSwiGLU) ? 128 : 256;
-    constexpr int BMT = BM * HALVES;                         // activation rows per tile
     const KParams& p = qp.k;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -941,7 +935,7 @@ grouped_gemm_q_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(smem_u32(&ctl->tfull[a]), 1);
-            mbar_init(smem_u32(&ctl->tempty[a]), QG::EPI_WARPS);
+            mbar_init(smem_u32(&ctl->tempty[a]), 4);                 // the 4 epilogue warps
         }
         mbar_init(smem_u32(&ctl->drain), 1);
         ctl->abort = 0;
@@ -979,7 +973,7 @@ grouped_gemm_q_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
         int run = 0;
         for (int g = 0; g < p.groups; ++g) {
             prefix[g] = run;
-            run += ((rcount[g] + BMT - 1) / BMT) * ntn;
+            run += ((rcount[g] + BM - 1) / BM) * ntn;
         }
         prefix[p.groups] = run;
         ctl->total_tiles = run;
@@ -1001,11 +995,9 @@ grouped_gemm_q_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
             long long armed = 0;
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
                 const Tile t = decode_tile<MODE == kGemmSwiGLU || MODE == kGemmReLU2>(tile, prefix, rstart, rcount, p,
-                                                                                     ntn, BMT);
-                const int a_row = t.row0 + t.mt * BMT;
-                // the tile's second 128-row half, when it has rows
-                const bool second = HALVES == 2 && t.mt * BMT + BM < t.mrows;
-                const uint32_t bytes = (second ? 2u : 1u) * A_BYTES + 2u * QC::CODE_BOX + 2u * QC::SCALE_BOX;
+                                                                                     ntn, BM);
+                const int a_row = t.row0 + t.mt * BM;
+                const uint32_t bytes = (uint32_t)QG::STAGE_BYTES;
                 const int b_lo = t.g * p.b_group_rows + t.nt * BN_OUT;
                 const int b_hi = (MODE == kGemmSwiGLU) ? b_lo + p.up_off : b_lo + 128;
                 for (int i = 0; i < nk; ++i) {
@@ -1014,9 +1006,8 @@ grouped_gemm_q_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                     const uint32_t sa = smem_base + stage * QG::STAGE_BYTES;
                     mbar_arrive_expect_tx(full, bytes);
                     tma_load_2d(sa, &tmA, full, i * BK, a_row);
-                    if (second) tma_load_2d(sa + A_BYTES, &tmA, full, i * BK, a_row + BM);
-                    tma_load_2d(sa + QG::A_PART, &tmB, full, i * QC::CODE_ROW, b_lo);
-                    tma_load_2d(sa + QG::A_PART + QC::CODE_BOX, &tmB, full, i * QC::CODE_ROW, b_hi);
+                    tma_load_2d(sa + A_BYTES, &tmB, full, i * QC::CODE_ROW, b_lo);
+                    tma_load_2d(sa + A_BYTES + QC::CODE_BOX, &tmB, full, i * QC::CODE_ROW, b_hi);
                     if (FP4W) {     // the 16-byte group of block scales holding step i's four
                         tma_load_2d(sa + QG::S_PART, &tmS, full, (i * (BK / 16)) & ~15, b_lo);
                         tma_load_2d(sa + QG::S_PART + QC::SCALE_BOX, &tmS, full, (i * (BK / 16)) & ~15, b_hi);
@@ -1040,29 +1031,21 @@ grouped_gemm_q_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
             bool ok = true;
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
                 const Tile t = decode_tile<MODE == kGemmSwiGLU || MODE == kGemmReLU2>(tile, prefix, rstart, rcount, p,
-                                                                                     ntn, BMT);
-                const int rows0 = t.mrows - t.mt * BMT;                   // rows from the first half on
-                const bool second = HALVES == 2 && rows0 > BM;
-                const uint32_t idesc = rows0 <= kTailRows ? IDESC64 : IDESC;
-                const uint32_t idesc1 = rows0 - BM <= kTailRows ? IDESC64 : IDESC;
+                                                                                     ntn, BM);
+                const uint32_t idesc = t.mrows - t.mt * BM <= kTailRows ? IDESC64 : IDESC;
                 if (!mbar_wait_bounded(smem_u32(&ctl->tempty[acc]), aph ^ 1u, abort)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t d0 = tmem_base + (uint32_t)(acc * BN_MMA);   // half 1: the next 256 columns
+                const uint32_t d0 = tmem_base + (uint32_t)(acc * BN_MMA);
                 for (int i = 0; i < nk; ++i) {
                     if (!mbar_wait_bounded(smem_u32(&ctl->full[stage]), ph, abort) ||
                         !mbar_wait_bounded(smem_u32(&ctl->cfull[cs]), cph, abort)) { ok = false; break; }
                     tc_fence_after();
                     const uint64_t ad = sdesc_k_sw128(smem_base + stage * QG::STAGE_BYTES);
-                    const uint64_t ad1 = sdesc_k_sw128(smem_base + stage * QG::STAGE_BYTES + A_BYTES);
                     const uint64_t bd = sdesc_k_sw128(slot_base + cs * Q_SLOT_BYTES);
 #pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk) {
+                    for (int kk = 0; kk < BK / 16; ++kk)
                         tc_mma_bf16(d0, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc,
                                     (i > 0 || kk > 0) ? 1u : 0u);
-                        if (second)   // the same converted B tile for the second 128 rows
-                            tc_mma_bf16(d0 + (uint32_t)BN_MMA, ad1 + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2),
-                                        idesc1, (i > 0 || kk > 0) ? 1u : 0u);
-                    }
                     tc_commit(smem_u32(&ctl->empty[stage]));
                     tc_commit(smem_u32(&ctl->cempty[cs]));
                     if (++stage == QG::STAGES) { stage = 0; ph ^= 1u; }
@@ -1070,7 +1053,7 @@ grouped_gemm_q_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                 }
                 if (!ok) break;
                 tc_commit(smem_u32(&ctl->tfull[acc]));
-                if (++acc == QG::NUM_ACC) { acc = 0; aph ^= 1u; }
+                if (++acc == 2) { acc = 0; aph ^= 1u; }
             }
             tc_commit(smem_u32(&ctl->drain));
             volatile int never = 0;
@@ -1096,7 +1079,7 @@ grouped_gemm_q_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
             for (int i = 0; i < nk; ++i) {
                 if (!mbar_wait_bounded(smem_u32(&ctl->full[stage]), ph, abort) ||
                     !mbar_wait_bounded(smem_u32(&ctl->cempty[cs]), cph ^ 1u, abort)) { ok = false; break; }
-                const uint8_t* codes = smem + stage * QG::STAGE_BYTES + QG::A_PART;
+                const uint8_t* codes = smem + stage * QG::STAGE_BYTES + A_BYTES;
                 // NVFP4: this quarter's block scale of each pass, from the stage (0x100
                 // marks a block past K: zeros; rows past the weights arrive as scale 0)
                 uint32_t s_cur[4] = {0u, 0u, 0u, 0u};
@@ -1154,16 +1137,15 @@ grouped_gemm_q_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
             }
         }
     } else {
-        // ---------------- epilogue (warps 2..2+EPI_WARPS-1): scales, activation, BF16 stores ----------------
-        // warp w: TMEM lane quarter w % 4 (the warps a warp may read), half (w - 2) / 4
+        // ---------------- epilogue (warps 2..5): scales, activation, BF16 stores ----------------
+        // warp w: TMEM lane quarter w % 4 (the warps a warp may read)
         const int q = warp & 3;
-        const int hf = (warp - 2) >> 2;
         const float undo = FP4W ? 256.f : 1.f;
         int acc = 0;
         uint32_t aph = 0;
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
             const Tile t = decode_tile<MODE == kGemmSwiGLU || MODE == kGemmReLU2>(tile, prefix, rstart, rcount, p,
-                                                                                 ntn, BMT);
+                                                                                 ntn, BM);
             const int n0 = t.nt * BN_OUT;
             // the tile's 256 weight-row scales into this warp's shared slice while
             // the accumulator fills (SwiGLU: 128 gate rows, then the 128 up rows);
@@ -1185,13 +1167,13 @@ grouped_gemm_q_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                 break;
             }
             tc_fence_after();
-            const int hrow0 = t.mt * BMT + hf * BM;                    // this half's first row
-            const bool m64 = t.mrows - hrow0 <= kTailRows;
-            const int r = m64 ? hrow0 + q * 16 + lane : hrow0 + q * 32 + lane;
-            // an empty second half had no MMAs: its (stale) columns are loaded, not stored
-            const bool row_ok = hrow0 < t.mrows && (!m64 || lane < 16) && r < t.mrows;
+            // M = 64 tiles keep row 16q + i in lane 32q + i (i < 16)
+            const int row0 = t.mt * BM;
+            const bool m64 = t.mrows - row0 <= kTailRows;
+            const int r = m64 ? row0 + q * 16 + lane : row0 + q * 32 + lane;
+            const bool row_ok = (!m64 || lane < 16) && r < t.mrows;
             __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(out_row<MODE>(p, t.row0 + (row_ok ? r : 0), t.g));
-            const uint32_t tbase = tmem_base + (uint32_t)((acc + hf) * BN_MMA) + ((uint32_t)(q * 32) << 16);
+            const uint32_t tbase = tmem_base + (uint32_t)(acc * BN_MMA) + ((uint32_t)(q * 32) << 16);
             if (MODE == kGemmSwiGLU) {
 #pragma unroll 1
                 for (int c = 0; c < 4; ++c)
@@ -1206,7 +1188,7 @@ grouped_gemm_q_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[acc]));
-            if (++acc == QG::NUM_ACC) { acc = 0; aph ^= 1u; }
+            if (++acc == 2) { acc = 0; aph ^= 1u; }
         }
     }
 
@@ -1325,28 +1307,28 @@ cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const KPar
     return e;
 }
 
-template <int MODE, int WF, int HALVES>
+template <int MODE, int WF>
 cudaError_t launch_q(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& ms, const QParams& qp,
                      size_t smem, cudaStream_t st) {
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(grouped_gemm_q_kernel<MODE, WF, HALVES>,
+        attr_err = cudaFuncSetAttribute(grouped_gemm_q_kernel<MODE, WF>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, MAX_DYN_SMEM);
     });
     if (attr_err != cudaSuccess) {
         set_error("cudaFuncSetAttribute(max dynamic smem %d): %s", MAX_DYN_SMEM, cudaGetErrorString(attr_err));
         return attr_err;
     }
-    const cudaError_t e = launch_kernel(grouped_gemm_q_kernel<MODE, WF, HALVES>, dim3((unsigned)device_sm_count()),
-                                        dim3(QGeo<WF, HALVES>::THREADS), smem, st, 1, kUsePdl, ma, mb, ms, qp);
+    const cudaError_t e = launch_kernel(grouped_gemm_q_kernel<MODE, WF>, dim3((unsigned)device_sm_count()),
+                                        dim3(QGeo<WF>::THREADS), smem, st, 1, kUsePdl, ma, mb, ms, qp);
     if (e != cudaSuccess) set_error("quantized grouped GEMM launch (smem %zu): %s", smem, cudaGetErrorString(e));
     return e;
 }
 
-template <int WF, int HALVES>
+template <int WF>
 size_t q_smem_bytes(int groups) {
-    return 1024 + (size_t)QGeo<WF, HALVES>::STAGES * QGeo<WF, HALVES>::STAGE_BYTES + (size_t)Q_CSLOTS * Q_SLOT_BYTES +
+    return 1024 + (size_t)QGeo<WF>::STAGES * QGeo<WF>::STAGE_BYTES + (size_t)Q_CSLOTS * Q_SLOT_BYTES +
            sizeof(QCtl) +
            3 * (size_t)(groups + 1) * 4;
 }
@@ -1481,13 +1463,7 @@ moe_status launch_grouped_gemm(const GemmProblem& g, WsHeader* hdr, cudaStream_t
             set_error("grouped GEMM: quantized weights need a scale per weight row");
             return MOE_ERR_UNSUPPORTED;
         }
-        // NVFP4 groups of more than 96 rows on average: 256-row tiles (its converter
-        // is the dearer one, and groups of 129..256 rows then convert each weight
-        // tile once instead of twice)
-        const long long avg_rows = g.offsets ? g.a_rows / g.groups : g.rows_all;
-        const bool two = fp4 && avg_rows > 96 && q_smem_bytes<kWeightNvfp4, 2>(g.groups) <= (size_t)MAX_DYN_SMEM;
-        const size_t smem = fp4 ? (two ? q_smem_bytes<kWeightNvfp4, 2>(g.groups) : q_smem_bytes<kWeightNvfp4, 1>(g.groups))
-                                : q_smem_bytes<kWeightFp8E4M3, 1>(g.groups);
+        const size_t smem = fp4 ? q_smem_bytes<kWeightNvfp4>(g.groups) : q_smem_bytes<kWeightFp8E4M3>(g.groups);
         if (smem > (size_t)MAX_DYN_SMEM) {
             set_error("quantized grouped GEMM needs %zu bytes of shared memory", smem);
             return MOE_ERR_UNSUPPORTED;
@@ -1522,23 +1498,17 @@ moe_status launch_grouped_gemm(const GemmProblem& g, WsHeader* hdr, cudaStream_t
         qp.k.gated = g.gated;
         qp.wscale = g.wscale;
         cudaError_t e;
-        if (fp4 && two) {
+        if (fp4) {
             switch (g.mode) {
-                case kGemmSwiGLU: e = launch_q<kGemmSwiGLU, kWeightNvfp4, 2>(ma, mb, ms, qp, smem, st); break;
-                case kGemmReLU2: e = launch_q<kGemmReLU2, kWeightNvfp4, 2>(ma, mb, ms, qp, smem, st); break;
-                default: e = launch_q<kGemmPlain, kWeightNvfp4, 2>(ma, mb, ms, qp, smem, st); break;
-            }
-        } else if (fp4) {
-            switch (g.mode) {
-                case kGemmSwiGLU: e = launch_q<kGemmSwiGLU, kWeightNvfp4, 1>(ma, mb, ms, qp, smem, st); break;
-                case kGemmReLU2: e = launch_q<kGemmReLU2, kWeightNvfp4, 1>(ma, mb, ms, qp, smem, st); break;
-                default: e = launch_q<kGemmPlain, kWeightNvfp4, 1>(ma, mb, ms, qp, smem, st); break;
+                case kGemmSwiGLU: e = launch_q<kGemmSwiGLU, kWeightNvfp4>(ma, mb, ms, qp, smem, st); break;
+                case kGemmReLU2: e = launch_q<kGemmReLU2, kWeightNvfp4>(ma, mb, ms, qp, smem, st); break;
+                default: e = launch_q<kGemmPlain, kWeightNvfp4>(ma, mb, ms, qp, smem, st); break;
             }
         } else {
             switch (g.mode) {
-                case kGemmSwiGLU: e = launch_q<kGemmSwiGLU, kWeightFp8E4M3, 1>(ma, mb, ms, qp, smem, st); break;
-                case kGemmReLU2: e = launch_q<kGemmReLU2, kWeightFp8E4M3, 1>(ma, mb, ms, qp, smem, st); break;
-                default: e = launch_q<kGemmPlain, kWeightFp8E4M3, 1>(ma, mb, ms, qp, smem, st); break;
+                case kGemmSwiGLU: e = launch_q<kGemmSwiGLU, kWeightFp8E4M3>(ma, mb, ms, qp, smem, st); break;
+                case kGemmReLU2: e = launch_q<kGemmReLU2, kWeightFp8E4M3>(ma, mb, ms, qp, smem, st); break;
+                default: e = launch_q<kGemmPlain, kWeightFp8E4M3>(ma, mb, ms, qp, smem, st); break;
             }
         }
         return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;

@@ -30,10 +30,10 @@ CASES = {
     "relu2_t300": synth.Workload("relu2_t300", 300, 1024, 16, 4, 1536, act=synth.ACT_RELU2),   # 75 rows
     "ragged_n_k": synth.Workload("ragged_n_k", 150, 288, 5, 2, 224),              # N and K tails
     "one_big_group": synth.Workload("one_big_group", 700, 256, 2, 1, 192, act=synth.ACT_RELU2),  # 350 rows
-    # more than 96 rows per group on average: NVFP4 takes 256-row tiles whose second
-    # half is empty, partial (64 rows or fewer: M = 64) or full; ragged N and K
-    "halves_mix": synth.Workload("halves_mix", 400, 256, 6, 2, 192),               # ~133 rows per group
-    "halves_relu2": synth.Workload("halves_relu2", 500, 320, 4, 1, 224, act=synth.ACT_RELU2),   # ~125 rows
+    # groups of 100-160 rows: a full 128-row tile and a tail of up to 64 rows (M = 64)
+    # or more (M = 128) per group; ragged N and K
+    "tails_mix": synth.Workload("tails_mix", 400, 256, 6, 2, 192),                 # ~133 rows per group
+    "tails_relu2": synth.Workload("tails_relu2", 500, 320, 4, 1, 224, act=synth.ACT_RELU2),     # ~125 rows
 }
 FULL = {
     "count_first": W["count_first"],
