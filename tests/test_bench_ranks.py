@@ -62,3 +62,27 @@ def test_reference_arm_other_ranks_exit_without_work():
     from mixture_experts_routing_router_gb300 import synth
     args = argparse.Namespace(gpus=2, steps=3, warmup=3)
     assert bench.run_reference(args, synth.WORKLOADS["large"], world=2, rank=1) == 0
+
+
+def test_reference_arm_line_on_rank0(capsys):
+    """Rank 0 of the reference arm times the oracle on a bounded sample and
+    prints one JSON line with the contract's keys: its own value as the
+    end-to-end figure (no host-device copies) and a cpu_baseline that names
+    the host."""
+    sys.path.insert(0, ROOT)
+    import argparse
+    import json
+
+    import bench
+    from mixture_experts_routing_router_gb300 import synth
+    args = argparse.Namespace(gpus=1, steps=2, warmup=1)
+    assert bench.run_reference(args, synth.WORKLOADS["tiny"], world=1, rank=0) == 0
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC
+    assert line["unit"] == "tokens/s" and line["value"] > 0 and line["higher_is_better"] is True
+    assert line["steps"] == 2 and line["warmup"] == 1 and line["dtype"] == "f64"
+    assert line["e2e"] == {"value": line["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == line["value"] and cb["cores"] >= 1
+    assert "nproc" in cb and "cpu_model" in cb and cb["sample"]
