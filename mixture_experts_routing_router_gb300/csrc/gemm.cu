@@ -820,7 +820,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
 // the epilogue (NVFP4 tiles are converted at 2^-8 of their value and undone there).
 // A ring stage is released by the converters (codes read) and the MMA (A read).
 // ---------------------------------------------------------------------------
-constexpr int Q_STAGES = 4;                               // the most any geometry uses
+constexpr int Q_STAGES = 5;                               // the most any geometry uses
 constexpr int Q_CSLOTS = 2;
 constexpr int Q_CONV_WARPS = 8;
 constexpr int Q_SLOT_BYTES = B_BYTES;                     // 256 rows x 64 BF16, 128-byte swizzled
@@ -833,14 +833,14 @@ struct QCfg {
     // K step's four), one box per 128 rows
     static constexpr int SCALE_BOX = WF == kWeightNvfp4 ? 128 * 16 : 0;
 };
-// Tile geometry: 128 activation rows per tile, four TMA stages, two converted B
-// tiles, double-buffered accumulators; warps: producer, MMA, four epilogue
-// warps, eight converter warps.
+// Tile geometry: 128 activation rows per tile, a ring of QParams::stages TMA
+// stages (four, or five of the smaller NVFP4 stages where they fit), two
+// converted B tiles, double-buffered accumulators; warps: producer, MMA, four
+// epilogue warps, eight converter warps.
 template <int WF>
 struct QGeo {
     static constexpr int S_PART = A_BYTES + 2 * QCfg<WF>::CODE_BOX;        // NVFP4 block-scale boxes
     static constexpr int STAGE_BYTES = S_PART + 2 * QCfg<WF>::SCALE_BOX;
-    static constexpr int STAGES = 4;
     static constexpr int CONV_W0 = 6;                                     // first converter warp
     static constexpr int THREADS = 32 * CONV_W0 + 32 * Q_CONV_WARPS;
 };
@@ -848,6 +848,7 @@ struct QGeo {
 struct QParams {
     KParams k;
     const float* wscale;        // FP32 scale per weight row
+    int stages;                 // TMA ring stages (at most Q_STAGES)
 };
 
 struct QCtl {
@@ -914,7 +915,8 @@ grouped_gemm_q_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + ((1024u - (raw_u32 & 1023u)) & 1023u);
-    uint8_t* slots = smem + QG::STAGES * QG::STAGE_BYTES;   // converted B tiles
+    const int nst = qp.stages;
+    uint8_t* slots = smem + nst * QG::STAGE_BYTES;          // converted B tiles
     QCtl* ctl = reinterpret_cast<QCtl*>(slots + Q_CSLOTS * Q_SLOT_BYTES);
     int* prefix = reinterpret_cast<int*>(ctl + 1);
     int* rstart = prefix + (p.groups + 1);
@@ -925,7 +927,7 @@ grouped_gemm_q_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
     const int ntn = (p.N + BN_OUT - 1) / BN_OUT;
 
     if (tid == 0) {
-        for (int s = 0; s < QG::STAGES; ++s) {
+        for (int s = 0; s < nst; ++s) {
             mbar_init(smem_u32(&ctl->full[s]), 1);
             mbar_init(smem_u32(&ctl->empty[s]), 1 + Q_CONV_WARPS);      // MMA commit + converter warps
         }
@@ -1013,12 +1015,12 @@ grouped_gemm_q_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                         tma_load_2d(sa + QG::S_PART + QC::SCALE_BOX, &tmS, full, (i * (BK / 16)) & ~15, b_hi);
                     }
                     ++armed;
-                    if (++stage == QG::STAGES) { stage = 0; ph ^= 1u; }
+                    if (++stage == nst) { stage = 0; ph ^= 1u; }
                 }
             }
             if (!ok) {
                 // let the copies already issued land before the CTA exits
-                if (!wait_armed_stages(smem_u32(&ctl->full[0]), QG::STAGES, armed)) settle_delay();
+                if (!wait_armed_stages(smem_u32(&ctl->full[0]), nst, armed)) settle_delay();
                 raise_status(p.hdr, MOE_ERR_TIMEOUT);
                 p.hdr->timeout_site = kSiteGemmProducer;
             }
@@ -1048,7 +1050,7 @@ grouped_gemm_q_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                                     (i > 0 || kk > 0) ? 1u : 0u);
                     tc_commit(smem_u32(&ctl->empty[stage]));
                     tc_commit(smem_u32(&ctl->cempty[cs]));
-                    if (++stage == QG::STAGES) { stage = 0; ph ^= 1u; }
+                    if (++stage == nst) { stage = 0; ph ^= 1u; }
                     if (++cs == Q_CSLOTS) { cs = 0; cph ^= 1u; }
                 }
                 if (!ok) break;
@@ -1132,7 +1134,7 @@ grouped_gemm_q_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                     mbar_arrive(smem_u32(&ctl->cfull[cs]));
                     mbar_arrive(smem_u32(&ctl->empty[stage]));
                 }
-                if (++stage == QG::STAGES) { stage = 0; ph ^= 1u; }
+                if (++stage == nst) { stage = 0; ph ^= 1u; }
                 if (++cs == Q_CSLOTS) { cs = 0; cph ^= 1u; }
             }
         }
@@ -1327,8 +1329,8 @@ cudaError_t launch_q(const CUtensorMap& ma, const CUtensorMap& mb, const CUtenso
 }
 
 template <int WF>
-size_t q_smem_bytes(int groups) {
-    return 1024 + (size_t)QGeo<WF>::STAGES * QGeo<WF>::STAGE_BYTES + (size_t)Q_CSLOTS * Q_SLOT_BYTES +
+size_t q_smem_bytes(int groups, int stages) {
+    return 1024 + (size_t)stages * QGeo<WF>::STAGE_BYTES + (size_t)Q_CSLOTS * Q_SLOT_BYTES +
            sizeof(QCtl) +
            3 * (size_t)(groups + 1) * 4;
 }
@@ -1463,7 +1465,9 @@ moe_status launch_grouped_gemm(const GemmProblem& g, WsHeader* hdr, cudaStream_t
             set_error("grouped GEMM: quantized weights need a scale per weight row");
             return MOE_ERR_UNSUPPORTED;
         }
-        const size_t smem = fp4 ? q_smem_bytes<kWeightNvfp4>(g.groups) : q_smem_bytes<kWeightFp8E4M3>(g.groups);
+        // five of the smaller NVFP4 stages where the group list leaves room, else four
+        const int qst = fp4 && q_smem_bytes<kWeightNvfp4>(g.groups, Q_STAGES) <= (size_t)MAX_DYN_SMEM ? Q_STAGES : 4;
+        const size_t smem = fp4 ? q_smem_bytes<kWeightNvfp4>(g.groups, qst) : q_smem_bytes<kWeightFp8E4M3>(g.groups, qst);
         if (smem > (size_t)MAX_DYN_SMEM) {
             set_error("quantized grouped GEMM needs %zu bytes of shared memory", smem);
             return MOE_ERR_UNSUPPORTED;
@@ -1497,6 +1501,7 @@ moe_status launch_grouped_gemm(const GemmProblem& g, WsHeader* hdr, cudaStream_t
         qp.k.hdr = hdr;
         qp.k.gated = g.gated;
         qp.wscale = g.wscale;
+        qp.stages = qst;
         cudaError_t e;
         if (fp4) {
             switch (g.mode) {
